@@ -1,0 +1,476 @@
+#!/usr/bin/env python
+"""Benchmark of the MoeReRoutingV2 re-routing step on GB300.
+
+One step = one mrr_v2_run call over one batch: the whole hot path (count validation, both
+offset scans, expert_token_num, the token / scale / top-k moves and the index) for the
+workload A=16384, H=7168 int8 tokens, N=16 ranks x E=16 experts with the skewed count matrix
+of the torch_npu.npu_moe_re_routing usage example (one cell holds 16129 of the 16384 rows),
+fp32 per-token scales [A], no top-k weights, idx_type 0.
+
+Prints ONE JSON line.  ``value`` is effective HBM GB/s: the algorithmic bytes (every input
+byte read once, every output byte written once) per step over the device time per step, with
+inputs resident in HBM.  Consecutive steps rotate over buffer sets whose combined footprint is
+several times the L2 size, so no step reads what an earlier step left in L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--impl gb300|reference]
+
+--impl reference times the CPU oracle (a plain loop restatement of the op, single-threaded)
+on the same workload: each step is a bounded row sample of it, so the run ends in minutes.
+Multi-GPU (torchrun, one rank per GPU) runs independent replicas: the op has no exchange step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "effective HBM GB/s (read+write) and % of GB300 peak; tokens/sec at A=16384,H=7168"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", type=int, default=2, help="workload 1..5 (2 is the headline)")
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU oracle baseline budget (seconds of oracle work)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The maximum of ``value`` over all ranks (the slowest rank sets the job's time)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput_gbs(world: int, bytes_per_step: int, steps: int, elapsed_ms: float) -> float:
+    """Whole-job GB/s: every rank moved ``bytes_per_step`` per step; time is the max over ranks."""
+    return world * bytes_per_step * steps / (elapsed_ms * 1e-3) / 1e9
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in ("moe_expert_token_gb300/csrc/mrr_v2.cu", "moe_expert_token_gb300/csrc/ptx.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config: int):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
+    path = os.path.join(ROOT, "profiles", f"reroute_kernel_C{config}.md")
+    try:
+        text = open(path, encoding="utf-8").read()
+    except OSError:
+        return None
+    src = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    if not src or not tr or src.group(1) != kernel_source_hash():
+        return None
+    return int(tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples, taken while the timed region runs."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.rows = []
+        self.proc = None
+        self.t_start = self.t_end = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.dev)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi gave no samples"}
+        lo, hi = self.t_start - 0.05, self.t_end + 0.05
+        win = [r for t, r in self.rows if lo <= t <= hi]
+        window = "timed"
+        if len(win) < 3:          # a short timed region: fall back to the whole run
+            win = [r for _, r in self.rows]
+            window = "run (timed region shorter than the sampling period)"
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], [], set()
+        for r in win:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for k, n in enumerate(names):
+                if len(r) > 5 + k and r[5 + k].lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(win), "window": window}
+
+
+# ----------------------------------------------------------------------------- sampling for the CPU legs
+
+def row_sample(p, frac: float):
+    """A smaller problem of the same kind: the first A' rows, counts scaled to sum to A'."""
+    import numpy as np
+
+    if frac >= 1.0:
+        return p
+    N, E = p.counts.shape
+    A2 = max(N * E, int(p.A * frac))
+    c = p.counts.astype(np.int64)
+    extra = (c - 1) * (A2 - N * E) // max(1, p.A - N * E)
+    c2 = 1 + extra
+    c2.flat[int(np.argmax(c2))] += A2 - int(c2.sum())
+    import copy
+
+    q = copy.copy(p)
+    q.A = A2
+    q.counts = c2.astype(p.counts.dtype)
+    q.tokens = p.tokens[:A2]
+    q.scales = None if p.scales is None else p.scales[:A2]
+    q.topk = None if p.topk is None else p.topk[:A2]
+    return q
+
+
+def time_oracle(p, budget_s: float, max_reps: int = 1000):
+    """Run the oracle on ``p`` repeatedly for about ``budget_s`` seconds; (GB/s, reps, s)."""
+    import oracle
+
+    lib = oracle.load()
+    oracle.run_problem(p, lib=lib)  # warm (page in the library and the inputs)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.run_problem(p, lib=lib)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= max_reps:
+            break
+    return p.algorithmic_bytes() * reps / el / 1e9, reps, el
+
+
+def config_dict(p, k, extra=None):
+    d = {"workload": p.name, "A": p.A, "H": p.H, "N": p.N, "E": p.E, "token_dtype": p.token_dtype,
+         "count_dtype": str(p.counts.dtype), "scales": p.scale_layout, "scale_cols": p.scale_cols,
+         "topk": p.topk is not None, "idx_type": p.idx_type, "expert_token_num_type": 1,
+         "bytes_per_step": p.algorithmic_bytes()}
+    d.update(extra or {})
+    return d
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    import workloads
+
+    p = workloads.config(args.config)
+    # size each step so that warmup + steps take about two minutes of oracle work at most
+    t_full = time.perf_counter()
+    import oracle
+
+    oracle.run_problem(p)
+    t_full = time.perf_counter() - t_full
+    frac = min(1.0, 120.0 / max(1e-9, t_full * (args.steps + args.warmup)))
+    q = row_sample(p, frac)
+    lib = oracle.load()
+    for _ in range(args.warmup):
+        oracle.run_problem(q, lib=lib)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.run_problem(q, lib=lib)
+    el = time.perf_counter() - t0
+    value = q.algorithmic_bytes() * args.steps / el / 1e9
+    sample = f"first {q.A} of {p.A} rows per step (counts scaled to sum to {q.A})"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic", "config": config_dict(p, args.config, {"sample_rows": q.A}),
+        "tokens_per_s": q.A * args.steps / el,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import workloads
+    from moe_expert_token_gb300 import build as mbuild
+    import moe_expert_token_gb300.mrr_v2 as m
+
+    rank, local_rank, world = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0:
+        mbuild.build()
+    if dist is not None:
+        dist.barrier()
+    m.load_library()
+
+    p = workloads.config(args.config)
+    code = m.DTYPE_CODES[p.token_dtype]
+    sl = m.SCALE_CODES[p.scale_layout]
+    A, H, N, E = p.A, p.H, p.N, p.E
+    i64 = p.counts.dtype == np.int64
+    st, plan = m.mrr_v2_plan(A, H, code, N, E, i64, sl, p.scale_cols, p.topk is not None, 1,
+                             p.idx_type, local_rank)
+    if st != m.MRR_OK:
+        raise SystemExit(m.mrr_status_str(st))
+    launches_per_step = 1 if plan.fuse_scan else 2
+    bytes_step = p.algorithmic_bytes()
+
+    def dev_bytes(arr):
+        if arr is None:
+            return None
+        return torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8).reshape(-1).copy()).to(dev)
+
+    # buffer sets: enough that consecutive steps never hit in L2
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    footprint = bytes_step
+    R = max(2, -(-4 * l2 // footprint))
+    host_in = {"tokens": p.tokens, "counts": p.counts, "scales": p.scales, "topk": p.topk}
+    sets = []
+    for _ in range(R):
+        s = {k: dev_bytes(v) for k, v in host_in.items()}
+        s["out_tokens"] = torch.empty(A * p.row_bytes, dtype=torch.uint8, device=dev)
+        s["out_scales"] = (None if p.scales is None
+                           else torch.empty(A * p.scale_row_bytes, dtype=torch.uint8, device=dev))
+        s["out_topk"] = None if p.topk is None else torch.empty(4 * A, dtype=torch.uint8, device=dev)
+        s["idx"] = torch.empty(A, dtype=torch.int32, device=dev)
+        s["etn"] = torch.empty(E * p.counts.dtype.itemsize, dtype=torch.uint8, device=dev)
+        s["ws"] = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+        sets.append(s)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+
+    def P(t):
+        return None if t is None else t.data_ptr()
+
+    def step(s):
+        st = m.mrr_v2_run(P(s["tokens"]), code, A, H, P(s["counts"]), i64, N, E, P(s["scales"]), sl,
+                          p.scale_cols, P(s["topk"]), P(s["out_tokens"]), P(s["out_scales"]),
+                          P(s["idx"]), P(s["etn"]), P(s["out_topk"]), 1, p.idx_type, P(s["ws"]),
+                          s["ws"].numel(), sp)
+        if st != m.MRR_OK:
+            raise RuntimeError(m.mrr_status_str(st))
+
+    # untimed correctness gate on every buffer set: device status and a permutation check
+    for s in sets:
+        step(s)
+        st = m.mrr_v2_read_status(P(s["ws"]), s["ws"].numel(), sp)
+        if st != m.MRR_OK:
+            raise RuntimeError(m.mrr_status_str(st))
+    idx_sorted = torch.sort(sets[0]["idx"].to(torch.int64)).values
+    assert torch.equal(idx_sorted, torch.arange(A, device=dev)), "index is not a permutation"
+
+    for k in range(args.warmup):
+        step(sets[k % R])
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.t_start = time.time()
+    t_begin.record(stream)
+    for k in range(K):
+        ev[k][0].record(stream)
+        step(sets[k % R])
+        ev[k][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.t_end = time.time()
+    if dist is not None:
+        dist.barrier()
+    time.sleep(0.2)
+    clocks.stop()
+    elapsed_ms = t_begin.elapsed_time(t_end)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
+    value = throughput_gbs(world, bytes_step, K, elapsed_ms)
+    ms_per_step = elapsed_ms / K
+    mean_launch_ms = sum(launch_ms) / K
+    achieved = bytes_step / (mean_launch_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+
+    # end to end through the C ABI from pinned host buffers: H2D inputs, run, D2H outputs
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, p, sets[0], step, dev, stream, bytes_step, world, dist)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, reps, el = time_oracle(p, args.cpu_seconds)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"the full workload, {reps} runs in {el:.1f} s, single thread"}
+
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic (seeded numpy draws shaped like the pages' workload)",
+        "config": config_dict(p, args.config, {
+            "l2": f"{R} rotating buffer sets, {R * footprint / 1e6:.0f} MB > 4x L2 ({l2 / 1e6:.0f} MB)",
+            "path": {1: "bulk", 2: "vector"}[plan.path], "grid": plan.grid, "block": plan.block,
+            "chunk_bytes": plan.chunk_bytes, "stages": plan.stages, "fused_scan": bool(plan.fuse_scan),
+            "parallelism": f"replicas x{world}"}),
+        "pct_of_peak": 100.0 * value / world / peak,
+        "tokens_per_s": world * A * K / (elapsed_ms * 1e-3),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind,
+                     "traffic": profiled_traffic(args.config),
+                     "kernel": "mrr::reroute_kernel", "bytes_per_launch": bytes_step,
+                     "mean_launch_us": mean_launch_ms * 1e3},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": K * launches_per_step,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, p, s, step, dev, stream, bytes_step, world, dist):
+    import numpy as np
+    import torch
+
+    def pinned(arr):
+        if arr is None:
+            return None
+        t = torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8).reshape(-1).copy())
+        return t.pin_memory()
+
+    h_in = {"tokens": pinned(p.tokens), "counts": pinned(p.counts), "scales": pinned(p.scales),
+            "topk": pinned(p.topk)}
+    outs = ["out_tokens", "out_scales", "out_topk", "idx", "etn"]
+    h_out = {k: (None if s[k] is None else torch.empty(s[k].numel() * s[k].element_size(),
+                                                        dtype=torch.uint8).pin_memory())
+             for k in outs}
+    h2d = sum(t.numel() for t in h_in.values() if t is not None)
+    d2h = sum(t.numel() for t in h_out.values() if t is not None)
+
+    def e2e_step():
+        for k, t in h_in.items():
+            if t is not None:
+                s[k].copy_(t, non_blocking=True)
+        step(s)
+        for k in outs:
+            if s[k] is not None:
+                h_out[k].copy_(s[k].view(torch.uint8).reshape(-1), non_blocking=True)
+
+    K = max(3, min(args.steps, 200))
+    for _ in range(3):
+        e2e_step()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(K):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(a.elapsed_time(b), dist, dev)
+    return {"value": throughput_gbs(world, bytes_step, K, ms), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
+            "ms_per_step": ms / K}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,190 @@
+/*
+ * mrr_v2.h -- C ABI of the GB300 (sm_103a) MoE re-routing library.
+ *
+ * The op (MoeReRoutingV2) runs after the expert-parallel AlltoAll.  The A token rows a GPU
+ * received arrive rank-major: one contiguous segment per (source rank i, expert j), sized by
+ * the count matrix counts[N,E].  The op lays them out expert-major, moves the per-token scales
+ * and top-k weights with them, and emits the permutation index and the per-expert counts.
+ *
+ * Definition (the "CANN ops-transformer MoeReRoutingV2" article, m.nlpx.cn/news/59074):
+ *   - section 计算公式: segment (i,j) moves from SrcOffset(i,j) to DstOffset(i,j), where
+ *     SrcOffset is the sum of all counts before (i,j) walking rank-outer (row-major) and
+ *     DstOffset the sum of all counts before (i,j) walking expert-outer (column-major);
+ *     permute_tokens[Dst+k] = tokens[Src+k], and the same for per_token_scales and
+ *     expert_topk_weight, 0 <= k < counts[i,j].
+ *   - section 参数说明 (parameter table) and 参数取值细节: input/output shapes and dtypes,
+ *     idx_type 0 = gather index (permute_token_idx[d] = s), 1 = scatter index
+ *     (permute_token_idx[s] = d); expert_token_num_type 1 = per-expert count.
+ *   - section 约束说明 (constraints): Sum(counts) = A, 0 < H < 16384, every count > 0,
+ *     only expert_token_num_type = 1 is supported.
+ *   - section 算子 IR 原型: permute_token_idx is INT32; attribute defaults
+ *     expert_token_num_type = 1, idx_type = 0.
+ *   - section InferShape 与 InferDtype: output shapes/dtypes follow the inputs; absent scales
+ *     give a meaningless [A] float32 output, absent top-k weights an empty output.
+ *
+ * Conventions for every entry point:
+ *   - All buffer pointers are DEVICE pointers unless stated otherwise.  The caller owns every
+ *     buffer, including the workspace.  The library allocates no device memory.
+ *   - Payload rows are moved as raw bytes: nothing is converted, so every output is
+ *     bit-identical to its input row (NaN payloads, fp8/e8m0/hifloat8/fp4 codes included).
+ *   - Inputs and outputs must not overlap.
+ *   - mrr_v2_run / mrr_v2_run_plan only enqueue work on `stream` and return after host-side
+ *     validation.  Errors found on the host are returned at once and nothing is enqueued.
+ *     Errors that depend on the count VALUES (a count <= 0, Sum != A) are found on the GPU:
+ *     the outputs are then left unspecified and mrr_v2_read_status reports the error.
+ *   - Calls on different streams must use different workspaces.
+ */
+#ifndef MRR_V2_H
+#define MRR_V2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle: the same type as cudaStream_t.  NULL is the legacy default stream. */
+typedef struct CUstream_st *mrr_stream_t;
+
+typedef enum mrr_status {
+    MRR_OK = 0,
+    MRR_ERR_NULL = 1,          /* a required pointer is NULL                                   */
+    MRR_ERR_SHAPE = 2,         /* A, H, N, E, scale_cols out of range (see mrr_v2_plan)         */
+    MRR_ERR_DTYPE = 3,         /* unknown token dtype or scale layout code                     */
+    MRR_ERR_ATTR = 4,          /* expert_token_num_type or idx_type not in {0, 1}              */
+    MRR_ERR_UNSUPPORTED = 5,   /* expert_token_num_type = 0 (cumsum mode; pages: unsupported)  */
+    MRR_ERR_TOPK_PAIR = 6,     /* exactly one of expert_topk_weight / permute_topk_weight given */
+    MRR_ERR_WORKSPACE = 7,     /* workspace NULL, misaligned or smaller than workspace_bytes   */
+    MRR_ERR_CUDA = 8,          /* a CUDA runtime call failed (no device, launch error, ...)    */
+    MRR_ERR_ALIGN = 9,         /* counts / index / expert_token_num pointer not aligned to its type */
+    MRR_ERR_PLAN = 10,         /* a plan passed to mrr_v2_run_plan is inconsistent             */
+    /* found on the GPU; reported by mrr_v2_read_status */
+    MRR_ERR_COUNT_NONPOS = 16, /* some counts[i,j] <= 0                                        */
+    MRR_ERR_COUNT_SUM = 17,    /* Sum(counts) != A (or a single count > A)                     */
+    MRR_ERR_TIMEOUT = 18       /* a bounded wait inside the copy kernel gave up                */
+} mrr_status;
+
+/* Token element types (section 参数说明).  Only the width matters: rows move as bytes.
+ * FP4 types are packed two per byte, so H must be even for them (row bytes = H / 2). */
+typedef enum mrr_token_dtype {
+    MRR_F16 = 0,      /* 16 bit */
+    MRR_BF16 = 1,     /* 16 bit */
+    MRR_I8 = 2,       /*  8 bit */
+    MRR_F8E5M2 = 3,   /*  8 bit */
+    MRR_F8E4M3FN = 4, /*  8 bit */
+    MRR_HIF8 = 5,     /*  8 bit */
+    MRR_F4E2M1 = 6,   /*  4 bit */
+    MRR_F4E1M2 = 7    /*  4 bit */
+} mrr_token_dtype;
+
+/* per_token_scales layouts (section 参数说明).  scale_cols = elements per scale row. */
+typedef enum mrr_scale_layout {
+    MRR_SCALE_NONE = 0,     /* no scales; scale_cols ignored; permute_scales not written     */
+    MRR_SCALE_F32_A = 1,    /* [A] float32;            scale_cols must be 1                  */
+    MRR_SCALE_F32_AS = 2,   /* [A, S] float32;         scale_cols = S >= 1                   */
+    MRR_SCALE_E8M0_AK2 = 3  /* [A, K/64, 2] e8m0 bytes; scale_cols = (K/64)*2, even, >= 2    */
+} mrr_scale_layout;
+
+/* copy paths of the token move */
+#define MRR_PATH_AUTO 0    /* run picks: BULK when rows and base pointers are 16-byte aligned */
+#define MRR_PATH_BULK 1    /* cp.async.bulk global->shared->global, one driver thread per CTA  */
+#define MRR_PATH_VECTOR 2  /* all threads, widest aligned vector loads/stores (any alignment) */
+
+/* Launch plan: plain data, owned by the caller.  mrr_v2_plan fills it; a caller may change the
+ * tuning fields (path, grid, block, chunk_bytes, stages) and pass it to mrr_v2_run_plan, which
+ * checks them again. */
+typedef struct mrr_v2_plan {
+    int64_t A, H, N, E;
+    int64_t row_bytes;        /* bytes per token row: H * bits / 8                          */
+    int64_t scale_row_bytes;  /* bytes per scale row; 0 without scales                      */
+    int64_t workspace_bytes;  /* device scratch mrr_v2_run needs (>= 4096: status region)   */
+    int32_t count_is_i64;
+    int32_t scale_layout;
+    int32_t has_topk;
+    int32_t idx_type;
+    int32_t fuse_scan;        /* 1: every CTA scans the counts itself (N*E <= 4096)
+                                 0: a one-CTA scan kernel writes the offsets to the workspace */
+    int32_t path;             /* MRR_PATH_*                                                  */
+    int32_t grid;             /* CTAs of the copy kernel (<= 1022)                            */
+    int32_t block;            /* threads per CTA (multiple of 32, 64..1024)                   */
+    int32_t chunk_bytes;      /* bulk path: bytes per pipeline stage (multiple of 16)         */
+    int32_t stages;           /* bulk path: pipeline depth (1..8)                             */
+    int32_t smem_bytes;       /* dynamic shared memory per CTA                                */
+    int32_t num_sms;          /* SMs on the device the plan was made for                      */
+} mrr_v2_plan_t;
+
+/*
+ * mrr_v2_plan -- host only, enqueues nothing, allocates nothing.
+ *   Validates the shape/attribute arguments (the same checks mrr_v2_run makes, except for
+ *   pointers) and fills *out with the launch plan and the workspace size for `device`.
+ *   A: rows (0 <= A <= INT32_MAX; A = 0 only with N*E = 0, the empty problem);
+ *   H: elements per token row, 0 < H < 16384, even for FP4 dtypes;
+ *   N, E: count-matrix rows (ranks) and columns (experts), >= 0;
+ *   count_is_i64: counts are int64 (1) or int32 (0); expert_token_num has the same type;
+ *   sl, scale_cols: the scale layout and elements per scale row (see mrr_scale_layout);
+ *   has_topk: expert_topk_weight / permute_topk_weight given;
+ *   expert_token_num_type must be 1 (0 -> MRR_ERR_UNSUPPORTED); idx_type 0 or 1.
+ *   Returns MRR_ERR_CUDA when the device cannot be queried (e.g. no GPU).
+ */
+mrr_status mrr_v2_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int64_t E,
+                       int count_is_i64, mrr_scale_layout sl, int64_t scale_cols, int has_topk,
+                       int64_t expert_token_num_type, int64_t idx_type, int device,
+                       mrr_v2_plan_t *out);
+
+/*
+ * mrr_v2_run -- enqueue one re-routing on `stream` (current device).
+ *   tokens          [A, H] dt, row-major, rank-major segments            (read)
+ *   counts          [N, E] int32 or int64 (count_is_i64), row = rank      (read)
+ *   scales          per the layout, or NULL with MRR_SCALE_NONE          (read)
+ *   topk_w          [A, 1] float32, or NULL                              (read)
+ *   permute_tokens  [A, H] dt                                            (written)
+ *   permute_scales  same shape as scales; may be NULL without scales     (written if scales)
+ *   permute_token_idx [A] int32, gather (idx_type 0) or scatter (1) index (written)
+ *   expert_token_num  [E] counts' type, tokens per expert                (written)
+ *   permute_topk_w  [A, 1] float32; NULL exactly when topk_w is NULL     (written if given)
+ *   workspace       >= plan.workspace_bytes device bytes, 256-byte aligned, caller-owned;
+ *                   it holds the status words read by mrr_v2_read_status and, for
+ *                   N*E > 4096, the scanned offsets.
+ * Host-side errors return before anything is enqueued.  The empty problem (N*E = 0, A = 0)
+ * only zero-fills expert_token_num.
+ */
+mrr_status mrr_v2_run(const void *tokens, mrr_token_dtype dt, int64_t A, int64_t H,
+                      const void *counts, int count_is_i64, int64_t N, int64_t E,
+                      const void *scales, mrr_scale_layout sl, int64_t scale_cols,
+                      const float *topk_w,
+                      void *permute_tokens, void *permute_scales, int32_t *permute_token_idx,
+                      void *expert_token_num, float *permute_topk_w,
+                      int64_t expert_token_num_type, int64_t idx_type,
+                      void *workspace, size_t workspace_bytes, mrr_stream_t stream);
+
+/*
+ * mrr_v2_run_plan -- as mrr_v2_run, with the launch taken from *plan (made by mrr_v2_plan for
+ * the same shapes, possibly with edited tuning fields).  The shape fields of the plan must
+ * match the arguments (else MRR_ERR_PLAN).  MRR_PATH_BULK with unaligned rows or pointers
+ * returns MRR_ERR_PLAN.
+ */
+mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan,
+                           const void *tokens, mrr_token_dtype dt, const void *counts,
+                           const void *scales, const float *topk_w,
+                           void *permute_tokens, void *permute_scales, int32_t *permute_token_idx,
+                           void *expert_token_num, float *permute_topk_w,
+                           int64_t expert_token_num_type,
+                           void *workspace, size_t workspace_bytes, mrr_stream_t stream);
+
+/*
+ * mrr_v2_read_status -- synchronise `stream`, read the status words of the last run that used
+ * `workspace`, and return MRR_OK or the device-detected error (MRR_ERR_COUNT_NONPOS,
+ * MRR_ERR_COUNT_SUM, MRR_ERR_TIMEOUT), or MRR_ERR_CUDA if the copy back fails.
+ * workspace_bytes must be >= 4096.
+ */
+mrr_status mrr_v2_read_status(const void *workspace, size_t workspace_bytes, mrr_stream_t stream);
+
+/* mrr_status_str -- static, human-readable name of a status code (never NULL). */
+const char *mrr_status_str(mrr_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MRR_V2_H */

@@ -1,0 +1,1029 @@
+// GB300 (sm_103a) implementation of the MoeReRoutingV2 re-routing step behind the C ABI in
+// include/mrr_v2.h.
+//
+// What the op computes ("CANN ops-transformer MoeReRoutingV2" article, section 计算公式):
+// the count matrix counts[N,E] splits the A received rows into segments (rank i, expert j);
+// segment (i,j) starts at SrcOffset(i,j) in the rank-major input (exclusive prefix of the
+// counts in row-major order) and moves, order kept, to DstOffset(i,j) in the expert-major
+// output (exclusive prefix in column-major order).  Token rows, scale rows and top-k weights
+// share the offsets; the index output and the per-expert counts come from the same offsets.
+//
+// GB300 design (pure data movement, bound by HBM bandwidth; no tensor-core work exists):
+//   * One kernel does everything for N*E <= 4096: each CTA scans the counts into shared
+//     memory (row-major and column-major exclusive prefixes, warp-shuffle block scans) while
+//     its first token chunks are already in flight, then streams its slice of the token bytes.
+//   * Work is split by SOURCE bytes: CTA b owns an equal, contiguous, 16-byte-aligned slice of
+//     the token buffer.  Source addresses need no offsets, so the bulk path issues its first
+//     loads before the scan and hides the scan behind them.  Inside a segment both sides are
+//     contiguous, so a slice maps to a few contiguous runs ("pieces"), each copied as a whole.
+//   * Bulk path (rows a multiple of 16 bytes): one thread per CTA drives the bulk-copy engine:
+//     cp.async.bulk global->shared into a ring of `stages` chunks (completion on mbarriers),
+//     then one cp.async.bulk shared->global per piece.  The other warps move the scale rows,
+//     top-k weights and the index at the same time.
+//   * Vector path (any alignment): every thread copies pieces with the widest vector width the
+//     relative alignment of source and destination allows (16 B down to 1 B).
+//   * N*E > 4096: a one-CTA scan kernel writes the offsets into the workspace first.
+//   * Data-dependent errors (count <= 0, Sum != A) set flags in a status word in the
+//     workspace; every CTA then skips its stores.  Every wait is bounded in time; a timeout
+//     sets a flag, drains the copies in flight and returns (no trap, no assert).
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "mrr_v2.h"
+#include "ptx.cuh"
+
+namespace mrr {
+
+constexpr int kStatusBytes = 4096;                 // status region at the front of the workspace
+constexpr int kStatusWords = kStatusBytes / 4;     // [0] flags, [1] grid, [2 + b] CTA b's flags
+constexpr int kMaxGrid = kStatusWords - 2;
+constexpr int64_t kFusedMaxSegs = 4096;            // N*E scanned inside every CTA up to this
+constexpr uint32_t kFlagNonPos = 1u, kFlagSum = 2u, kFlagTimeout = 4u;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // bound on any single mbarrier wait: 2 s
+constexpr int kMaxStages = 8;
+
+struct Params {
+    const uint8_t *tokens;
+    uint8_t *out_tokens;
+    int64_t total_bytes;  // A * row_bytes
+    int64_t row_bytes;
+    int64_t A;
+    const void *counts;
+    int count_is_i64;
+    int N, E, NE;
+    const uint8_t *scales;
+    uint8_t *out_scales;
+    int64_t scale_row_bytes;
+    int scale_w;          // vector width for scale rows (1..16)
+    const uint8_t *topk;
+    uint8_t *out_topk;
+    int topk_w;           // vector width for the 4-byte weights (1..4)
+    int32_t *idx;
+    int idx_type;
+    void *etn;
+    uint32_t *status;
+    uint32_t *g_row_ex;   // N*E > 4096: offsets scanned into the workspace
+    uint32_t *g_dst_off;
+    int chunk_bytes;
+    int stages;
+};
+
+// ------------------------------------------------------------------------------------------------
+// helpers
+
+__device__ __forceinline__ int64_t load_count(const Params &p, int64_t k)
+{
+    if (p.count_is_i64)
+        return (int64_t)__ldg(reinterpret_cast<const long long *>(p.counts) + k);
+    return (int64_t)__ldg(reinterpret_cast<const int *>(p.counts) + k);
+}
+
+// Segment of source row s: the last q in [0, NE) with row_ex[q] <= s.  row_ex is strictly
+// increasing (every count > 0) with row_ex[0] = 0 and row_ex[NE] = A.
+__device__ __forceinline__ int find_seg(const uint32_t *row_ex, int NE, uint32_t s)
+{
+    int lo = 0, hi = NE;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (row_ex[mid] <= s)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+// Exclusive block-wide scan of one uint32 per thread (warp shuffles + one smem pass).
+// Every thread of the block must call it.  *total receives the block sum.
+__device__ __forceinline__ uint32_t block_exscan(uint32_t v, uint32_t *total, uint32_t *s_warp)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = (blockDim.x + 31) >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o)
+            x += y;
+    }
+    if (lane == 31)
+        s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t w = lane < nwarps ? s_warp[lane] : 0u;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o)
+                w += y;
+        }
+        s_warp[lane] = w;  // inclusive prefix of the warp totals
+    }
+    __syncthreads();
+    const uint32_t base = warp ? s_warp[warp - 1] : 0u;
+    *total = s_warp[nwarps - 1];
+    __syncthreads();  // s_warp is reused by the next call
+    return base + x - v;
+}
+
+// Load and validate the counts, then build both prefixes in shared memory:
+//   row_ex[q]  = SrcOffset of segment q = i*E + j (row-major walk), row_ex[NE] = A
+//   dst_off[q] = DstOffset of segment q (column-major walk: expert outer, rank inner)
+// Returns the error flags (uniform over the block); the tables are valid when it returns 0.
+__device__ uint32_t cta_scan(const Params &p, uint32_t *cnt, uint32_t *row_ex, uint32_t *dst_off,
+                             uint32_t *s_warp, uint32_t *s_flags, unsigned long long *s_sum)
+{
+    const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31;
+    const int NE = p.NE, N = p.N, E = p.E;
+    if (tid == 0) {
+        *s_flags = 0u;
+        *s_sum = 0ull;
+    }
+    __syncthreads();
+    uint32_t f = 0u;
+    unsigned long long sum = 0ull;
+    for (int k = tid; k < NE; k += nthr) {
+        const int64_t c = load_count(p, k);
+        uint32_t v = 0u;
+        if (c <= 0)
+            f |= kFlagNonPos;
+        else if (c > p.A)
+            f |= kFlagSum;
+        else {
+            v = (uint32_t)c;
+            sum += (unsigned long long)c;
+        }
+        cnt[k] = v;
+    }
+    f = __reduce_or_sync(0xffffffffu, f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        sum += __shfl_down_sync(0xffffffffu, sum, o);
+    if (lane == 0) {
+        if (f)
+            atomicOr(s_flags, f);
+        if (sum)
+            atomicAdd(s_sum, sum);
+    }
+    __syncthreads();
+    uint32_t flags = *s_flags;
+    if (!flags && *s_sum != (unsigned long long)p.A)
+        flags |= kFlagSum;
+    if (flags)
+        return flags;  // uniform: every thread read the same smem values
+
+    // each thread scans a contiguous run of `per` positions
+    const int per = (NE + nthr - 1) / nthr;
+    const int k0 = min(NE, tid * per), k1 = min(NE, k0 + per);
+    uint32_t total;
+
+    uint32_t local = 0u;
+    for (int k = k0; k < k1; ++k)
+        local += cnt[k];
+    uint32_t run = block_exscan(local, &total, s_warp);
+    for (int k = k0; k < k1; ++k) {
+        row_ex[k] = run;
+        run += cnt[k];
+    }
+    if (tid == 0)
+        row_ex[NE] = (uint32_t)p.A;
+
+    local = 0u;
+    for (int pos = k0; pos < k1; ++pos)
+        local += cnt[(pos % N) * E + pos / N];
+    run = block_exscan(local, &total, s_warp);
+    for (int pos = k0; pos < k1; ++pos) {
+        const int q = (pos % N) * E + pos / N;
+        dst_off[q] = run;
+        run += cnt[q];
+    }
+    __syncthreads();
+    return 0u;
+}
+
+// expert_token_num[j] (count mode) = size of expert j's block in the destination
+//                                  = DstOffset(0, j+1) - DstOffset(0, j)   (A for the last one)
+__device__ __forceinline__ void write_expert_token_num(const Params &p, const uint32_t *dst_off, int t0,
+                                                       int ts)
+{
+    for (int j = t0; j < p.E; j += ts) {
+        const uint32_t next = (j + 1 < p.E) ? dst_off[j + 1] : (uint32_t)p.A;
+        const uint32_t v = next - dst_off[j];
+        if (p.count_is_i64)
+            reinterpret_cast<long long *>(p.etn)[j] = (long long)v;
+        else
+            reinterpret_cast<int *>(p.etn)[j] = (int)v;
+    }
+}
+
+__device__ __forceinline__ void copy_unit(uint8_t *d, const uint8_t *s, int w)
+{
+    switch (w) {
+    case 16:
+        *reinterpret_cast<uint4 *>(d) = __ldg(reinterpret_cast<const uint4 *>(s));
+        break;
+    case 8:
+        *reinterpret_cast<uint2 *>(d) = __ldg(reinterpret_cast<const uint2 *>(s));
+        break;
+    case 4:
+        *reinterpret_cast<uint32_t *>(d) = __ldg(reinterpret_cast<const uint32_t *>(s));
+        break;
+    case 2:
+        *reinterpret_cast<uint16_t *>(d) = __ldg(reinterpret_cast<const uint16_t *>(s));
+        break;
+    default:
+        *d = __ldg(s);
+        break;
+    }
+}
+
+// Scale rows, top-k weights and the index for this CTA's share of the SOURCE rows,
+// processed by threads t0, t0 + ts, ... of the block.
+__device__ void side_arrays(const Params &p, const uint32_t *row_ex, const uint32_t *dst_off, int t0, int ts)
+{
+    const int64_t G = gridDim.x, b = blockIdx.x;
+    const int64_t r_lo = b * p.A / G, r_hi = (b + 1) * p.A / G;
+    for (int64_t s = r_lo + t0; s < r_hi; s += ts) {
+        const int q = find_seg(row_ex, p.NE, (uint32_t)s);
+        const int64_t d = (int64_t)dst_off[q] + (s - (int64_t)row_ex[q]);
+        if (p.idx_type == 0)
+            p.idx[d] = (int32_t)s;  // gather index: out[d] = in[idx[d]]
+        else
+            p.idx[s] = (int32_t)d;  // scatter index: out[idx[s]] = in[s]
+        if (p.topk) {
+            for (int k = 0; k < 4; k += p.topk_w)
+                copy_unit(p.out_topk + d * 4 + k, p.topk + s * 4 + k, p.topk_w);
+        }
+    }
+    if (p.scales) {
+        const int w = p.scale_w;
+        const int64_t sb = p.scale_row_bytes, vpr = sb / w;
+        const int64_t items = (r_hi - r_lo) * vpr;
+        for (int64_t t = t0; t < items; t += ts) {
+            const int64_t r = t / vpr;
+            const int64_t v = t - r * vpr;
+            const int64_t s = r_lo + r;
+            const int q = find_seg(row_ex, p.NE, (uint32_t)s);
+            const int64_t d = (int64_t)dst_off[q] + (s - (int64_t)row_ex[q]);
+            copy_unit(p.out_scales + d * sb + v * w, p.scales + s * sb + v * w, w);
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// vector path: cooperative copy of one contiguous run
+
+template <int W>
+struct Vec;
+template <>
+struct Vec<16> {
+    static __device__ __forceinline__ uint4 ld(const uint8_t *p) { return ld_stream_v4(p); }
+    static __device__ __forceinline__ void st(uint8_t *p, uint4 v) { st_v4(p, v); }
+    using T = uint4;
+};
+template <>
+struct Vec<8> {
+    static __device__ __forceinline__ uint2 ld(const uint8_t *p) { return __ldg(reinterpret_cast<const uint2 *>(p)); }
+    static __device__ __forceinline__ void st(uint8_t *p, uint2 v) { *reinterpret_cast<uint2 *>(p) = v; }
+    using T = uint2;
+};
+template <>
+struct Vec<4> {
+    static __device__ __forceinline__ uint32_t ld(const uint8_t *p) { return __ldg(reinterpret_cast<const uint32_t *>(p)); }
+    static __device__ __forceinline__ void st(uint8_t *p, uint32_t v) { *reinterpret_cast<uint32_t *>(p) = v; }
+    using T = uint32_t;
+};
+template <>
+struct Vec<2> {
+    static __device__ __forceinline__ uint16_t ld(const uint8_t *p) { return __ldg(reinterpret_cast<const uint16_t *>(p)); }
+    static __device__ __forceinline__ void st(uint8_t *p, uint16_t v) { *reinterpret_cast<uint16_t *>(p) = v; }
+    using T = uint16_t;
+};
+template <>
+struct Vec<1> {
+    static __device__ __forceinline__ uint8_t ld(const uint8_t *p) { return __ldg(p); }
+    static __device__ __forceinline__ void st(uint8_t *p, uint8_t v) { *p = v; }
+    using T = uint8_t;
+};
+
+// dst and src are congruent modulo W: bytes up to dst's W boundary, W-wide body, byte tail
+template <int W>
+__device__ __forceinline__ void copy_run(uint8_t *dst, const uint8_t *src, int64_t len, int tid, int nthr)
+{
+    int64_t head = (int64_t)((W - ((uintptr_t)dst & (W - 1))) & (W - 1));
+    if (head > len)
+        head = len;
+    for (int64_t i = tid; i < head; i += nthr)
+        dst[i] = __ldg(src + i);
+    const int64_t nv = (len - head) / W;
+    uint8_t *d = dst + head;
+    const uint8_t *s = src + head;
+    constexpr int U = 4;
+    int64_t i = tid;
+    for (; i + (int64_t)(U - 1) * nthr < nv; i += (int64_t)U * nthr) {
+        typename Vec<W>::T r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            r[u] = Vec<W>::ld(s + (i + (int64_t)u * nthr) * W);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            Vec<W>::st(d + (i + (int64_t)u * nthr) * W, r[u]);
+    }
+    for (; i < nv; i += nthr)
+        Vec<W>::st(d + i * W, Vec<W>::ld(s + i * W));
+    for (int64_t k = head + nv * W + tid; k < len; k += nthr)
+        dst[k] = __ldg(src + k);
+}
+
+__device__ __forceinline__ void copy_block(uint8_t *dst, const uint8_t *src, int64_t len, int tid, int nthr)
+{
+    const uintptr_t mis = ((uintptr_t)dst ^ (uintptr_t)src) & 15u;
+    if (mis == 0)
+        copy_run<16>(dst, src, len, tid, nthr);
+    else if ((mis & 7u) == 0)
+        copy_run<8>(dst, src, len, tid, nthr);
+    else if ((mis & 3u) == 0)
+        copy_run<4>(dst, src, len, tid, nthr);
+    else if ((mis & 1u) == 0)
+        copy_run<2>(dst, src, len, tid, nthr);
+    else
+        copy_run<1>(dst, src, len, tid, nthr);
+}
+
+// Walk the pieces of source byte range [lo, hi): each piece lies inside one segment, where the
+// destination is the source shifted by (DstOffset - SrcOffset) rows.
+__device__ void vector_copy(const Params &p, const uint32_t *row_ex, const uint32_t *dst_off, int64_t lo,
+                            int64_t hi, int tid, int nthr)
+{
+    if (lo >= hi)
+        return;
+    const int64_t rb = p.row_bytes;
+    int q = find_seg(row_ex, p.NE, (uint32_t)(lo / rb));
+    int64_t seg_end = (int64_t)row_ex[q + 1] * rb;
+    int64_t delta = ((int64_t)dst_off[q] - (int64_t)row_ex[q]) * rb;
+    for (int64_t pos = lo; pos < hi;) {
+        while (pos >= seg_end) {
+            ++q;
+            seg_end = (int64_t)row_ex[q + 1] * rb;
+            delta = ((int64_t)dst_off[q] - (int64_t)row_ex[q]) * rb;
+        }
+        const int64_t pe = min(hi, seg_end);
+        copy_block(p.out_tokens + pos + delta, p.tokens + pos, pe - pos, tid, nthr);
+        pos = pe;
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// bulk path: one driver thread per CTA
+
+struct BulkRing {
+    uint64_t *bars;
+    uint8_t *base;
+    int64_t lo, hi, nch;
+    int64_t issued;  // loads issued so far (chunks 0 .. issued-1)
+};
+
+__device__ __forceinline__ void bulk_issue_load(const Params &p, BulkRing &r, int64_t c)
+{
+    const int S = p.stages;
+    const int64_t C = p.chunk_bytes;
+    const int st = (int)(c % S);
+    const int64_t b0 = r.lo + c * C;
+    const uint32_t bytes = (uint32_t)min(C, r.hi - b0);
+    const uint32_t bar = smem_addr(&r.bars[st]);
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(smem_addr(r.base + (size_t)st * C), p.tokens + b0, bytes, bar);
+    r.issued = c + 1;
+}
+
+__device__ uint32_t bulk_driver(const Params &p, BulkRing &r, const uint32_t *row_ex, const uint32_t *dst_off,
+                                uint32_t flags)
+{
+    const int S = p.stages;
+    const int64_t C = p.chunk_bytes, rb = p.row_bytes;
+    int64_t consumed = 0;
+    uint32_t tflag = 0u;
+    if (!flags && r.nch > 0) {
+        int q = find_seg(row_ex, p.NE, (uint32_t)(r.lo / rb));
+        int64_t seg_end = (int64_t)row_ex[q + 1] * rb;
+        int64_t delta = ((int64_t)dst_off[q] - (int64_t)row_ex[q]) * rb;
+        for (int64_t c = 0; c < r.nch; ++c) {
+            const int st = (int)(c % S);
+            if (!mbar_wait_bounded(smem_addr(&r.bars[st]), (uint32_t)((c / S) & 1), kWaitLimitNs)) {
+                tflag = kFlagTimeout;
+                break;
+            }
+            consumed = c + 1;
+            const int64_t b0 = r.lo + c * C, b1 = min(b0 + C, r.hi);
+            const uint32_t sbase = smem_addr(r.base + (size_t)st * C);
+            for (int64_t pos = b0; pos < b1;) {
+                while (pos >= seg_end) {
+                    ++q;
+                    seg_end = (int64_t)row_ex[q + 1] * rb;
+                    delta = ((int64_t)dst_off[q] - (int64_t)row_ex[q]) * rb;
+                }
+                const int64_t pe = min(b1, seg_end);
+                bulk_s2g(p.out_tokens + pos + delta, sbase + (uint32_t)(pos - b0), (uint32_t)(pe - pos));
+                pos = pe;
+            }
+            bulk_commit();
+            // the stage of chunk c-1 is free once its stores have read it: refill it
+            if (c >= 1 && c - 1 + S < r.nch) {
+                bulk_wait_read<1>();
+                bulk_issue_load(p, r, c - 1 + S);
+            }
+        }
+    }
+    // loads issued but not consumed (invalid counts or a timeout): let them land before exit
+    for (int64_t c = consumed; c < r.issued; ++c)
+        (void)mbar_wait_bounded(smem_addr(&r.bars[c % S]), (uint32_t)((c / S) & 1), kWaitLimitNs);
+    bulk_wait_all<0>();
+    return tflag;
+}
+
+// ------------------------------------------------------------------------------------------------
+// kernels
+
+template <bool kBulk, bool kFused>
+__global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ uint64_t bars[kMaxStages];
+    __shared__ uint32_t s_warp[32];
+    __shared__ uint32_t s_flags;
+    __shared__ unsigned long long s_sum;
+
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int64_t G = gridDim.x, b = blockIdx.x;
+
+    // this CTA's slice of the source bytes, in 16-byte units
+    const int64_t units = (p.total_bytes + 15) >> 4;
+    const int64_t lo = min(p.total_bytes, (b * units / G) << 4);
+    const int64_t hi = (b == G - 1) ? p.total_bytes : min(p.total_bytes, ((b + 1) * units / G) << 4);
+
+    BulkRing ring;
+    ring.bars = bars;
+    ring.base = smem;
+    ring.lo = lo;
+    ring.hi = hi;
+    ring.nch = kBulk ? (hi - lo + p.chunk_bytes - 1) / p.chunk_bytes : 0;
+    ring.issued = 0;
+    uint32_t *tab = reinterpret_cast<uint32_t *>(smem + (kBulk ? (size_t)p.stages * p.chunk_bytes : 0));
+
+    if (kBulk && tid == 0) {
+        for (int s = 0; s < p.stages; ++s)
+            mbar_init(smem_addr(&bars[s]), 1u);
+        mbar_init_fence();
+        // source addresses need no offsets: start streaming before the scan
+        const int64_t first = min((int64_t)p.stages, ring.nch);
+        for (int64_t c = 0; c < first; ++c)
+            bulk_issue_load(p, ring, c);
+    }
+
+    uint32_t flags;
+    const uint32_t *row_ex, *dst_off;
+    if (kFused) {
+        uint32_t *cnt = tab, *rex = tab + p.NE, *dof = tab + 2 * p.NE + 1;
+        flags = cta_scan(p, cnt, rex, dof, s_warp, &s_flags, &s_sum);
+        row_ex = rex;
+        dst_off = dof;
+        if (b == 0) {
+            if (!flags)
+                write_expert_token_num(p, dst_off, tid, nthr);
+            if (tid == 0) {
+                p.status[0] = flags;
+                p.status[1] = (uint32_t)G;
+            }
+        }
+    } else {
+        flags = *reinterpret_cast<volatile uint32_t *>(p.status);  // written by the scan kernel
+        row_ex = p.g_row_ex;
+        dst_off = p.g_dst_off;
+        if (b == 0 && tid == 0)
+            p.status[1] = (uint32_t)G;
+    }
+
+    uint32_t tflag = 0u;
+    if (kBulk) {
+        if (tid == 0)
+            tflag = bulk_driver(p, ring, row_ex, dst_off, flags);
+        else if (tid >= 32 && !flags)
+            side_arrays(p, row_ex, dst_off, tid - 32, nthr - 32);
+    } else if (!flags) {
+        vector_copy(p, row_ex, dst_off, lo, hi, tid, nthr);
+        side_arrays(p, row_ex, dst_off, tid, nthr);
+    }
+    if (tid == 0)
+        p.status[2 + b] = tflag;
+}
+
+// N*E > 4096: one CTA validates the counts and writes both prefixes and expert_token_num to
+// global memory, tile by tile with a running carry.
+__global__ void __launch_bounds__(1024) scan_kernel(const Params p)
+{
+    __shared__ uint32_t s_warp[32];
+    __shared__ uint32_t s_flags;
+    __shared__ unsigned long long s_sum;
+    const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31;
+    const int NE = p.NE, N = p.N, E = p.E;
+    if (tid == 0) {
+        s_flags = 0u;
+        s_sum = 0ull;
+    }
+    __syncthreads();
+    uint32_t f = 0u;
+    unsigned long long sum = 0ull;
+    for (int k = tid; k < NE; k += nthr) {
+        const int64_t c = load_count(p, k);
+        if (c <= 0)
+            f |= kFlagNonPos;
+        else if (c > p.A)
+            f |= kFlagSum;
+        else
+            sum += (unsigned long long)c;
+    }
+    f = __reduce_or_sync(0xffffffffu, f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        sum += __shfl_down_sync(0xffffffffu, sum, o);
+    if (lane == 0) {
+        if (f)
+            atomicOr(&s_flags, f);
+        if (sum)
+            atomicAdd(&s_sum, sum);
+    }
+    __syncthreads();
+    uint32_t flags = s_flags;
+    if (!flags && s_sum != (unsigned long long)p.A)
+        flags |= kFlagSum;
+    if (flags) {
+        if (tid == 0)
+            p.status[0] = flags;
+        return;
+    }
+    uint32_t carry = 0u, total;
+    for (int base = 0; base < NE; base += nthr) {
+        const int k = base + tid;
+        const uint32_t v = k < NE ? (uint32_t)load_count(p, k) : 0u;
+        const uint32_t ex = block_exscan(v, &total, s_warp);
+        if (k < NE)
+            p.g_row_ex[k] = carry + ex;
+        carry += total;
+    }
+    if (tid == 0)
+        p.g_row_ex[NE] = (uint32_t)p.A;
+    carry = 0u;
+    for (int base = 0; base < NE; base += nthr) {
+        const int pos = base + tid;
+        const int q = pos < NE ? (pos % N) * E + pos / N : 0;
+        const uint32_t v = pos < NE ? (uint32_t)load_count(p, q) : 0u;
+        const uint32_t ex = block_exscan(v, &total, s_warp);
+        if (pos < NE)
+            p.g_dst_off[q] = carry + ex;
+        carry += total;
+    }
+    __syncthreads();  // global writes of the block visible to the whole block
+    write_expert_token_num(p, p.g_dst_off, tid, nthr);
+    if (tid == 0)
+        p.status[0] = 0u;
+}
+
+}  // namespace mrr
+
+// ================================================================================================
+// host side
+
+using namespace mrr;
+
+namespace {
+
+int token_bits(int dt)
+{
+    switch (dt) {
+    case MRR_F16:
+    case MRR_BF16:
+        return 16;
+    case MRR_I8:
+    case MRR_F8E5M2:
+    case MRR_F8E4M3FN:
+    case MRR_HIF8:
+        return 8;
+    case MRR_F4E2M1:
+    case MRR_F4E1M2:
+        return 4;
+    default:
+        return 0;
+    }
+}
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+int widest_width(uintptr_t a, uintptr_t b, int64_t bytes, int cap)
+{
+    int w = cap;
+    while (w > 1 && (((a | b) & (uintptr_t)(w - 1)) != 0 || bytes % w != 0))
+        w >>= 1;
+    return w;
+}
+
+// checks shared by plan and run: shapes and attributes (no pointers)
+mrr_status check_shape(int64_t A, int64_t H, int dt, int64_t N, int64_t E, int count_is_i64, int sl,
+                       int64_t scale_cols, int64_t etn_type, int64_t idx_type, int64_t *row_bytes,
+                       int64_t *scale_row_bytes)
+{
+    const int bits = token_bits(dt);
+    if (bits == 0 || sl < MRR_SCALE_NONE || sl > MRR_SCALE_E8M0_AK2 || (count_is_i64 != 0 && count_is_i64 != 1))
+        return MRR_ERR_DTYPE;
+    if (etn_type != 0 && etn_type != 1)
+        return MRR_ERR_ATTR;
+    if (idx_type != 0 && idx_type != 1)
+        return MRR_ERR_ATTR;
+    if (etn_type == 0)
+        return MRR_ERR_UNSUPPORTED;
+    // section 约束说明: 0 < H < 16384; A = Sum(counts) with every count > 0 (so N*E <= A);
+    // the index output is int32, so A <= INT32_MAX
+    if (H <= 0 || H >= 16384 || (bits == 4 && (H & 1)))
+        return MRR_ERR_SHAPE;
+    if (A < 0 || A > INT32_MAX || N < 0 || E < 0)
+        return MRR_ERR_SHAPE;
+    if (N > INT32_MAX || E > INT32_MAX || (N > 0 && E > INT32_MAX / N))
+        return MRR_ERR_SHAPE;
+    const int64_t NE = N * E;
+    if ((NE == 0) != (A == 0) || NE > A)
+        return MRR_ERR_SHAPE;
+    int64_t sb = 0;
+    switch (sl) {
+    case MRR_SCALE_NONE:
+        sb = 0;
+        break;
+    case MRR_SCALE_F32_A:
+        if (scale_cols != 1)
+            return MRR_ERR_SHAPE;
+        sb = 4;
+        break;
+    case MRR_SCALE_F32_AS:
+        if (scale_cols < 1 || scale_cols > (1 << 20))
+            return MRR_ERR_SHAPE;
+        sb = 4 * scale_cols;
+        break;
+    case MRR_SCALE_E8M0_AK2:
+        if (scale_cols < 2 || (scale_cols & 1) || scale_cols > (1 << 20))
+            return MRR_ERR_SHAPE;
+        sb = scale_cols;
+        break;
+    }
+    *row_bytes = H * bits / 8;
+    *scale_row_bytes = sb;
+    return MRR_OK;
+}
+
+// pointer checks shared by run and run_plan (section 参数说明: the top-k input and output come
+// as a pair; scales need an output; index and counts are read/written as their int types)
+mrr_status check_buffers(int64_t NE, int64_t E, int cb, int sl, const void *tokens, const void *counts,
+                         const void *scales, const void *topk_w, const void *permute_tokens,
+                         const void *permute_scales, const void *idx, const void *etn, const void *permute_topk_w,
+                         const void *workspace, size_t workspace_bytes)
+{
+    if ((topk_w == nullptr) != (permute_topk_w == nullptr))
+        return MRR_ERR_TOPK_PAIR;
+    if (sl != MRR_SCALE_NONE && (!scales || !permute_scales))
+        return MRR_ERR_NULL;
+    if (sl == MRR_SCALE_NONE && scales)
+        return MRR_ERR_DTYPE;
+    if (E > 0 && !etn)
+        return MRR_ERR_NULL;
+    if (NE > 0 && (!tokens || !counts || !permute_tokens || !idx))
+        return MRR_ERR_NULL;
+    if (((uintptr_t)counts % cb) || ((uintptr_t)etn % cb) || ((uintptr_t)idx % 4))
+        return MRR_ERR_ALIGN;
+    if (!workspace || ((uintptr_t)workspace % 256) || workspace_bytes < (size_t)kStatusBytes)
+        return MRR_ERR_WORKSPACE;
+    return MRR_OK;
+}
+
+constexpr int kNumKernels = 5;
+bool g_smem_attr_set[64][kNumKernels];  // per device: max dynamic smem raised for each kernel
+
+template <bool kBulk, bool kFused>
+int kernel_slot()
+{
+    return (kBulk ? 2 : 0) + (kFused ? 1 : 0);
+}
+
+template <bool kBulk, bool kFused>
+cudaError_t launch_copy(const Params &p, int grid, int block, int smem, cudaStream_t stream, int device)
+{
+    auto kern = reroute_kernel<kBulk, kFused>;
+    const int slot = kernel_slot<kBulk, kFused>();
+    if (device >= 0 && device < 64 && !g_smem_attr_set[device][slot]) {
+        int optin = 0;
+        cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+        if (e != cudaSuccess)
+            return e;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - 1024);
+        if (e != cudaSuccess)
+            return e;
+        g_smem_attr_set[device][slot] = true;
+    }
+    kern<<<grid, block, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *mrr_status_str(mrr_status s)
+{
+    switch (s) {
+    case MRR_OK:
+        return "MRR_OK";
+    case MRR_ERR_NULL:
+        return "MRR_ERR_NULL: a required pointer is NULL";
+    case MRR_ERR_SHAPE:
+        return "MRR_ERR_SHAPE: A, H, N, E or scale_cols out of range";
+    case MRR_ERR_DTYPE:
+        return "MRR_ERR_DTYPE: unknown token dtype, scale layout or count type";
+    case MRR_ERR_ATTR:
+        return "MRR_ERR_ATTR: expert_token_num_type or idx_type not in {0, 1}";
+    case MRR_ERR_UNSUPPORTED:
+        return "MRR_ERR_UNSUPPORTED: expert_token_num_type 0 (cumsum mode) is not supported";
+    case MRR_ERR_TOPK_PAIR:
+        return "MRR_ERR_TOPK_PAIR: expert_topk_weight and permute_topk_weight must be given together";
+    case MRR_ERR_WORKSPACE:
+        return "MRR_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case MRR_ERR_CUDA:
+        return "MRR_ERR_CUDA: a CUDA runtime call failed";
+    case MRR_ERR_ALIGN:
+        return "MRR_ERR_ALIGN: counts, index or expert_token_num pointer misaligned for its type";
+    case MRR_ERR_PLAN:
+        return "MRR_ERR_PLAN: the plan does not match the arguments or is out of range";
+    case MRR_ERR_COUNT_NONPOS:
+        return "MRR_ERR_COUNT_NONPOS: a count is <= 0";
+    case MRR_ERR_COUNT_SUM:
+        return "MRR_ERR_COUNT_SUM: the counts do not sum to A";
+    case MRR_ERR_TIMEOUT:
+        return "MRR_ERR_TIMEOUT: a bounded wait in the copy kernel gave up";
+    }
+    return "unknown mrr_status";
+}
+
+mrr_status mrr_v2_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int64_t E, int count_is_i64,
+                       mrr_scale_layout sl, int64_t scale_cols, int has_topk, int64_t expert_token_num_type,
+                       int64_t idx_type, int device, mrr_v2_plan_t *out)
+{
+    if (!out)
+        return MRR_ERR_NULL;
+    int64_t rb = 0, sb = 0;
+    mrr_status st = check_shape(A, H, (int)dt, N, E, count_is_i64, (int)sl, scale_cols, expert_token_num_type,
+                                idx_type, &rb, &sb);
+    if (st != MRR_OK)
+        return st;
+    int sms = 0, optin = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return MRR_ERR_CUDA;
+    }
+    const int64_t NE = N * E;
+    const int64_t total = A * rb;
+    mrr_v2_plan_t p;
+    memset(&p, 0, sizeof(p));
+    p.A = A;
+    p.H = H;
+    p.N = N;
+    p.E = E;
+    p.row_bytes = rb;
+    p.scale_row_bytes = sb;
+    p.count_is_i64 = count_is_i64;
+    p.scale_layout = (int32_t)sl;
+    p.has_topk = has_topk ? 1 : 0;
+    p.idx_type = (int32_t)idx_type;
+    p.fuse_scan = NE <= kFusedMaxSegs ? 1 : 0;
+    p.path = (rb % 16 == 0) ? MRR_PATH_BULK : MRR_PATH_VECTOR;
+    p.num_sms = sms;
+    p.chunk_bytes = 32768;
+    p.stages = 4;
+    const int64_t table_bytes = p.fuse_scan ? round_up((3 * NE + 1) * 4, 128) : 0;
+    if (p.path == MRR_PATH_BULK) {
+        p.block = 256;
+        while (p.stages > 2 && (int64_t)p.stages * p.chunk_bytes + table_bytes > optin - 1024)
+            --p.stages;
+        while (p.chunk_bytes > 4096 && (int64_t)p.stages * p.chunk_bytes + table_bytes > optin - 1024)
+            p.chunk_bytes /= 2;
+        p.smem_bytes = (int32_t)((int64_t)p.stages * p.chunk_bytes + table_bytes);
+        const int64_t want = (total + 65535) / 65536;
+        p.grid = (int32_t)(want < 1 ? 1 : (want > sms ? sms : want));
+    } else {
+        p.block = 512;
+        p.smem_bytes = (int32_t)table_bytes;
+        const int64_t want = (total + 65535) / 65536;
+        const int64_t cap = 2 * (int64_t)sms;
+        p.grid = (int32_t)(want < 1 ? 1 : (want > cap ? cap : want));
+    }
+    if (p.grid > kMaxGrid)
+        p.grid = kMaxGrid;
+    p.workspace_bytes = kStatusBytes + (p.fuse_scan ? 0 : round_up(4 * (NE + 1), 256) + round_up(4 * NE, 256));
+    *out = p;
+    return MRR_OK;
+}
+
+mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_token_dtype dt, const void *counts,
+                           const void *scales, const float *topk_w, void *permute_tokens, void *permute_scales,
+                           int32_t *permute_token_idx, void *expert_token_num, float *permute_topk_w,
+                           int64_t expert_token_num_type, void *workspace, size_t workspace_bytes,
+                           mrr_stream_t stream_)
+{
+    if (!plan)
+        return MRR_ERR_NULL;
+    const mrr_v2_plan_t &pl = *plan;
+    int64_t rb = 0, sb = 0;
+    mrr_status st = check_shape(pl.A, pl.H, (int)dt, pl.N, pl.E, pl.count_is_i64, pl.scale_layout,
+                                pl.scale_layout == MRR_SCALE_E8M0_AK2 ? pl.scale_row_bytes
+                                                                      : pl.scale_row_bytes / 4,
+                                expert_token_num_type, pl.idx_type, &rb, &sb);
+    if (st != MRR_OK)
+        return st;
+    if (rb != pl.row_bytes || sb != pl.scale_row_bytes)
+        return MRR_ERR_PLAN;
+    const int64_t A = pl.A, N = pl.N, E = pl.E, NE = N * E;
+    const int cb = pl.count_is_i64 ? 8 : 4;
+
+    st = check_buffers(NE, E, cb, pl.scale_layout, tokens, counts, scales, topk_w, permute_tokens, permute_scales,
+                       permute_token_idx, expert_token_num, permute_topk_w, workspace, workspace_bytes);
+    if (st != MRR_OK)
+        return st;
+    if ((topk_w != nullptr) != (pl.has_topk != 0))
+        return MRR_ERR_PLAN;
+    if ((int64_t)workspace_bytes < pl.workspace_bytes)
+        return MRR_ERR_WORKSPACE;
+
+    // plan fields
+    const int64_t table_bytes = pl.fuse_scan ? round_up((3 * NE + 1) * 4, 128) : 0;
+    if (pl.fuse_scan != (NE <= kFusedMaxSegs ? 1 : 0))
+        return MRR_ERR_PLAN;
+    if (pl.workspace_bytes < kStatusBytes + (pl.fuse_scan ? 0 : round_up(4 * (NE + 1), 256) + round_up(4 * NE, 256)))
+        return MRR_ERR_PLAN;
+    if (pl.grid < 1 || pl.grid > kMaxGrid || pl.block < 64 || pl.block > 1024 || pl.block % 32)
+        return MRR_ERR_PLAN;
+    int path = pl.path;
+    const bool aligned16 = rb % 16 == 0 && ((uintptr_t)tokens % 16) == 0 && ((uintptr_t)permute_tokens % 16) == 0;
+    if (path == MRR_PATH_AUTO)
+        path = aligned16 ? MRR_PATH_BULK : MRR_PATH_VECTOR;
+    if (path == MRR_PATH_BULK && !aligned16)
+        path = (pl.path == MRR_PATH_BULK) ? -1 : MRR_PATH_VECTOR;
+    if (path != MRR_PATH_BULK && path != MRR_PATH_VECTOR)
+        return MRR_ERR_PLAN;
+    int64_t smem = table_bytes;
+    if (path == MRR_PATH_BULK) {
+        if (pl.stages < 2 || pl.stages > kMaxStages || pl.chunk_bytes < 16 || pl.chunk_bytes % 16 ||
+            pl.chunk_bytes > (1 << 20))
+            return MRR_ERR_PLAN;
+        smem += (int64_t)pl.stages * pl.chunk_bytes;
+    }
+
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int device = -1;
+    if (cudaGetDevice(&device) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return MRR_ERR_CUDA;
+    }
+    int optin = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return MRR_ERR_CUDA;
+    }
+    if (smem > optin - 1024)
+        return MRR_ERR_PLAN;
+
+    uint32_t *status = reinterpret_cast<uint32_t *>(workspace);
+    if (NE == 0) {
+        // the empty problem: no rows; expert_token_num is all zero
+        cudaError_t e = cudaSuccess;
+        if (E > 0)
+            e = cudaMemsetAsync(expert_token_num, 0, (size_t)(E * cb), stream);
+        if (e == cudaSuccess)
+            e = cudaMemsetAsync(status, 0, 8, stream);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return MRR_ERR_CUDA;
+        }
+        return MRR_OK;
+    }
+
+    Params p;
+    memset(&p, 0, sizeof(p));
+    p.tokens = static_cast<const uint8_t *>(tokens);
+    p.out_tokens = static_cast<uint8_t *>(permute_tokens);
+    p.total_bytes = A * rb;
+    p.row_bytes = rb;
+    p.A = A;
+    p.counts = counts;
+    p.count_is_i64 = pl.count_is_i64;
+    p.N = (int)N;
+    p.E = (int)E;
+    p.NE = (int)NE;
+    p.scales = static_cast<const uint8_t *>(scales);
+    p.out_scales = scales ? static_cast<uint8_t *>(permute_scales) : nullptr;
+    p.scale_row_bytes = sb;
+    p.scale_w = scales ? widest_width((uintptr_t)scales, (uintptr_t)permute_scales, sb, 16) : 1;
+    p.topk = reinterpret_cast<const uint8_t *>(topk_w);
+    p.out_topk = reinterpret_cast<uint8_t *>(permute_topk_w);
+    p.topk_w = topk_w ? widest_width((uintptr_t)topk_w, (uintptr_t)permute_topk_w, 4, 4) : 4;
+    p.idx = permute_token_idx;
+    p.idx_type = pl.idx_type;
+    p.etn = expert_token_num;
+    p.status = status;
+    p.chunk_bytes = pl.chunk_bytes;
+    p.stages = pl.stages;
+    if (!pl.fuse_scan) {
+        uint8_t *ws = static_cast<uint8_t *>(workspace) + kStatusBytes;
+        p.g_row_ex = reinterpret_cast<uint32_t *>(ws);
+        p.g_dst_off = reinterpret_cast<uint32_t *>(ws + round_up(4 * (NE + 1), 256));
+    }
+
+    cudaError_t e = cudaSuccess;
+    if (!pl.fuse_scan) {
+        scan_kernel<<<1, 1024, 0, stream>>>(p);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) {
+        const int grid = pl.grid, block = pl.block, sm = (int)smem;
+        if (path == MRR_PATH_BULK)
+            e = pl.fuse_scan ? launch_copy<true, true>(p, grid, block, sm, stream, device)
+                             : launch_copy<true, false>(p, grid, block, sm, stream, device);
+        else
+            e = pl.fuse_scan ? launch_copy<false, true>(p, grid, block, sm, stream, device)
+                             : launch_copy<false, false>(p, grid, block, sm, stream, device);
+    }
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return MRR_ERR_CUDA;
+    }
+    return MRR_OK;
+}
+
+mrr_status mrr_v2_run(const void *tokens, mrr_token_dtype dt, int64_t A, int64_t H, const void *counts,
+                      int count_is_i64, int64_t N, int64_t E, const void *scales, mrr_scale_layout sl,
+                      int64_t scale_cols, const float *topk_w, void *permute_tokens, void *permute_scales,
+                      int32_t *permute_token_idx, void *expert_token_num, float *permute_topk_w,
+                      int64_t expert_token_num_type, int64_t idx_type, void *workspace, size_t workspace_bytes,
+                      mrr_stream_t stream)
+{
+    int64_t rb = 0, sb = 0;
+    mrr_status st = check_shape(A, H, (int)dt, N, E, count_is_i64, (int)sl, scale_cols, expert_token_num_type,
+                                idx_type, &rb, &sb);
+    if (st != MRR_OK)
+        return st;
+    if (sl == MRR_SCALE_NONE)
+        scales = nullptr;  // "meaningless" output: nothing is read or written
+    st = check_buffers(N * E, E, count_is_i64 ? 8 : 4, (int)sl, tokens, counts, scales, topk_w, permute_tokens,
+                       permute_scales, permute_token_idx, expert_token_num, permute_topk_w, workspace,
+                       workspace_bytes);
+    if (st != MRR_OK)
+        return st;
+    int device = -1;
+    if (cudaGetDevice(&device) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return MRR_ERR_CUDA;
+    }
+    mrr_v2_plan_t plan;
+    st = mrr_v2_plan(A, H, dt, N, E, count_is_i64, sl, scale_cols, topk_w != nullptr, expert_token_num_type,
+                     idx_type, device, &plan);
+    if (st != MRR_OK)
+        return st;
+    plan.path = MRR_PATH_AUTO;
+    return mrr_v2_run_plan(&plan, tokens, dt, counts, scales, topk_w, permute_tokens, permute_scales,
+                           permute_token_idx, expert_token_num, permute_topk_w, expert_token_num_type, workspace,
+                           workspace_bytes, stream);
+}
+
+mrr_status mrr_v2_read_status(const void *workspace, size_t workspace_bytes, mrr_stream_t stream_)
+{
+    if (!workspace)
+        return MRR_ERR_NULL;
+    if (workspace_bytes < (size_t)kStatusBytes)
+        return MRR_ERR_WORKSPACE;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    uint32_t words[kStatusWords];
+    if (cudaMemcpyAsync(words, workspace, sizeof(words), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return MRR_ERR_CUDA;
+    }
+    uint32_t flags = words[0];
+    uint32_t n = words[1];
+    if (n > (uint32_t)kMaxGrid)
+        n = kMaxGrid;
+    for (uint32_t b = 0; b < n; ++b)
+        flags |= words[2 + b];
+    if (flags & kFlagNonPos)
+        return MRR_ERR_COUNT_NONPOS;
+    if (flags & kFlagSum)
+        return MRR_ERR_COUNT_SUM;
+    if (flags & kFlagTimeout)
+        return MRR_ERR_TIMEOUT;
+    return MRR_OK;
+}
+
+}  // extern "C"

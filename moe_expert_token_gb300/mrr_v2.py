@@ -1,0 +1,263 @@
+"""Thin ctypes binding of the C ABI in include/mrr_v2.h (argument marshalling only).
+
+The functions keep the C names.  ``moe_re_routing`` is the torch-level convenience call with
+the signature of the pages' PyTorch API (``cann_ops_transformer.moe_re_routing``, section
+PyTorch API 调用单算子模式 of the "CANN ops-transformer MoeReRoutingV2" article): it
+allocates the five outputs and the workspace with torch and runs the op through
+``mrr_v2_run``.  Every step of the op runs in the CUDA library; there is no other code path,
+and loading fails loudly when the library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional, Tuple
+
+from . import build as _build
+
+# ---------------------------------------------------------------------------- constants (mrr_v2.h)
+
+MRR_OK = 0
+MRR_ERR_NULL = 1
+MRR_ERR_SHAPE = 2
+MRR_ERR_DTYPE = 3
+MRR_ERR_ATTR = 4
+MRR_ERR_UNSUPPORTED = 5
+MRR_ERR_TOPK_PAIR = 6
+MRR_ERR_WORKSPACE = 7
+MRR_ERR_CUDA = 8
+MRR_ERR_ALIGN = 9
+MRR_ERR_PLAN = 10
+MRR_ERR_COUNT_NONPOS = 16
+MRR_ERR_COUNT_SUM = 17
+MRR_ERR_TIMEOUT = 18
+
+MRR_F16, MRR_BF16, MRR_I8, MRR_F8E5M2, MRR_F8E4M3FN, MRR_HIF8, MRR_F4E2M1, MRR_F4E1M2 = range(8)
+MRR_SCALE_NONE, MRR_SCALE_F32_A, MRR_SCALE_F32_AS, MRR_SCALE_E8M0_AK2 = range(4)
+MRR_PATH_AUTO, MRR_PATH_BULK, MRR_PATH_VECTOR = 0, 1, 2
+
+DTYPE_CODES = {
+    "float16": MRR_F16, "bfloat16": MRR_BF16, "int8": MRR_I8, "float8_e5m2": MRR_F8E5M2,
+    "float8_e4m3fn": MRR_F8E4M3FN, "hifloat8": MRR_HIF8, "float4_e2m1": MRR_F4E2M1,
+    "float4_e1m2": MRR_F4E1M2,
+}
+SCALE_CODES = {"none": MRR_SCALE_NONE, "f32_a": MRR_SCALE_F32_A, "f32_as": MRR_SCALE_F32_AS,
+               "e8m0": MRR_SCALE_E8M0_AK2}
+
+
+class MrrError(RuntimeError):
+    def __init__(self, code: int, where: str = ""):
+        super().__init__(f"{where}: {mrr_status_str(code)}" if where else mrr_status_str(code))
+        self.code = code
+
+
+class mrr_v2_plan_t(ctypes.Structure):
+    _fields_ = [
+        ("A", ctypes.c_int64), ("H", ctypes.c_int64), ("N", ctypes.c_int64), ("E", ctypes.c_int64),
+        ("row_bytes", ctypes.c_int64), ("scale_row_bytes", ctypes.c_int64),
+        ("workspace_bytes", ctypes.c_int64),
+        ("count_is_i64", ctypes.c_int32), ("scale_layout", ctypes.c_int32),
+        ("has_topk", ctypes.c_int32), ("idx_type", ctypes.c_int32),
+        ("fuse_scan", ctypes.c_int32), ("path", ctypes.c_int32), ("grid", ctypes.c_int32),
+        ("block", ctypes.c_int32), ("chunk_bytes", ctypes.c_int32), ("stages", ctypes.c_int32),
+        ("smem_bytes", ctypes.c_int32), ("num_sms", ctypes.c_int32),
+    ]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+# ---------------------------------------------------------------------------- loading
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libmrr_v2.so.  Raises if it has not been built: there is no fallback."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or _build.LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build the CUDA library first "
+            "(python -m moe_expert_token_gb300.build)")
+    lib = ctypes.CDLL(path)
+    P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.mrr_status_str.restype = ctypes.c_char_p
+    lib.mrr_status_str.argtypes = [I32]
+    lib.mrr_v2_plan.restype = I32
+    lib.mrr_v2_plan.argtypes = [I64, I64, I32, I64, I64, I32, I32, I64, I32, I64, I64, I32,
+                                ctypes.POINTER(mrr_v2_plan_t)]
+    lib.mrr_v2_run.restype = I32
+    lib.mrr_v2_run.argtypes = [P, I32, I64, I64, P, I32, I64, I64, P, I32, I64, P,
+                               P, P, P, P, P, I64, I64, P, ctypes.c_size_t, P]
+    lib.mrr_v2_run_plan.restype = I32
+    lib.mrr_v2_run_plan.argtypes = [ctypes.POINTER(mrr_v2_plan_t), P, I32, P, P, P,
+                                    P, P, P, P, P, I64, P, ctypes.c_size_t, P]
+    lib.mrr_v2_read_status.restype = I32
+    lib.mrr_v2_read_status.argtypes = [P, ctypes.c_size_t, P]
+    if path == _build.LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def header_functions() -> list:
+    """Names of the functions include/mrr_v2.h declares."""
+    text = open(os.path.join(_build.INCLUDE, "mrr_v2.h"), encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_]\w*\s*\*?\s*(mrr_\w+)\s*\(", text, flags=re.M)))
+
+
+# ---------------------------------------------------------------------------- C functions, same names
+
+def mrr_status_str(code: int) -> str:
+    return load_library().mrr_status_str(int(code)).decode()
+
+
+def mrr_v2_plan(A, H, dt, N, E, count_is_i64, sl, scale_cols, has_topk,
+                expert_token_num_type=1, idx_type=0, device=0) -> Tuple[int, mrr_v2_plan_t]:
+    plan = mrr_v2_plan_t()
+    st = load_library().mrr_v2_plan(A, H, dt, N, E, int(count_is_i64), sl, scale_cols,
+                                    int(has_topk), expert_token_num_type, idx_type, device,
+                                    ctypes.byref(plan))
+    return st, plan
+
+
+def mrr_v2_run(tokens, dt, A, H, counts, count_is_i64, N, E, scales, sl, scale_cols, topk_w,
+               permute_tokens, permute_scales, permute_token_idx, expert_token_num, permute_topk_w,
+               expert_token_num_type, idx_type, workspace, workspace_bytes, stream) -> int:
+    """All buffers are integer device addresses (or None); stream is a cudaStream_t value."""
+    return load_library().mrr_v2_run(
+        tokens, dt, A, H, counts, int(count_is_i64), N, E, scales, sl, scale_cols, topk_w,
+        permute_tokens, permute_scales, permute_token_idx, expert_token_num, permute_topk_w,
+        expert_token_num_type, idx_type, workspace, workspace_bytes, stream)
+
+
+def mrr_v2_run_plan(plan: mrr_v2_plan_t, tokens, dt, counts, scales, topk_w, permute_tokens,
+                    permute_scales, permute_token_idx, expert_token_num, permute_topk_w,
+                    expert_token_num_type, workspace, workspace_bytes, stream) -> int:
+    return load_library().mrr_v2_run_plan(
+        ctypes.byref(plan), tokens, dt, counts, scales, topk_w, permute_tokens, permute_scales,
+        permute_token_idx, expert_token_num, permute_topk_w, expert_token_num_type, workspace,
+        workspace_bytes, stream)
+
+
+def mrr_v2_read_status(workspace, workspace_bytes, stream) -> int:
+    return load_library().mrr_v2_read_status(workspace, workspace_bytes, stream)
+
+
+# ---------------------------------------------------------------------------- torch-level call
+
+def _torch_token_code(t, tokens_dtype: Optional[str]):
+    """(dtype code, H) for a tokens tensor; FP4 payloads hold two elements per byte."""
+    import torch
+
+    names = {torch.float16: "float16", torch.bfloat16: "bfloat16", torch.int8: "int8",
+             torch.float8_e5m2: "float8_e5m2", torch.float8_e4m3fn: "float8_e4m3fn"}
+    fp4 = getattr(torch, "float4_e2m1fn_x2", None)
+    if tokens_dtype is not None:
+        name = {"float4_e2m1fn_x2": "float4_e2m1", "float4_e1m2fn_x2": "float4_e1m2"}.get(
+            tokens_dtype, tokens_dtype)
+        if t.element_size() != 1 and name not in ("float16", "bfloat16"):
+            raise TypeError("tokens_dtype names a 1-byte or packed type but tokens are wider")
+    elif fp4 is not None and t.dtype == fp4:
+        name = "float4_e2m1"
+    elif t.dtype in names:
+        name = names[t.dtype]
+    else:
+        raise TypeError(f"unsupported tokens dtype {t.dtype}; pass tokens_dtype for uint8 storage")
+    code = DTYPE_CODES[name]
+    H = t.shape[-1] * (2 if code in (MRR_F4E2M1, MRR_F4E1M2) else 1)
+    return code, H
+
+
+def _scale_layout(s):
+    import torch
+
+    if s is None:
+        return MRR_SCALE_NONE, 0
+    if s.dtype == torch.float32 and s.dim() == 1:
+        return MRR_SCALE_F32_A, 1
+    if s.dtype == torch.float32 and s.dim() == 2:
+        return MRR_SCALE_F32_AS, s.shape[1]
+    if s.element_size() == 1 and s.dim() == 3 and s.shape[2] == 2:
+        return MRR_SCALE_E8M0_AK2, s.shape[1] * 2
+    raise TypeError("per_token_scales must be [A] / [A,S] float32 or [A, K/64, 2] e8m0 bytes")
+
+
+def moe_re_routing(tokens, expert_token_num_per_rank, *, per_token_scales=None,
+                   expert_topk_weight=None, expert_token_num_type: int = 1, idx_type: int = 0,
+                   tokens_dtype: Optional[str] = None, workspace=None, stream=None,
+                   check_status: bool = False):
+    """Re-route rank-major tokens to expert-major order on the GPU.
+
+    Returns (permute_tokens, permute_per_token_scales, permute_token_idx, expert_token_num,
+    permute_topk_weight) with the shapes of the pages' InferShape rules: absent scales give an
+    unwritten [A] float32 tensor, absent top-k weights an empty (0,) tensor.
+    ``check_status=True`` synchronises and raises on a device-detected count error.
+    """
+    import torch
+
+    t, c = tokens, expert_token_num_per_rank
+    if t.dim() != 2 or c.dim() != 2:
+        raise ValueError("tokens and expert_token_num_per_rank must be 2-D")
+    if not t.is_cuda:
+        raise ValueError("tokens must be a CUDA tensor")
+    if c.dtype not in (torch.int32, torch.int64):
+        raise TypeError("expert_token_num_per_rank must be int32 or int64")
+    dev = t.device
+    code, H = _torch_token_code(t, tokens_dtype)
+    A = t.shape[0]
+    N, E = c.shape
+    sl, scale_cols = _scale_layout(per_token_scales)
+    for x in (c, per_token_scales, expert_topk_weight):
+        if x is not None and (x.device != dev or not x.is_contiguous()):
+            raise ValueError("all tensors must be contiguous and on the tokens' device")
+    if not t.is_contiguous():
+        raise ValueError("tokens must be contiguous")
+    if expert_topk_weight is not None and (expert_topk_weight.dtype != torch.float32
+                                           or expert_topk_weight.shape != (A, 1)):
+        raise ValueError("expert_topk_weight must be float32 [A, 1]")
+
+    st, plan = mrr_v2_plan(A, H, code, N, E, c.dtype == torch.int64, sl, scale_cols,
+                           expert_topk_weight is not None, expert_token_num_type, idx_type,
+                           dev.index if dev.index is not None else torch.cuda.current_device())
+    if st != MRR_OK:
+        raise MrrError(st, "mrr_v2_plan")
+
+    out_tok = torch.empty_like(t)
+    out_sc = (torch.empty_like(per_token_scales) if per_token_scales is not None
+              else torch.empty(A, dtype=torch.float32, device=dev))
+    idx = torch.empty(A, dtype=torch.int32, device=dev)
+    etn = torch.empty(E, dtype=c.dtype, device=dev)
+    out_tw = (torch.empty_like(expert_topk_weight) if expert_topk_weight is not None
+              else torch.empty(0, dtype=torch.float32, device=dev))
+    if workspace is None or workspace.numel() < plan.workspace_bytes:
+        workspace = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+
+    def ptr(x):
+        return None if x is None else x.data_ptr()
+
+    with torch.cuda.device(dev):
+        st = mrr_v2_run(ptr(t), code, A, H, ptr(c), c.dtype == torch.int64, N, E,
+                        ptr(per_token_scales), sl, scale_cols, ptr(expert_topk_weight),
+                        ptr(out_tok), ptr(out_sc) if per_token_scales is not None else None,
+                        ptr(idx), ptr(etn),
+                        ptr(out_tw) if expert_topk_weight is not None else None,
+                        expert_token_num_type, idx_type, workspace.data_ptr(),
+                        workspace.numel(), stream.cuda_stream)
+        if st != MRR_OK:
+            raise MrrError(st, "mrr_v2_run")
+        if check_status:
+            st = mrr_v2_read_status(workspace.data_ptr(), workspace.numel(), stream.cuda_stream)
+            if st != MRR_OK:
+                raise MrrError(st, "device")
+    return out_tok, out_sc, idx, etn, out_tw

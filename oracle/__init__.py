@@ -45,6 +45,17 @@ def build(source: str = SOURCE, out: str = LIB, extra_flags=()) -> str:
 _lib = None
 
 
+def _built_for_this_host(path: str) -> bool:
+    import platform
+    import struct
+
+    with open(path, "rb") as f:
+        head = f.read(20)
+    want = {"x86_64": 62, "aarch64": 183}.get(platform.machine())
+    return (len(head) == 20 and head[:4] == b"\x7fELF"
+            and (want is None or struct.unpack_from("<H", head, 18)[0] == want))
+
+
 def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     P = ctypes.c_void_p
     I64 = ctypes.c_int64
@@ -64,7 +75,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     if path is not None:
         return _bind(ctypes.CDLL(path))
     if _lib is None:
-        if not os.path.exists(LIB) or os.path.getmtime(LIB) < os.path.getmtime(SOURCE):
+        if (not os.path.exists(LIB) or os.path.getmtime(LIB) < os.path.getmtime(SOURCE)
+                or not _built_for_this_host(LIB)):
             build()
         _lib = _bind(ctypes.CDLL(LIB))
     return _lib

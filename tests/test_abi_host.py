@@ -1,0 +1,159 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every function
+include/mrr_v2.h declares, and rejects bad arguments before touching CUDA.
+
+Validation rules (MoeReRoutingV2 article, sections 参数说明, 参数取值细节, 约束说明 and
+Torch 扩展的图转换细节): 0 < H < 16384; every count > 0 with Sum(counts) = A (so N*E <= A);
+the index output is int32 (A <= INT32_MAX); expert_token_num_type and idx_type are 0 or 1, and
+only expert_token_num_type = 1 is supported; expert_topk_weight and permute_topk_weight are
+given together.
+"""
+import ctypes
+import subprocess
+
+import pytest
+
+from moe_expert_token_gb300 import build as mbuild
+import moe_expert_token_gb300.mrr_v2 as m
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mbuild.build()
+    return m.load_library()
+
+
+def test_exports_every_header_function(lib):
+    names = m.header_functions()
+    assert set(names) == {"mrr_v2_plan", "mrr_v2_run", "mrr_v2_run_plan", "mrr_v2_read_status",
+                          "mrr_status_str"}
+    out = subprocess.run(["nm", "-D", "--defined-only", m.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for n in names:
+        assert n in exported, n
+        assert hasattr(lib, n)
+
+
+def test_library_has_sm103a_code():
+    out = subprocess.run(["cuobjdump", "--list-elf", m.library_path()], capture_output=True,
+                         text=True)
+    if out.returncode != 0:
+        pytest.skip("cuobjdump unavailable")
+    assert "sm_103a" in out.stdout
+
+
+def test_status_strings(lib):
+    for code in list(range(0, 11)) + [16, 17, 18]:
+        s = m.mrr_status_str(code)
+        assert s.startswith("MRR_"), (code, s)
+    assert m.mrr_status_str(12345) == "unknown mrr_status"
+
+
+def plan(**kw):
+    args = dict(A=16384, H=7168, dt=m.MRR_I8, N=16, E=16, count_is_i64=0, sl=m.MRR_SCALE_F32_A,
+                scale_cols=1, has_topk=0, expert_token_num_type=1, idx_type=0, device=0)
+    args.update(kw)
+    return m.mrr_v2_plan(**args)[0]
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dt=99), m.MRR_ERR_DTYPE),
+    (dict(sl=7), m.MRR_ERR_DTYPE),
+    (dict(count_is_i64=2), m.MRR_ERR_DTYPE),
+    (dict(H=0), m.MRR_ERR_SHAPE),
+    (dict(H=-3), m.MRR_ERR_SHAPE),
+    (dict(H=16384), m.MRR_ERR_SHAPE),
+    (dict(H=79, dt=m.MRR_F4E2M1), m.MRR_ERR_SHAPE),          # FP4 packs two per byte
+    (dict(A=-1), m.MRR_ERR_SHAPE),
+    (dict(A=2**31), m.MRR_ERR_SHAPE),                        # int32 index output
+    (dict(A=100, N=16, E=16), m.MRR_ERR_SHAPE),              # N*E > A: no positive counts
+    (dict(A=0), m.MRR_ERR_SHAPE),                            # A = 0 needs N*E = 0
+    (dict(A=10, N=0, E=4), m.MRR_ERR_SHAPE),                 # N*E = 0 needs A = 0
+    (dict(N=-1), m.MRR_ERR_SHAPE),
+    (dict(sl=m.MRR_SCALE_F32_A, scale_cols=2), m.MRR_ERR_SHAPE),
+    (dict(sl=m.MRR_SCALE_F32_AS, scale_cols=0), m.MRR_ERR_SHAPE),
+    (dict(sl=m.MRR_SCALE_E8M0_AK2, scale_cols=3), m.MRR_ERR_SHAPE),
+    (dict(expert_token_num_type=0), m.MRR_ERR_UNSUPPORTED),
+    (dict(expert_token_num_type=2), m.MRR_ERR_ATTR),
+    (dict(idx_type=2), m.MRR_ERR_ATTR),
+    (dict(idx_type=-1), m.MRR_ERR_ATTR),
+])
+def test_plan_rejects(lib, kw, code):
+    assert plan(**kw) == code
+
+
+def test_plan_valid_args_reach_the_device_query(lib):
+    import torch
+
+    st = plan()
+    if torch.cuda.is_available():
+        assert st == m.MRR_OK
+    else:
+        assert st == m.MRR_ERR_CUDA
+
+
+def test_plan_null_out(lib):
+    assert lib.mrr_v2_plan(16, 8, 0, 4, 4, 0, 0, 0, 0, 1, 0, 0, None) == m.MRR_ERR_NULL
+
+
+# fake, never-dereferenced device addresses: every error below is found before any CUDA call
+T, C, S, W, O1, O2, I, X, OW, WS = (0x10000 * k for k in range(1, 11))
+
+
+def run(**kw):
+    a = dict(tokens=T, dt=m.MRR_BF16, A=64, H=128, counts=C, count_is_i64=0, N=4, E=4, scales=S,
+             sl=m.MRR_SCALE_F32_A, scale_cols=1, topk_w=W, permute_tokens=O1, permute_scales=O2,
+             permute_token_idx=I, expert_token_num=X, permute_topk_w=OW,
+             expert_token_num_type=1, idx_type=0, workspace=WS, workspace_bytes=4096, stream=None)
+    a.update(kw)
+    return m.mrr_v2_run(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(permute_topk_w=None), m.MRR_ERR_TOPK_PAIR),
+    (dict(topk_w=None), m.MRR_ERR_TOPK_PAIR),
+    (dict(tokens=None), m.MRR_ERR_NULL),
+    (dict(counts=None), m.MRR_ERR_NULL),
+    (dict(permute_tokens=None), m.MRR_ERR_NULL),
+    (dict(permute_token_idx=None), m.MRR_ERR_NULL),
+    (dict(expert_token_num=None), m.MRR_ERR_NULL),
+    (dict(scales=None), m.MRR_ERR_NULL),
+    (dict(permute_scales=None), m.MRR_ERR_NULL),
+    (dict(counts=C + 2), m.MRR_ERR_ALIGN),
+    (dict(counts=C + 4, count_is_i64=1), m.MRR_ERR_ALIGN),
+    (dict(permute_token_idx=I + 2), m.MRR_ERR_ALIGN),
+    (dict(expert_token_num=X + 1), m.MRR_ERR_ALIGN),
+    (dict(workspace=None), m.MRR_ERR_WORKSPACE),
+    (dict(workspace=WS + 16), m.MRR_ERR_WORKSPACE),
+    (dict(workspace_bytes=1024), m.MRR_ERR_WORKSPACE),
+    (dict(H=16384), m.MRR_ERR_SHAPE),
+    (dict(expert_token_num_type=0), m.MRR_ERR_UNSUPPORTED),
+    (dict(idx_type=3), m.MRR_ERR_ATTR),
+    (dict(dt=42), m.MRR_ERR_DTYPE),
+])
+def test_run_rejects_before_any_cuda_call(lib, kw, code):
+    assert run(**kw) == code
+
+
+def test_run_without_scales_ignores_scale_pointers(lib):
+    import torch
+
+    st = run(scales=None, permute_scales=None, sl=m.MRR_SCALE_NONE)
+    # valid arguments: reaches CUDA (no device here -> MRR_ERR_CUDA)
+    if not torch.cuda.is_available():
+        assert st == m.MRR_ERR_CUDA
+
+
+def test_read_status_checks_arguments(lib):
+    assert m.mrr_v2_read_status(None, 4096, None) == m.MRR_ERR_NULL
+    assert m.mrr_v2_read_status(WS, 100, None) == m.MRR_ERR_WORKSPACE
+
+
+def test_run_plan_rejects_null_plan(lib):
+    assert lib.mrr_v2_run_plan(None, T, 0, C, None, None, O1, None, I, X, None, 1, WS, 4096,
+                               None) == m.MRR_ERR_NULL
+
+
+def test_plan_struct_layout_matches_header():
+    # 7 int64 fields followed by 12 int32 fields, no padding
+    assert ctypes.sizeof(m.mrr_v2_plan_t) == 7 * 8 + 12 * 4

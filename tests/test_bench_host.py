@@ -1,0 +1,81 @@
+"""CPU checks of bench.py's host logic: the multi-rank aggregation (max time over ranks, whole-job
+throughput) on two gloo ranks, the reference arm's JSON line, and the row sampler."""
+import json
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+import workloads
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    slowest = bench.max_over_ranks(10.0 + 5.0 * rank, dist, "cpu")
+    q.put((rank, slowest))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_max_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = dict(q.get(timeout=10) for _ in range(2))
+    assert got == {0: 15.0, 1: 15.0}
+
+
+def test_throughput_counts_every_rank():
+    # 2 replicas, 1 GB per step each, 10 steps in 1 s -> 20 GB/s for the job
+    assert bench.throughput_gbs(2, 10**9, 10, 1000.0) == pytest.approx(20.0)
+    assert bench.max_over_ranks(3.5) == 3.5
+
+
+def test_row_sample_keeps_the_workload_kind():
+    p = workloads.config(2)
+    q = bench.row_sample(p, 0.05)
+    assert q.counts.shape == p.counts.shape and q.counts.dtype == p.counts.dtype
+    assert int(q.counts.sum()) == q.A and (q.counts >= 1).all()
+    assert q.tokens.shape == (q.A, p.row_bytes)
+    # the skew survives: the last cell still holds almost every row
+    assert q.counts[-1, -1] == q.A - 255
+
+
+def test_reference_arm_prints_one_line(capsys, monkeypatch):
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    assert bench.main(["--impl", "reference", "--config", "1", "--steps", "5", "--warmup", "3"]) == 0
+    out = capsys.readouterr().out.strip().splitlines()
+    assert len(out) == 1
+    line = json.loads(out[0])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["steps"] == 5 and line["warmup"] == 3
+
+
+def test_reference_arm_other_ranks_do_nothing(capsys, monkeypatch):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    assert bench.main(["--impl", "reference", "--steps", "5", "--warmup", "3"]) == 0
+    assert capsys.readouterr().out == ""
