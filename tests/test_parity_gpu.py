@@ -134,7 +134,7 @@ STRESS_EDITS = [
 
 
 @pytest.mark.parametrize("edit", STRESS_EDITS, ids=lambda e: "-".join(f"{k}{v}" for k, v in e.items()))
-@pytest.mark.parametrize("shape", [(64, 128, 4, 4), (3000, 256, 64, 64), (700, 5000, 8, 32)])
+@pytest.mark.parametrize("shape", [(64, 128, 4, 4), (6000, 256, 64, 64), (700, 5000, 8, 32)])
 def test_bulk_pipeline_stress(edit, shape):
     A, H, N, E = shape
     p = workloads.make_problem(np.random.default_rng(A + H), A=A, H=H, N=N, E=E,
