@@ -183,6 +183,47 @@ mrr_status mrr_v2_read_status(const void *workspace, size_t workspace_bytes, mrr
 /* mrr_status_str -- static, human-readable name of a status code (never NULL). */
 const char *mrr_status_str(mrr_status s);
 
+/* Limits of the fixed scratch used by mrr_v2_run_noalloc. */
+#define MRR_NOALLOC_MAX_SEGMENTS 16384   /* largest N*E it accepts                          */
+#define MRR_NOALLOC_SCRATCH_BYTES 135424 /* device bytes it holds on every GPU that loads
+                                            the library, until the process exits            */
+
+/*
+ * mrr_v2_run_noalloc -- mrr_v2_run without a caller-provided workspace.  The paper has no
+ * counterpart to this entry point.
+ *
+ * Intended for callers that cannot allocate device memory at the call site, for example:
+ *   - a plugin whose host framework owns all device memory and passes it only the input and
+ *     output tensors;
+ *   - a serving loop whose device memory budget is fixed when it starts;
+ *   - code that must not call cudaMalloc/cudaFree, which can synchronise the whole device and
+ *     stall work on other streams.
+ * It allocates nothing and calls no allocating routine.  Its scratch is one fixed array of
+ * MRR_NOALLOC_SCRATCH_BYTES in the library's device memory, and that array holds the status
+ * words and, for N*E > 4096, the two offset tables.
+ *
+ * The arguments and outputs are those of mrr_v2_run.  The caller still passes every input and
+ * output buffer.
+ *   - N*E > MRR_NOALLOC_MAX_SEGMENTS returns MRR_ERR_WORKSPACE before anything is enqueued.
+ *   - wait_and_check != 0 synchronises `stream` after enqueuing and returns any error the device
+ *     found, as mrr_v2_read_status does.  With 0 the call only enqueues, and device-detected
+ *     count errors go unreported.
+ *   - The first call on each device looks up the array's device address, with that device
+ *     current.  Make that first call before any stream capture.
+ *   - Every call on a device uses the same array, which keeps the last call's contents.  Each
+ *     call rewrites the status words and tables it reads, so nothing needs clearing.  Calls
+ *     that overlap on the GPU (e.g. on two streams at once) race on the array and may report
+ *     wrong statuses or move rows wrongly: serialise them.
+ */
+mrr_status mrr_v2_run_noalloc(const void *tokens, mrr_token_dtype dt, int64_t A, int64_t H,
+                              const void *counts, int count_is_i64, int64_t N, int64_t E,
+                              const void *scales, mrr_scale_layout sl, int64_t scale_cols,
+                              const float *topk_w,
+                              void *permute_tokens, void *permute_scales, int32_t *permute_token_idx,
+                              void *expert_token_num, float *permute_topk_w,
+                              int64_t expert_token_num_type, int64_t idx_type,
+                              int wait_and_check, mrr_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

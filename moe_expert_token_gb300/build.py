@@ -16,7 +16,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 CSRC = os.path.join(PKG, "csrc")
-SOURCES = [os.path.join(CSRC, "mrr_v2.cu")]
+SOURCES = [os.path.join(CSRC, "mrr_v2.cu"), os.path.join(CSRC, "mrr_v2_noalloc.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, "ptx.cuh"), os.path.join(INCLUDE, "mrr_v2.h")]
 LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libmrr_v2.so")

@@ -102,6 +102,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                                     P, P, P, P, P, I64, P, ctypes.c_size_t, P]
     lib.mrr_v2_read_status.restype = I32
     lib.mrr_v2_read_status.argtypes = [P, ctypes.c_size_t, P]
+    lib.mrr_v2_run_noalloc.restype = I32
+    lib.mrr_v2_run_noalloc.argtypes = [P, I32, I64, I64, P, I32, I64, I64, P, I32, I64, P,
+                                       P, P, P, P, P, I64, I64, I32, P]
     if path == _build.LIB_PATH:
         _lib = lib
     return lib
@@ -150,6 +153,18 @@ def mrr_v2_run_plan(plan: mrr_v2_plan_t, tokens, dt, counts, scales, topk_w, per
 
 def mrr_v2_read_status(workspace, workspace_bytes, stream) -> int:
     return load_library().mrr_v2_read_status(workspace, workspace_bytes, stream)
+
+
+def mrr_v2_run_noalloc(tokens, dt, A, H, counts, count_is_i64, N, E, scales, sl, scale_cols, topk_w,
+                       permute_tokens, permute_scales, permute_token_idx, expert_token_num,
+                       permute_topk_w, expert_token_num_type, idx_type, wait_and_check,
+                       stream) -> int:
+    """mrr_v2_run without a workspace, for callers that cannot allocate device memory: the
+    library's own fixed device array serves as scratch (see include/mrr_v2.h)."""
+    return load_library().mrr_v2_run_noalloc(
+        tokens, dt, A, H, counts, int(count_is_i64), N, E, scales, sl, scale_cols, topk_w,
+        permute_tokens, permute_scales, permute_token_idx, expert_token_num, permute_topk_w,
+        expert_token_num_type, idx_type, int(wait_and_check), stream)
 
 
 # ---------------------------------------------------------------------------- torch-level call

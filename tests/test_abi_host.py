@@ -25,7 +25,7 @@ def lib():
 def test_exports_every_header_function(lib):
     names = m.header_functions()
     assert set(names) == {"mrr_v2_plan", "mrr_v2_run", "mrr_v2_run_plan", "mrr_v2_read_status",
-                          "mrr_status_str"}
+                          "mrr_status_str", "mrr_v2_run_noalloc"}
     out = subprocess.run(["nm", "-D", "--defined-only", m.library_path()], capture_output=True,
                          text=True, check=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
