@@ -91,6 +91,10 @@ typedef enum mrr_scale_layout {
 #define MRR_PATH_BULK 1    /* cp.async.bulk global->shared->global, one driver thread per CTA  */
 #define MRR_PATH_VECTOR 2  /* all threads, widest aligned vector loads/stores (any alignment) */
 
+/* bulk-path L2 cache hints (plan.hints bits) */
+#define MRR_HINT_LOAD_EVICT_FIRST 1   /* token loads marked evict-first in L2  */
+#define MRR_HINT_STORE_EVICT_FIRST 2  /* token stores marked evict-first in L2 */
+
 /* Launch plan: plain data, owned by the caller.  mrr_v2_plan fills it; a caller may change the
  * tuning fields (path, grid, block, chunk_bytes, stages) and pass it to mrr_v2_run_plan, which
  * checks them again. */
@@ -98,7 +102,7 @@ typedef struct mrr_v2_plan {
     int64_t A, H, N, E;
     int64_t row_bytes;        /* bytes per token row: H * bits / 8                          */
     int64_t scale_row_bytes;  /* bytes per scale row; 0 without scales                      */
-    int64_t workspace_bytes;  /* device scratch mrr_v2_run needs (>= 4096: status region)   */
+    int64_t workspace_bytes;  /* device scratch mrr_v2_run needs (>= 4352: status + counter) */
     int32_t count_is_i64;
     int32_t scale_layout;
     int32_t has_topk;
@@ -109,7 +113,12 @@ typedef struct mrr_v2_plan {
     int32_t grid;             /* CTAs of the copy kernel (<= 1022)                            */
     int32_t block;            /* threads per CTA (multiple of 32, 64..1024)                   */
     int32_t chunk_bytes;      /* bulk path: bytes per pipeline stage (multiple of 16)         */
-    int32_t stages;           /* bulk path: pipeline depth (1..8)                             */
+    int32_t stages;           /* bulk path: pipeline depth (2..8)                             */
+    int32_t hints;            /* bulk path: MRR_HINT_* bits                                   */
+    int32_t sched;            /* bulk path: 0 = each CTA an equal slice of the token bytes;
+                                 1 = static_chunks chunks per CTA, then chunks claimed from a
+                                 counter in the workspace (balances uneven CTA speeds)        */
+    int32_t static_chunks;    /* bulk path, sched 1: chunks per CTA before claiming           */
     int32_t smem_bytes;       /* dynamic shared memory per CTA                                */
     int32_t num_sms;          /* SMs on the device the plan was made for                      */
 } mrr_v2_plan_t;
@@ -144,8 +153,9 @@ mrr_status mrr_v2_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int6
  *   expert_token_num  [E] counts' type, tokens per expert                (written)
  *   permute_topk_w  [A, 1] float32; NULL exactly when topk_w is NULL     (written if given)
  *   workspace       >= plan.workspace_bytes device bytes, 256-byte aligned, caller-owned;
- *                   it holds the status words read by mrr_v2_read_status and, for
- *                   N*E > 4096, the scanned offsets.
+ *                   it holds the status words read by mrr_v2_read_status, the chunk counter
+ *                   of the bulk path and, for N*E > 4096, the scanned offsets.  It needs no
+ *                   initialisation: each launch tags the counter with its own epoch.
  * Host-side errors return before anything is enqueued.  The empty problem (N*E = 0, A = 0)
  * only zero-fills expert_token_num.
  */
@@ -185,7 +195,7 @@ const char *mrr_status_str(mrr_status s);
 
 /* Limits of the fixed scratch used by mrr_v2_run_noalloc. */
 #define MRR_NOALLOC_MAX_SEGMENTS 16384   /* largest N*E it accepts                          */
-#define MRR_NOALLOC_SCRATCH_BYTES 135424 /* device bytes it holds on every GPU that loads
+#define MRR_NOALLOC_SCRATCH_BYTES 137984 /* device bytes it holds on every GPU that loads
                                             the library, until the process exits            */
 
 /*

@@ -30,6 +30,9 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+#include <chrono>
+
 #include "mrr_v2.h"
 #include "ptx.cuh"
 
@@ -37,6 +40,8 @@ namespace mrr {
 
 constexpr int kStatusBytes = 4096;                 // status region at the front of the workspace
 constexpr int kStatusWords = kStatusBytes / 4;     // [0] flags, [1] grid, [2 + b] CTA b's flags
+constexpr int kTicketOffset = kStatusBytes;        // 8-byte shared chunk counter (dynamic scheduling)
+constexpr int kHeaderBytes = kStatusBytes + 256;   // status region + counter; offset tables follow
 constexpr int kMaxGrid = kStatusWords - 2;
 constexpr int64_t kFusedMaxSegs = 4096;            // N*E scanned inside every CTA up to this
 constexpr uint32_t kFlagNonPos = 1u, kFlagSum = 2u, kFlagTimeout = 4u;
@@ -67,6 +72,11 @@ struct Params {
     uint32_t *g_dst_off;
     int chunk_bytes;
     int stages;
+    int hints;            // bulk path: MRR_HINT_* bits (L2 evict-first policies)
+    int sched;            // bulk path: 0 static slices, 1 static chunks then shared-counter chunks
+    int static_chunks;    // bulk path, sched 1: chunks each CTA takes before using the counter
+    unsigned long long *ticket;  // sched 1: shared chunk counter in the workspace
+    unsigned long long epoch;    // sched 1: this launch's tag for the counter (40 bits, nonzero)
 };
 
 // ------------------------------------------------------------------------------------------------
@@ -92,6 +102,18 @@ __device__ __forceinline__ int find_seg(const uint32_t *row_ex, int NE, uint32_t
             hi = mid;
     }
     return lo;
+}
+
+// Shared-memory index with one padding word per 32: walks with a stride that is a multiple of
+// 32 words (a column of the count matrix) then spread over the banks instead of hitting one.
+__device__ __forceinline__ int pad32(int k) { return k + (k >> 5); }
+__host__ __device__ constexpr int64_t padded_len(int64_t n) { return n + (n >> 5) + 1; }
+
+// Destination row of source row s.
+__device__ __forceinline__ int64_t dst_row(const uint32_t *row_ex, const uint32_t *dst_off, int NE, int64_t s)
+{
+    const int q = find_seg(row_ex, NE, (uint32_t)s);
+    return (int64_t)dst_off[pad32(q)] + (s - (int64_t)row_ex[q]);
 }
 
 // Exclusive block-wide scan of one uint32 per thread (warp shuffles + one smem pass).
@@ -126,34 +148,150 @@ __device__ __forceinline__ uint32_t block_exscan(uint32_t v, uint32_t *total, ui
     return base + x - v;
 }
 
-// Load and validate the counts, then build both prefixes in shared memory:
-//   row_ex[q]  = SrcOffset of segment q = i*E + j (row-major walk), row_ex[NE] = A
-//   dst_off[q] = DstOffset of segment q (column-major walk: expert outer, rank inner)
-// Returns the error flags (uniform over the block); the tables are valid when it returns 0.
-__device__ uint32_t cta_scan(const Params &p, uint32_t *cnt, uint32_t *row_ex, uint32_t *dst_off,
-                             uint32_t *s_warp, uint32_t *s_flags, unsigned long long *s_sum)
+// Exclusive scan over positions 0..n-1 of the block, read through in(k); out(k, prefix) receives
+// each exclusive prefix, in increasing k for each thread.  Warp w owns a contiguous span; inside
+// it each lane scans a run of kScanRun consecutive positions on its own, so one warp-shuffle
+// scan serves 32 * kScanRun positions.  Every thread of the block must call it.
+constexpr int kScanRun = 8;
+template <class In, class Out>
+__device__ __forceinline__ void block_scan_runs(int n, uint32_t *s_warp, In in, Out out)
 {
-    const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31;
-    const int NE = p.NE, N = p.N, E = p.E;
-    if (tid == 0) {
-        *s_flags = 0u;
-        *s_sum = 0ull;
-    }
-    __syncthreads();
-    uint32_t f = 0u;
-    unsigned long long sum = 0ull;
-    for (int k = tid; k < NE; k += nthr) {
-        const int64_t c = load_count(p, k);
-        uint32_t v = 0u;
-        if (c <= 0)
-            f |= kFlagNonPos;
-        else if (c > p.A)
-            f |= kFlagSum;
-        else {
-            v = (uint32_t)c;
-            sum += (unsigned long long)c;
+    constexpr int kTile = 32 * kScanRun;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = (blockDim.x + 31) >> 5;
+    const int span = ((n + nwarps - 1) / nwarps + kTile - 1) / kTile * kTile;
+    const int lo = min(n, warp * span), hi = min(n, lo + span);
+    uint32_t wsum = 0u;
+    for (int k = lo + lane; k < hi; k += 32)
+        wsum += in(k);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    uint32_t total;
+    uint32_t run = block_exscan(lane == 0 ? wsum : 0u, &total, s_warp);  // lane 0 carries the warp
+    run = __shfl_sync(0xffffffffu, run, 0);
+    for (int t = lo; t < hi; t += kTile) {
+        const int k0 = t + lane * kScanRun;
+        uint32_t x[kScanRun];
+        uint32_t local = 0u;
+#pragma unroll
+        for (int e = 0; e < kScanRun; ++e) {
+            x[e] = (k0 + e < hi) ? in(k0 + e) : 0u;
+            local += x[e];
         }
-        cnt[k] = v;
+        uint32_t incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += y;
+        }
+        uint32_t ex = run + incl - local;
+#pragma unroll
+        for (int e = 0; e < kScanRun; ++e) {
+            if (k0 + e < hi)
+                out(k0 + e, ex);
+            ex += x[e];
+        }
+        run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+}
+
+// The counts are loaded in batches: each thread has up to kCountBatch 16-byte vectors (4 int32
+// or 2 int64 counts each) in flight at once.  The first batch is issued before the token stream
+// starts, so these few loads do not queue behind it.
+constexpr int kCountBatch = 4;
+struct CountBatch {
+    uint4 raw[kCountBatch];
+};
+
+template <typename CT>
+__device__ __forceinline__ void issue_count_loads(const Params &p, int base, CountBatch &cb)
+{
+    constexpr int kPer = 16 / sizeof(CT);
+    const int tid = threadIdx.x, nthr = blockDim.x, NE = p.NE;
+    const CT *src = reinterpret_cast<const CT *>(p.counts);
+    const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
+#pragma unroll
+    for (int b = 0; b < kCountBatch; ++b) {
+        const int k0 = base + (b * nthr + tid) * kPer;
+        if (vec && k0 + kPer <= NE) {
+            cb.raw[b] = __ldg(reinterpret_cast<const uint4 *>(src + k0));
+        } else {
+            CT v[kPer];
+#pragma unroll
+            for (int e = 0; e < kPer; ++e)
+                v[e] = (k0 + e < NE) ? __ldg(src + k0 + e) : CT(1);
+            memcpy(&cb.raw[b], v, 16);
+        }
+    }
+}
+
+// Validate one batch and store each count twice: row-major at row_ex[q] (scanned in place
+// later) and column-major at cnt_t[pad32(j*N + i)].  Returns error flags; adds valid counts.
+template <typename CT>
+__device__ __forceinline__ uint32_t process_counts(const Params &p, int base, const CountBatch &cb,
+                                                   uint32_t *row_ex, uint32_t *cnt_t, unsigned long long *sum)
+{
+    constexpr int kPer = 16 / sizeof(CT);
+    const int tid = threadIdx.x, nthr = blockDim.x, NE = p.NE, N = p.N, E = p.E;
+    uint32_t f = 0u;
+#pragma unroll
+    for (int b = 0; b < kCountBatch; ++b) {
+        const int k0 = base + (b * nthr + tid) * kPer;
+        CT v[kPer];
+        memcpy(v, &cb.raw[b], 16);
+        int i = k0 / E, j = k0 - (k0 / E) * E;  // k0 = i*E + j
+#pragma unroll
+        for (int e = 0; e < kPer; ++e, ++j) {
+            if (j == E) {
+                j = 0;
+                ++i;
+            }
+            const int k = k0 + e;
+            if (k >= NE)
+                break;
+            const int64_t c = (int64_t)v[e];
+            uint32_t u32 = 0u;
+            if (c <= 0)
+                f |= kFlagNonPos;
+            else if (c > p.A)
+                f |= kFlagSum;
+            else {
+                u32 = (uint32_t)c;
+                *sum += (unsigned long long)c;
+            }
+            row_ex[k] = u32;
+            cnt_t[pad32(j * N + i)] = u32;
+        }
+    }
+    return f;
+}
+
+// Validate the counts (first batch already issued into `cb`), then build both prefixes in shared
+// memory:
+//   row_ex[q]          = SrcOffset of segment q = i*E + j (row-major walk), row_ex[NE] = A
+//   dst_off[pad32(q)]  = DstOffset of segment q (column-major walk: expert outer, rank inner)
+// *s_flags and *s_sum must be zero before the call.  Returns the error flags (uniform over the
+// block); the tables are valid when it returns 0.
+__device__ uint32_t cta_scan(const Params &p, CountBatch &cb, uint32_t *row_ex, uint32_t *cnt_t,
+                             uint32_t *dst_off, uint32_t *s_warp, uint32_t *s_flags, unsigned long long *s_sum)
+{
+    const int tid = threadIdx.x, lane = tid & 31, nthr = blockDim.x;
+    const int NE = p.NE, N = p.N, E = p.E;
+    const int stride = nthr * (p.count_is_i64 ? 2 : 4) * kCountBatch;
+    __syncthreads();  // *s_flags / *s_sum zeroed
+    unsigned long long sum = 0ull;
+    uint32_t f = 0u;
+    for (int base = 0; base < NE; base += stride) {
+        if (p.count_is_i64) {
+            if (base)
+                issue_count_loads<long long>(p, base, cb);
+            f |= process_counts<long long>(p, base, cb, row_ex, cnt_t, &sum);
+        } else {
+            if (base)
+                issue_count_loads<int>(p, base, cb);
+            f |= process_counts<int>(p, base, cb, row_ex, cnt_t, &sum);
+        }
     }
     f = __reduce_or_sync(0xffffffffu, f);
 #pragma unroll
@@ -172,31 +310,29 @@ __device__ uint32_t cta_scan(const Params &p, uint32_t *cnt, uint32_t *row_ex, u
     if (flags)
         return flags;  // uniform: every thread read the same smem values
 
-    // each thread scans a contiguous run of `per` positions
-    const int per = (NE + nthr - 1) / nthr;
-    const int k0 = min(NE, tid * per), k1 = min(NE, k0 + per);
-    uint32_t total;
-
-    uint32_t local = 0u;
-    for (int k = k0; k < k1; ++k)
-        local += cnt[k];
-    uint32_t run = block_exscan(local, &total, s_warp);
-    for (int k = k0; k < k1; ++k) {
-        row_ex[k] = run;
-        run += cnt[k];
-    }
+    // SrcOffset: row-major exclusive prefix, in place (each element is read before it is written)
+    block_scan_runs(
+        NE, s_warp, [&](int k) { return row_ex[k]; }, [&](int k, uint32_t v) { row_ex[k] = v; });
     if (tid == 0)
         row_ex[NE] = (uint32_t)p.A;
-
-    local = 0u;
-    for (int pos = k0; pos < k1; ++pos)
-        local += cnt[(pos % N) * E + pos / N];
-    run = block_exscan(local, &total, s_warp);
-    for (int pos = k0; pos < k1; ++pos) {
-        const int q = (pos % N) * E + pos / N;
-        dst_off[q] = run;
-        run += cnt[q];
-    }
+    // DstOffset: exclusive prefix over the column-major copy, stored at pad32(q), q = i*E + j.
+    // Each thread's positions come in increasing runs, so (i, j) of pos = j*N + i is stepped.
+    int ci = -1, cj = 0, cpos = -2;
+    block_scan_runs(
+        NE, s_warp, [&](int pos) { return cnt_t[pad32(pos)]; },
+        [&](int pos, uint32_t v) {
+            if (pos == cpos + 1) {
+                if (++ci == N) {
+                    ci = 0;
+                    ++cj;
+                }
+            } else {
+                cj = pos / N;
+                ci = pos - cj * N;
+            }
+            cpos = pos;
+            dst_off[pad32(ci * E + cj)] = v;
+        });
     __syncthreads();
     return 0u;
 }
@@ -207,8 +343,8 @@ __device__ __forceinline__ void write_expert_token_num(const Params &p, const ui
                                                        int ts)
 {
     for (int j = t0; j < p.E; j += ts) {
-        const uint32_t next = (j + 1 < p.E) ? dst_off[j + 1] : (uint32_t)p.A;
-        const uint32_t v = next - dst_off[j];
+        const uint32_t next = (j + 1 < p.E) ? dst_off[pad32(j + 1)] : (uint32_t)p.A;
+        const uint32_t v = next - dst_off[pad32(j)];
         if (p.count_is_i64)
             reinterpret_cast<long long *>(p.etn)[j] = (long long)v;
         else
@@ -236,42 +372,6 @@ __device__ __forceinline__ void copy_unit(uint8_t *d, const uint8_t *s, int w)
         break;
     }
 }
-
-// Scale rows, top-k weights and the index for this CTA's share of the SOURCE rows,
-// processed by threads t0, t0 + ts, ... of the block.
-__device__ void side_arrays(const Params &p, const uint32_t *row_ex, const uint32_t *dst_off, int t0, int ts)
-{
-    const int64_t G = gridDim.x, b = blockIdx.x;
-    const int64_t r_lo = b * p.A / G, r_hi = (b + 1) * p.A / G;
-    for (int64_t s = r_lo + t0; s < r_hi; s += ts) {
-        const int q = find_seg(row_ex, p.NE, (uint32_t)s);
-        const int64_t d = (int64_t)dst_off[q] + (s - (int64_t)row_ex[q]);
-        if (p.idx_type == 0)
-            p.idx[d] = (int32_t)s;  // gather index: out[d] = in[idx[d]]
-        else
-            p.idx[s] = (int32_t)d;  // scatter index: out[idx[s]] = in[s]
-        if (p.topk) {
-            for (int k = 0; k < 4; k += p.topk_w)
-                copy_unit(p.out_topk + d * 4 + k, p.topk + s * 4 + k, p.topk_w);
-        }
-    }
-    if (p.scales) {
-        const int w = p.scale_w;
-        const int64_t sb = p.scale_row_bytes, vpr = sb / w;
-        const int64_t items = (r_hi - r_lo) * vpr;
-        for (int64_t t = t0; t < items; t += ts) {
-            const int64_t r = t / vpr;
-            const int64_t v = t - r * vpr;
-            const int64_t s = r_lo + r;
-            const int q = find_seg(row_ex, p.NE, (uint32_t)s);
-            const int64_t d = (int64_t)dst_off[q] + (s - (int64_t)row_ex[q]);
-            copy_unit(p.out_scales + d * sb + v * w, p.scales + s * sb + v * w, w);
-        }
-    }
-}
-
-// ------------------------------------------------------------------------------------------------
-// vector path: cooperative copy of one contiguous run
 
 template <int W>
 struct Vec;
@@ -305,6 +405,102 @@ struct Vec<1> {
     static __device__ __forceinline__ void st(uint8_t *p, uint8_t v) { *p = v; }
     using T = uint8_t;
 };
+
+constexpr int kSideBatch = 4;  // rows (or scale vectors) per thread with their loads in flight
+
+// Scale vectors of width W (16, 8 or 4 bytes, both pointers aligned to W) for source rows
+// [r_lo, r_hi): kSideBatch loads in flight per thread, then the stores.
+template <int W>
+__device__ void move_scales(const Params &p, const uint32_t *row_ex, const uint32_t *dst_off, int64_t r_lo,
+                            int64_t r_hi, int t0, int ts)
+{
+    const int64_t sb = p.scale_row_bytes, vpr = sb / W;
+    const int64_t items = (r_hi - r_lo) * vpr;
+    for (int64_t t = t0; t < items; t += (int64_t)ts * kSideBatch) {
+        typename Vec<W>::T v[kSideBatch];
+        int64_t s[kSideBatch], off[kSideBatch];
+#pragma unroll
+        for (int u = 0; u < kSideBatch; ++u) {
+            const int64_t it = t + (int64_t)u * ts;
+            if (it < items) {
+                const int64_t r = it / vpr;
+                s[u] = r_lo + r;
+                off[u] = (it - r * vpr) * W;
+                v[u] = Vec<W>::ld(p.scales + s[u] * sb + off[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kSideBatch; ++u) {
+            if (t + (int64_t)u * ts < items) {
+                const int64_t d = dst_row(row_ex, dst_off, p.NE, s[u]);
+                Vec<W>::st(p.out_scales + d * sb + off[u], v[u]);
+            }
+        }
+    }
+}
+
+// Scale rows, top-k weights and the index for this CTA's share of the SOURCE rows,
+// processed by threads t0, t0 + ts, ... of the block.
+__device__ void side_arrays(const Params &p, const uint32_t *row_ex, const uint32_t *dst_off, int t0, int ts)
+{
+    const int64_t G = gridDim.x, b = blockIdx.x;
+    const int64_t r_lo = b * p.A / G, r_hi = (b + 1) * p.A / G;
+    const bool topk4 = p.topk && p.topk_w == 4;
+    for (int64_t base = r_lo + t0; base < r_hi; base += (int64_t)ts * kSideBatch) {
+        uint32_t w[kSideBatch];
+#pragma unroll
+        for (int u = 0; u < kSideBatch; ++u) {
+            const int64_t s = base + (int64_t)u * ts;
+            if (topk4 && s < r_hi)
+                w[u] = __ldg(reinterpret_cast<const uint32_t *>(p.topk) + s);
+        }
+#pragma unroll
+        for (int u = 0; u < kSideBatch; ++u) {
+            const int64_t s = base + (int64_t)u * ts;
+            if (s >= r_hi)
+                break;
+            const int64_t d = dst_row(row_ex, dst_off, p.NE, s);
+            if (p.idx_type == 0)
+                p.idx[d] = (int32_t)s;  // gather index: out[d] = in[idx[d]]
+            else
+                p.idx[s] = (int32_t)d;  // scatter index: out[idx[s]] = in[s]
+            if (topk4)
+                reinterpret_cast<uint32_t *>(p.out_topk)[d] = w[u];
+            else if (p.topk) {
+                for (int k = 0; k < 4; k += p.topk_w)
+                    copy_unit(p.out_topk + d * 4 + k, p.topk + s * 4 + k, p.topk_w);
+            }
+        }
+    }
+    if (!p.scales)
+        return;
+    switch (p.scale_w) {
+    case 16:
+        move_scales<16>(p, row_ex, dst_off, r_lo, r_hi, t0, ts);
+        break;
+    case 8:
+        move_scales<8>(p, row_ex, dst_off, r_lo, r_hi, t0, ts);
+        break;
+    case 4:
+        move_scales<4>(p, row_ex, dst_off, r_lo, r_hi, t0, ts);
+        break;
+    default: {  // 1- or 2-byte aligned scale rows
+        const int w = p.scale_w;
+        const int64_t sb = p.scale_row_bytes, vpr = sb / w;
+        const int64_t items = (r_hi - r_lo) * vpr;
+        for (int64_t t = t0; t < items; t += ts) {
+            const int64_t r = t / vpr;
+            const int64_t v = t - r * vpr;
+            const int64_t s = r_lo + r;
+            const int64_t d = dst_row(row_ex, dst_off, p.NE, s);
+            copy_unit(p.out_scales + d * sb + v * w, p.scales + s * sb + v * w, w);
+        }
+    }
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// vector path: cooperative copy of one contiguous run
 
 // dst and src are congruent modulo W: bytes up to dst's W boundary, W-wide body, byte tail
 template <int W>
@@ -360,12 +556,12 @@ __device__ void vector_copy(const Params &p, const uint32_t *row_ex, const uint3
     const int64_t rb = p.row_bytes;
     int q = find_seg(row_ex, p.NE, (uint32_t)(lo / rb));
     int64_t seg_end = (int64_t)row_ex[q + 1] * rb;
-    int64_t delta = ((int64_t)dst_off[q] - (int64_t)row_ex[q]) * rb;
+    int64_t delta = ((int64_t)dst_off[pad32(q)] - (int64_t)row_ex[q]) * rb;
     for (int64_t pos = lo; pos < hi;) {
         while (pos >= seg_end) {
             ++q;
             seg_end = (int64_t)row_ex[q + 1] * rb;
-            delta = ((int64_t)dst_off[q] - (int64_t)row_ex[q]) * rb;
+            delta = ((int64_t)dst_off[pad32(q)] - (int64_t)row_ex[q]) * rb;
         }
         const int64_t pe = min(hi, seg_end);
         copy_block(p.out_tokens + pos + delta, p.tokens + pos, pe - pos, tid, nthr);
@@ -375,62 +571,170 @@ __device__ void vector_copy(const Params &p, const uint32_t *row_ex, const uint3
 
 // ------------------------------------------------------------------------------------------------
 // bulk path: one driver thread per CTA
+//
+// Chunks of chunk_bytes source bytes move through a ring of `stages` shared-memory buffers.
+// Scheduling (plan.sched):
+//   0  static: CTA b owns an equal 16-byte-aligned slice of the token bytes;
+//   1  dynamic: CTA b first takes the static_chunks chunks starting at chunk b*static_chunks,
+//      then claims further chunks from a counter shared by all CTAs, so CTAs whose memory
+//      traffic drains faster take more chunks and all finish together.
+
+constexpr int kTicketBits = 24;  // shared counter: [epoch of the launch | ticket (low 24 bits)]
+constexpr unsigned long long kTicketMask = (1ull << kTicketBits) - 1;
+constexpr uint32_t kNoTicket = 0xFFFFFFFFu;
+
+// First claim of this launch on the shared counter.  The counter still holds the epoch of the
+// launch that used it last (or anything, in a fresh workspace); the first claimant installs
+// (epoch, 1) with a compare-and-swap and takes ticket 0, later claimants see the epoch and add.
+// Every launch has a different epoch, so no reset pass is needed.  Bounded: kNoTicket on failure.
+__device__ uint32_t claim_first_ticket(unsigned long long *ticket, unsigned long long epoch)
+{
+    unsigned long long cur = atomicAdd(ticket, 0ull);
+    for (int it = 0; it < (1 << 16); ++it) {
+        if ((cur >> kTicketBits) == epoch)
+            return (uint32_t)(atomicAdd(ticket, 1ull) & kTicketMask);
+        const unsigned long long prev = atomicCAS(ticket, cur, (epoch << kTicketBits) | 1ull);
+        if (prev == cur)
+            return 0u;
+        cur = prev;
+    }
+    return kNoTicket;
+}
 
 struct BulkRing {
     uint64_t *bars;
     uint8_t *base;
-    int64_t lo, hi, nch;
-    int64_t issued;  // loads issued so far (chunks 0 .. issued-1)
+    int64_t *stage_b0, *stage_b1;  // shared memory: byte range held by each stage
+    int64_t issued;                // chunk loads issued so far (sequence numbers 0 .. issued-1)
+    uint64_t policy;               // L2 evict-first policy, used when hints ask for it
+    int64_t next, hi;              // static part: next byte to load and the end of the range
+    int64_t dyn_first;             // first chunk id served by tickets; -1 when none (left)
+    int64_t nch;                   // chunks in the whole token buffer
+    uint32_t pending[2];           // the next two tickets, claimed ahead of use
+    bool started;                  // the first ticket has been taken
+    int64_t tk_next, tk_end;       // chunk ids of the current ticket not yet served
+    int per_ticket;                // consecutive chunks per ticket (about 64 KiB per claim)
 };
 
-__device__ __forceinline__ void bulk_issue_load(const Params &p, BulkRing &r, int64_t c)
+// Next chunk of this CTA as the byte range [*b0, *b1); false when the CTA has no more work.
+__device__ bool next_chunk(const Params &p, BulkRing &r, volatile uint32_t *s_first, int64_t *b0, int64_t *b1,
+                           uint32_t *tflag)
 {
-    const int S = p.stages;
     const int64_t C = p.chunk_bytes;
-    const int st = (int)(c % S);
-    const int64_t b0 = r.lo + c * C;
-    const uint32_t bytes = (uint32_t)min(C, r.hi - b0);
+    if (r.next < r.hi) {
+        *b0 = r.next;
+        *b1 = min(r.next + C, r.hi);
+        r.next = *b1;
+        return true;
+    }
+    if (r.dyn_first < 0)
+        return false;
+    if (r.tk_next >= r.tk_end) {
+        uint32_t t;
+        if (!r.started) {
+            // the first ticket is claimed by warp 1 (off this thread's path) and handed over in smem
+            const uint64_t t0 = global_timer_ns();
+            while (s_first[1] == 0u) {
+                if (global_timer_ns() - t0 > kWaitLimitNs) {
+                    *tflag |= kFlagTimeout;
+                    r.dyn_first = -1;
+                    return false;
+                }
+            }
+            t = s_first[0];
+            r.started = true;
+            // keep two claims in flight: a ticket is read two tickets after its atomic was issued
+            r.pending[0] = (uint32_t)(atomicAdd(p.ticket, 1ull) & kTicketMask);
+            r.pending[1] = (uint32_t)(atomicAdd(p.ticket, 1ull) & kTicketMask);
+        } else {
+            t = r.pending[0];
+            r.pending[0] = r.pending[1];
+            r.pending[1] = (uint32_t)(atomicAdd(p.ticket, 1ull) & kTicketMask);
+        }
+        if (t == kNoTicket) {
+            *tflag |= kFlagTimeout;
+            r.dyn_first = -1;
+            return false;
+        }
+        r.tk_next = r.dyn_first + (int64_t)t * r.per_ticket;
+        r.tk_end = min(r.nch, r.tk_next + r.per_ticket);
+        if (r.tk_next >= r.nch) {
+            r.dyn_first = -1;
+            return false;
+        }
+    }
+    const int64_t id = r.tk_next++;
+    *b0 = id * C;
+    *b1 = min(*b0 + C, p.total_bytes);
+    return true;
+}
+
+__device__ __forceinline__ void bulk_issue_load(const Params &p, BulkRing &r, int64_t b0, int64_t b1)
+{
+    const int st = (int)(r.issued % p.stages);
+    const uint32_t bytes = (uint32_t)(b1 - b0);
     const uint32_t bar = smem_addr(&r.bars[st]);
+    const uint32_t dst = smem_addr(r.base + (size_t)st * p.chunk_bytes);
+    r.stage_b0[st] = b0;
+    r.stage_b1[st] = b1;
     mbar_arrive_expect_tx(bar, bytes);
-    bulk_g2s(smem_addr(r.base + (size_t)st * C), p.tokens + b0, bytes, bar);
-    r.issued = c + 1;
+    if (p.hints & MRR_HINT_LOAD_EVICT_FIRST)
+        bulk_g2s_hint(dst, p.tokens + b0, bytes, bar, r.policy);
+    else
+        bulk_g2s(dst, p.tokens + b0, bytes, bar);
+    ++r.issued;
 }
 
 __device__ uint32_t bulk_driver(const Params &p, BulkRing &r, const uint32_t *row_ex, const uint32_t *dst_off,
-                                uint32_t flags)
+                                uint32_t flags, volatile uint32_t *s_first)
 {
     const int S = p.stages;
-    const int64_t C = p.chunk_bytes, rb = p.row_bytes;
+    const int64_t rb = p.row_bytes;
     int64_t consumed = 0;
     uint32_t tflag = 0u;
-    if (!flags && r.nch > 0) {
-        int q = find_seg(row_ex, p.NE, (uint32_t)(r.lo / rb));
-        int64_t seg_end = (int64_t)row_ex[q + 1] * rb;
-        int64_t delta = ((int64_t)dst_off[q] - (int64_t)row_ex[q]) * rb;
-        for (int64_t c = 0; c < r.nch; ++c) {
-            const int st = (int)(c % S);
-            if (!mbar_wait_bounded(smem_addr(&r.bars[st]), (uint32_t)((c / S) & 1), kWaitLimitNs)) {
-                tflag = kFlagTimeout;
+    if (!flags) {
+        bool more = true;
+        int64_t b0, b1;
+        // stages the pre-scan prologue left empty (fewer static chunks than stages)
+        while (more && r.issued < S) {
+            more = next_chunk(p, r, s_first, &b0, &b1, &tflag);
+            if (more)
+                bulk_issue_load(p, r, b0, b1);
+        }
+        for (int64_t n = 0; n < r.issued; ++n) {
+            const int st = (int)(n % S);
+            if (!mbar_wait_bounded(smem_addr(&r.bars[st]), (uint32_t)((n / S) & 1), kWaitLimitNs)) {
+                tflag |= kFlagTimeout;
                 break;
             }
-            consumed = c + 1;
-            const int64_t b0 = r.lo + c * C, b1 = min(b0 + C, r.hi);
-            const uint32_t sbase = smem_addr(r.base + (size_t)st * C);
-            for (int64_t pos = b0; pos < b1;) {
-                while (pos >= seg_end) {
-                    ++q;
-                    seg_end = (int64_t)row_ex[q + 1] * rb;
-                    delta = ((int64_t)dst_off[q] - (int64_t)row_ex[q]) * rb;
-                }
-                const int64_t pe = min(b1, seg_end);
-                bulk_s2g(p.out_tokens + pos + delta, sbase + (uint32_t)(pos - b0), (uint32_t)(pe - pos));
+            consumed = n + 1;
+            const int64_t c0 = r.stage_b0[st], c1 = r.stage_b1[st];
+            const uint32_t sbase = smem_addr(r.base + (size_t)st * p.chunk_bytes);
+            // one bulk store per piece: the part of the chunk inside one segment
+            int q = find_seg(row_ex, p.NE, (uint32_t)(c0 / rb));
+            for (int64_t pos = c0; pos < c1; ++q) {
+                const int64_t seg_end = (int64_t)row_ex[q + 1] * rb;
+                const int64_t delta = ((int64_t)dst_off[pad32(q)] - (int64_t)row_ex[q]) * rb;
+                const int64_t pe = min(c1, seg_end);
+                if (p.hints & MRR_HINT_STORE_EVICT_FIRST)
+                    bulk_s2g_hint(p.out_tokens + pos + delta, sbase + (uint32_t)(pos - c0), (uint32_t)(pe - pos),
+                                  r.policy);
+                else
+                    bulk_s2g(p.out_tokens + pos + delta, sbase + (uint32_t)(pos - c0), (uint32_t)(pe - pos));
                 pos = pe;
             }
             bulk_commit();
-            // the stage of chunk c-1 is free once its stores have read it: refill it
-            if (c >= 1 && c - 1 + S < r.nch) {
-                bulk_wait_read<1>();
-                bulk_issue_load(p, r, c - 1 + S);
+            // refill each stage whose previous chunk (sequence issued - S <= n - 1) has been read out
+            bool waited = false;
+            while (more && r.issued <= n - 1 + S) {
+                more = next_chunk(p, r, s_first, &b0, &b1, &tflag);
+                if (!more)
+                    break;
+                if (!waited) {
+                    bulk_wait_read<1>();
+                    waited = true;
+                }
+                bulk_issue_load(p, r, b0, b1);
             }
         }
     }
@@ -449,14 +753,16 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ uint64_t bars[kMaxStages];
+    __shared__ int64_t stage_b0[kMaxStages], stage_b1[kMaxStages];
     __shared__ uint32_t s_warp[32];
     __shared__ uint32_t s_flags;
     __shared__ unsigned long long s_sum;
+    __shared__ volatile uint32_t s_first[2];  // [0] first ticket of this CTA, [1] set once [0] is valid
 
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int64_t G = gridDim.x, b = blockIdx.x;
 
-    // this CTA's slice of the source bytes, in 16-byte units
+    // this CTA's slice of the source bytes, in 16-byte units (static scheduling, vector path)
     const int64_t units = (p.total_bytes + 15) >> 4;
     const int64_t lo = min(p.total_bytes, (b * units / G) << 4);
     const int64_t hi = (b == G - 1) ? p.total_bytes : min(p.total_bytes, ((b + 1) * units / G) << 4);
@@ -464,27 +770,61 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
     BulkRing ring;
     ring.bars = bars;
     ring.base = smem;
-    ring.lo = lo;
-    ring.hi = hi;
-    ring.nch = kBulk ? (hi - lo + p.chunk_bytes - 1) / p.chunk_bytes : 0;
+    ring.stage_b0 = stage_b0;
+    ring.stage_b1 = stage_b1;
     ring.issued = 0;
+    ring.policy = 0;
+    ring.pending[0] = ring.pending[1] = 0u;
+    ring.tk_next = ring.tk_end = 0;
+    ring.per_ticket = (int)max(1, min(64, 65536 / p.chunk_bytes));
+    ring.started = false;
+    ring.nch = (p.total_bytes + p.chunk_bytes - 1) / p.chunk_bytes;
+    const bool dynamic = kBulk && p.sched == 1;
+    if (dynamic) {
+        const int64_t span = (int64_t)p.static_chunks * p.chunk_bytes;
+        ring.next = min(p.total_bytes, b * span);
+        ring.hi = min(p.total_bytes, (b + 1) * span);
+        ring.dyn_first = (G * span < p.total_bytes) ? G * (int64_t)p.static_chunks : -1;
+    } else {
+        ring.next = lo;
+        ring.hi = hi;
+        ring.dyn_first = -1;
+    }
     uint32_t *tab = reinterpret_cast<uint32_t *>(smem + (kBulk ? (size_t)p.stages * p.chunk_bytes : 0));
 
+    CountBatch cb;
+    if (tid == 0)
+        s_first[1] = 0u;
+    if (kFused) {
+        if (tid == 0) {
+            s_flags = 0u;
+            s_sum = 0ull;
+        }
+        if (p.count_is_i64)
+            issue_count_loads<long long>(p, 0, cb);
+        else
+            issue_count_loads<int>(p, 0, cb);
+    }
+
     if (kBulk && tid == 0) {
+        if (p.hints)
+            ring.policy = policy_evict_first();
         for (int s = 0; s < p.stages; ++s)
             mbar_init(smem_addr(&bars[s]), 1u);
         mbar_init_fence();
-        // source addresses need no offsets: start streaming before the scan
-        const int64_t first = min((int64_t)p.stages, ring.nch);
-        for (int64_t c = 0; c < first; ++c)
-            bulk_issue_load(p, ring, c);
+        // source addresses need no offsets: start streaming the static chunks before the scan
+        while (ring.issued < p.stages && ring.next < ring.hi) {
+            const int64_t b0 = ring.next, b1 = min(ring.next + p.chunk_bytes, ring.hi);
+            ring.next = b1;
+            bulk_issue_load(p, ring, b0, b1);
+        }
     }
 
     uint32_t flags;
     const uint32_t *row_ex, *dst_off;
     if (kFused) {
-        uint32_t *cnt = tab, *rex = tab + p.NE, *dof = tab + 2 * p.NE + 1;
-        flags = cta_scan(p, cnt, rex, dof, s_warp, &s_flags, &s_sum);
+        uint32_t *rex = tab, *cnt_t = tab + p.NE + 1, *dof = cnt_t + padded_len(p.NE);
+        flags = cta_scan(p, cb, rex, cnt_t, dof, s_warp, &s_flags, &s_sum);
         row_ex = rex;
         dst_off = dof;
         if (b == 0) {
@@ -496,6 +836,7 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
             }
         }
     } else {
+        __syncthreads();  // s_first[1] cleared before warp 1 may set it
         flags = *reinterpret_cast<volatile uint32_t *>(p.status);  // written by the scan kernel
         row_ex = p.g_row_ex;
         dst_off = p.g_dst_off;
@@ -505,10 +846,16 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
 
     uint32_t tflag = 0u;
     if (kBulk) {
-        if (tid == 0)
-            tflag = bulk_driver(p, ring, row_ex, dst_off, flags);
-        else if (tid >= 32 && !flags)
+        if (tid == 0) {
+            tflag = bulk_driver(p, ring, row_ex, dst_off, flags, s_first);
+        } else if (tid >= 32 && !flags) {
+            if (tid == 32 && dynamic && ring.dyn_first >= 0) {
+                s_first[0] = claim_first_ticket(p.ticket, p.epoch);
+                __threadfence_block();
+                s_first[1] = 1u;
+            }
             side_arrays(p, row_ex, dst_off, tid - 32, nthr - 32);
+        }
     } else if (!flags) {
         vector_copy(p, row_ex, dst_off, lo, hi, tid, nthr);
         side_arrays(p, row_ex, dst_off, tid, nthr);
@@ -579,7 +926,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(const Params p)
         const uint32_t v = pos < NE ? (uint32_t)load_count(p, q) : 0u;
         const uint32_t ex = block_exscan(v, &total, s_warp);
         if (pos < NE)
-            p.g_dst_off[q] = carry + ex;
+            p.g_dst_off[pad32(q)] = carry + ex;
         carry += total;
     }
     __syncthreads();  // global writes of the block visible to the whole block
@@ -617,6 +964,9 @@ int token_bits(int dt)
 }
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+// workspace bytes of the two offset tables for N*E > 4096: SrcOffset dense, DstOffset padded
+int64_t table_workspace_bytes(int64_t NE) { return round_up(4 * (NE + 1), 256) + round_up(4 * padded_len(NE), 256); }
 
 int widest_width(uintptr_t a, uintptr_t b, int64_t bytes, int cap)
 {
@@ -696,9 +1046,30 @@ mrr_status check_buffers(int64_t NE, int64_t E, int cb, int sl, const void *toke
         return MRR_ERR_NULL;
     if (((uintptr_t)counts % cb) || ((uintptr_t)etn % cb) || ((uintptr_t)idx % 4))
         return MRR_ERR_ALIGN;
-    if (!workspace || ((uintptr_t)workspace % 256) || workspace_bytes < (size_t)kStatusBytes)
+    if (!workspace || ((uintptr_t)workspace % 256) || workspace_bytes < (size_t)kHeaderBytes)
         return MRR_ERR_WORKSPACE;
     return MRR_OK;
+}
+
+// A fresh 40-bit tag for every launch: it marks the shared chunk counter as belonging to that
+// launch, so stale counter values from earlier launches (or a fresh workspace) are recognised.
+unsigned long long next_launch_epoch()
+{
+    static std::atomic<unsigned long long> counter{0};
+    static const unsigned long long seed = [] {
+        unsigned long long x = (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count();
+        x ^= (unsigned long long)(uintptr_t)&counter;
+        x += 0x9E3779B97F4A7C15ull;  // splitmix64 finaliser
+        x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
+        x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
+        return x ^ (x >> 31);
+    }();
+    const unsigned long long mask = (1ull << (64 - kTicketBits)) - 1;
+    for (;;) {
+        const unsigned long long e = (seed + counter.fetch_add(1)) & mask;
+        if (e)
+            return e;
+    }
 }
 
 constexpr int kNumKernels = 5;
@@ -802,20 +1173,35 @@ mrr_status mrr_v2_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int6
     p.fuse_scan = NE <= kFusedMaxSegs ? 1 : 0;
     p.path = (rb % 16 == 0) ? MRR_PATH_BULK : MRR_PATH_VECTOR;
     p.num_sms = sms;
-    p.chunk_bytes = 32768;
-    p.stages = 4;
-    const int64_t table_bytes = p.fuse_scan ? round_up((3 * NE + 1) * 4, 128) : 0;
+    const int64_t table_bytes = p.fuse_scan ? round_up(4 * (NE + 1 + 2 * padded_len(NE)), 128) : 0;
     if (p.path == MRR_PATH_BULK) {
-        p.block = 256;
+        // the deepest ring shared memory allows: 3 x 64 KiB, else 3 x 48 KiB, else 4 x 32 KiB, ...
+        // More threads when the in-CTA scan of many segments is long.
+        p.block = NE > 1024 ? 512 : 256;
+        p.hints = MRR_HINT_LOAD_EVICT_FIRST;
+        p.chunk_bytes = 65536;
+        p.stages = 3;
+        if ((int64_t)p.stages * p.chunk_bytes + table_bytes > optin - 1024)
+            p.chunk_bytes = 49152;
+        if ((int64_t)p.stages * p.chunk_bytes + table_bytes > optin - 1024) {
+            p.chunk_bytes = 32768;
+            p.stages = 4;
+        }
         while (p.stages > 2 && (int64_t)p.stages * p.chunk_bytes + table_bytes > optin - 1024)
             --p.stages;
         while (p.chunk_bytes > 4096 && (int64_t)p.stages * p.chunk_bytes + table_bytes > optin - 1024)
             p.chunk_bytes /= 2;
+        // dynamic chunk scheduling unless the counter's 24-bit ticket space could run out
+        p.static_chunks = p.stages + 1;
+        const int64_t nch = (total + p.chunk_bytes - 1) / p.chunk_bytes;
+        p.sched = (nch + kMaxGrid < (int64_t)kTicketMask) ? 1 : 0;
         p.smem_bytes = (int32_t)((int64_t)p.stages * p.chunk_bytes + table_bytes);
         const int64_t want = (total + 65535) / 65536;
         p.grid = (int32_t)(want < 1 ? 1 : (want > sms ? sms : want));
     } else {
         p.block = 512;
+        p.chunk_bytes = 32768;
+        p.stages = 4;
         p.smem_bytes = (int32_t)table_bytes;
         const int64_t want = (total + 65535) / 65536;
         const int64_t cap = 2 * (int64_t)sms;
@@ -823,7 +1209,7 @@ mrr_status mrr_v2_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int6
     }
     if (p.grid > kMaxGrid)
         p.grid = kMaxGrid;
-    p.workspace_bytes = kStatusBytes + (p.fuse_scan ? 0 : round_up(4 * (NE + 1), 256) + round_up(4 * NE, 256));
+    p.workspace_bytes = kHeaderBytes + (p.fuse_scan ? 0 : table_workspace_bytes(NE));
     *out = p;
     return MRR_OK;
 }
@@ -859,12 +1245,14 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
         return MRR_ERR_WORKSPACE;
 
     // plan fields
-    const int64_t table_bytes = pl.fuse_scan ? round_up((3 * NE + 1) * 4, 128) : 0;
+    const int64_t table_bytes = pl.fuse_scan ? round_up(4 * (NE + 1 + 2 * padded_len(NE)), 128) : 0;
     if (pl.fuse_scan != (NE <= kFusedMaxSegs ? 1 : 0))
         return MRR_ERR_PLAN;
-    if (pl.workspace_bytes < kStatusBytes + (pl.fuse_scan ? 0 : round_up(4 * (NE + 1), 256) + round_up(4 * NE, 256)))
+    if (pl.workspace_bytes < kHeaderBytes + (pl.fuse_scan ? 0 : table_workspace_bytes(NE)))
         return MRR_ERR_PLAN;
     if (pl.grid < 1 || pl.grid > kMaxGrid || pl.block < 64 || pl.block > 1024 || pl.block % 32)
+        return MRR_ERR_PLAN;
+    if (pl.hints & ~(MRR_HINT_LOAD_EVICT_FIRST | MRR_HINT_STORE_EVICT_FIRST))
         return MRR_ERR_PLAN;
     int path = pl.path;
     const bool aligned16 = rb % 16 == 0 && ((uintptr_t)tokens % 16) == 0 && ((uintptr_t)permute_tokens % 16) == 0;
@@ -879,6 +1267,13 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
         if (pl.stages < 2 || pl.stages > kMaxStages || pl.chunk_bytes < 16 || pl.chunk_bytes % 16 ||
             pl.chunk_bytes > (1 << 20))
             return MRR_ERR_PLAN;
+        if (pl.sched != 0 && pl.sched != 1)
+            return MRR_ERR_PLAN;
+        if (pl.sched == 1) {
+            const int64_t nch = (A * rb + pl.chunk_bytes - 1) / pl.chunk_bytes;
+            if (pl.static_chunks < 1 || pl.static_chunks > (1 << 20) || nch + kMaxGrid >= (int64_t)kTicketMask)
+                return MRR_ERR_PLAN;
+        }
         smem += (int64_t)pl.stages * pl.chunk_bytes;
     }
 
@@ -936,8 +1331,13 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
     p.status = status;
     p.chunk_bytes = pl.chunk_bytes;
     p.stages = pl.stages;
+    p.hints = pl.hints;
+    p.sched = pl.sched;
+    p.static_chunks = pl.static_chunks;
+    p.ticket = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(workspace) + kTicketOffset);
+    p.epoch = (path == MRR_PATH_BULK && pl.sched == 1) ? next_launch_epoch() : 0ull;
     if (!pl.fuse_scan) {
-        uint8_t *ws = static_cast<uint8_t *>(workspace) + kStatusBytes;
+        uint8_t *ws = static_cast<uint8_t *>(workspace) + kHeaderBytes;
         p.g_row_ex = reinterpret_cast<uint32_t *>(ws);
         p.g_dst_off = reinterpret_cast<uint32_t *>(ws + round_up(4 * (NE + 1), 256));
     }

@@ -36,6 +36,7 @@ MRR_ERR_TIMEOUT = 18
 MRR_F16, MRR_BF16, MRR_I8, MRR_F8E5M2, MRR_F8E4M3FN, MRR_HIF8, MRR_F4E2M1, MRR_F4E1M2 = range(8)
 MRR_SCALE_NONE, MRR_SCALE_F32_A, MRR_SCALE_F32_AS, MRR_SCALE_E8M0_AK2 = range(4)
 MRR_PATH_AUTO, MRR_PATH_BULK, MRR_PATH_VECTOR = 0, 1, 2
+MRR_HINT_LOAD_EVICT_FIRST, MRR_HINT_STORE_EVICT_FIRST = 1, 2
 
 DTYPE_CODES = {
     "float16": MRR_F16, "bfloat16": MRR_BF16, "int8": MRR_I8, "float8_e5m2": MRR_F8E5M2,
@@ -61,6 +62,7 @@ class mrr_v2_plan_t(ctypes.Structure):
         ("has_topk", ctypes.c_int32), ("idx_type", ctypes.c_int32),
         ("fuse_scan", ctypes.c_int32), ("path", ctypes.c_int32), ("grid", ctypes.c_int32),
         ("block", ctypes.c_int32), ("chunk_bytes", ctypes.c_int32), ("stages", ctypes.c_int32),
+        ("hints", ctypes.c_int32), ("sched", ctypes.c_int32), ("static_chunks", ctypes.c_int32),
         ("smem_bytes", ctypes.c_int32), ("num_sms", ctypes.c_int32),
     ]
 

@@ -104,7 +104,7 @@ def run(**kw):
     a = dict(tokens=T, dt=m.MRR_BF16, A=64, H=128, counts=C, count_is_i64=0, N=4, E=4, scales=S,
              sl=m.MRR_SCALE_F32_A, scale_cols=1, topk_w=W, permute_tokens=O1, permute_scales=O2,
              permute_token_idx=I, expert_token_num=X, permute_topk_w=OW,
-             expert_token_num_type=1, idx_type=0, workspace=WS, workspace_bytes=4096, stream=None)
+             expert_token_num_type=1, idx_type=0, workspace=WS, workspace_bytes=1 << 20, stream=None)
     a.update(kw)
     return m.mrr_v2_run(**a)
 
@@ -126,6 +126,7 @@ def run(**kw):
     (dict(workspace=None), m.MRR_ERR_WORKSPACE),
     (dict(workspace=WS + 16), m.MRR_ERR_WORKSPACE),
     (dict(workspace_bytes=1024), m.MRR_ERR_WORKSPACE),
+    (dict(workspace_bytes=4096), m.MRR_ERR_WORKSPACE),                # status, but no counter
     (dict(H=16384), m.MRR_ERR_SHAPE),
     (dict(expert_token_num_type=0), m.MRR_ERR_UNSUPPORTED),
     (dict(idx_type=3), m.MRR_ERR_ATTR),
@@ -155,5 +156,5 @@ def test_run_plan_rejects_null_plan(lib):
 
 
 def test_plan_struct_layout_matches_header():
-    # 7 int64 fields followed by 12 int32 fields, no padding
-    assert ctypes.sizeof(m.mrr_v2_plan_t) == 7 * 8 + 12 * 4
+    # 7 int64 fields followed by 15 int32 fields, padded to 8 bytes
+    assert ctypes.sizeof(m.mrr_v2_plan_t) == 7 * 8 + 15 * 4 + 4

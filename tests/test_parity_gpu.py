@@ -130,6 +130,13 @@ STRESS_EDITS = [
     dict(chunk_bytes=65536, stages=2, grid=1022),      # most CTAs own no bytes
     dict(chunk_bytes=1024, stages=5, grid=152, block=1024),
     dict(grid=1, block=64),
+    dict(hints=3),
+    dict(chunk_bytes=4096, stages=8, hints=1),
+    dict(chunk_bytes=8192, stages=3, hints=2),
+    dict(sched=0),                                     # equal static slices, no counter
+    dict(sched=1, static_chunks=1, chunk_bytes=2048),  # almost everything from the counter
+    dict(sched=1, static_chunks=64, chunk_bytes=1024), # static chunks cover the buffer
+    dict(sched=1, static_chunks=1, chunk_bytes=16, stages=2, grid=7),
 ]
 
 
@@ -141,8 +148,20 @@ def test_bulk_pipeline_stress(edit, shape):
                                token_dtype="bfloat16", scale_layout="f32_as", scale_cols=4)
     ref = oracle.run_problem(p)
     assert_bit_exact(run_gpu(p, path=m.MRR_PATH_BULK, edit=edit), ref, p)
-    vec_edit = {k: v for k, v in edit.items() if k in ("grid", "block")}
+    vec_edit = {k: v for k, v in edit.items() if k in ("grid", "block", "hints", "sched")}
     assert_bit_exact(run_gpu(p, path=m.MRR_PATH_VECTOR, edit=vec_edit), ref, p)
+
+
+def test_counter_workspace_reused_across_launches():
+    """The chunk counter keeps the previous launch's epoch; every launch must still cover every
+    chunk exactly once (garbage at first use, stale values afterwards)."""
+    p = workloads.make_problem(np.random.default_rng(77), A=4000, H=2048, N=8, E=16,
+                               token_dtype="bfloat16", scale_layout="f32_a", scale_cols=1)
+    ref = oracle.run_problem(p)
+    ws = DevBuf(1 << 20, "cuda:0", fill=0x5A)
+    for k in range(6):
+        edit = dict(sched=1, static_chunks=1 + k % 3, chunk_bytes=4096 * (1 + k % 2), grid=16 + 40 * k)
+        assert_bit_exact(run_gpu(p, path=m.MRR_PATH_BULK, edit=edit, workspace=ws), ref, p)
 
 
 # ------------------------------------------------------------------------------ alignment
@@ -172,7 +191,7 @@ def test_empty_problem_zero_fills_expert_token_num():
 
     d = torch.device("cuda:0")
     etn = DevBuf(3 * 4, d)
-    ws = DevBuf(4096, d)
+    ws = DevBuf(8192, d)
     st = m.mrr_v2_run(None, m.MRR_BF16, 0, 16, DevBuf(4, d).ptr, 0, 0, 3, None, m.MRR_SCALE_NONE, 0,
                       None, None, None, None, etn.ptr, None, 1, 0, ws.ptr, ws.n,
                       torch.cuda.current_stream().cuda_stream)
