@@ -119,6 +119,9 @@ typedef struct mrr_v2_plan {
                                  1 = static_chunks chunks per CTA, then chunks claimed from a
                                  counter in the workspace (balances uneven CTA speeds)        */
     int32_t static_chunks;    /* bulk path, sched 1: chunks per CTA before claiming           */
+    int32_t pdl;              /* 1: launch with programmatic stream serialization, so the next
+                                 launch on the stream is scheduled while this one drains; the
+                                 kernels wait for their predecessor before any global access */
     int32_t smem_bytes;       /* dynamic shared memory per CTA                                */
     int32_t num_sms;          /* SMs on the device the plan was made for                      */
 } mrr_v2_plan_t;

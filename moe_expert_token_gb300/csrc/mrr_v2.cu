@@ -795,6 +795,15 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
     CountBatch cb;
     if (tid == 0)
         s_first[1] = 0u;
+    if (kBulk && tid == 0) {
+        for (int s = 0; s < p.stages; ++s)
+            mbar_init(smem_addr(&bars[s]), 1u);
+        mbar_init_fence();
+    }
+    // Nothing above touches global memory.  When launched behind another kernel with
+    // programmatic stream serialization, wait for it here, then let the next launch be scheduled.
+    grid_dependency_wait();
+    grid_launch_dependents();
     if (kFused) {
         if (tid == 0) {
             s_flags = 0u;
@@ -809,9 +818,6 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
     if (kBulk && tid == 0) {
         if (p.hints)
             ring.policy = policy_evict_first();
-        for (int s = 0; s < p.stages; ++s)
-            mbar_init(smem_addr(&bars[s]), 1u);
-        mbar_init_fence();
         // source addresses need no offsets: start streaming the static chunks before the scan
         while (ring.issued < p.stages && ring.next < ring.hi) {
             const int64_t b0 = ring.next, b1 = min(ring.next + p.chunk_bytes, ring.hi);
@@ -877,6 +883,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(const Params p)
         s_flags = 0u;
         s_sum = 0ull;
     }
+    grid_dependency_wait();
+    grid_launch_dependents();
     __syncthreads();
     uint32_t f = 0u;
     unsigned long long sum = 0ull;
@@ -1081,8 +1089,27 @@ int kernel_slot()
     return (kBulk ? 2 : 0) + (kFused ? 1 : 0);
 }
 
+// Launch with or without programmatic stream serialization (the kernels wait for their
+// predecessor before touching global memory either way).
+template <typename K>
+cudaError_t launch(K kern, const Params &p, int grid, int block, int smem, cudaStream_t stream, bool pdl)
+{
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 template <bool kBulk, bool kFused>
-cudaError_t launch_copy(const Params &p, int grid, int block, int smem, cudaStream_t stream, int device)
+cudaError_t launch_copy(const Params &p, int grid, int block, int smem, cudaStream_t stream, int device, bool pdl)
 {
     auto kern = reroute_kernel<kBulk, kFused>;
     const int slot = kernel_slot<kBulk, kFused>();
@@ -1096,8 +1123,7 @@ cudaError_t launch_copy(const Params &p, int grid, int block, int smem, cudaStre
             return e;
         g_smem_attr_set[device][slot] = true;
     }
-    kern<<<grid, block, smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch(kern, p, grid, block, smem, stream, pdl);
 }
 
 }  // namespace
@@ -1173,6 +1199,7 @@ mrr_status mrr_v2_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int6
     p.fuse_scan = NE <= kFusedMaxSegs ? 1 : 0;
     p.path = (rb % 16 == 0) ? MRR_PATH_BULK : MRR_PATH_VECTOR;
     p.num_sms = sms;
+    p.pdl = 1;
     const int64_t table_bytes = p.fuse_scan ? round_up(4 * (NE + 1 + 2 * padded_len(NE)), 128) : 0;
     if (p.path == MRR_PATH_BULK) {
         // the deepest ring shared memory allows: 3 x 64 KiB, else 3 x 48 KiB, else 4 x 32 KiB, ...
@@ -1253,6 +1280,8 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
     if (pl.grid < 1 || pl.grid > kMaxGrid || pl.block < 64 || pl.block > 1024 || pl.block % 32)
         return MRR_ERR_PLAN;
     if (pl.hints & ~(MRR_HINT_LOAD_EVICT_FIRST | MRR_HINT_STORE_EVICT_FIRST))
+        return MRR_ERR_PLAN;
+    if (pl.pdl != 0 && pl.pdl != 1)
         return MRR_ERR_PLAN;
     int path = pl.path;
     const bool aligned16 = rb % 16 == 0 && ((uintptr_t)tokens % 16) == 0 && ((uintptr_t)permute_tokens % 16) == 0;
@@ -1343,18 +1372,17 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
     }
 
     cudaError_t e = cudaSuccess;
-    if (!pl.fuse_scan) {
-        scan_kernel<<<1, 1024, 0, stream>>>(p);
-        e = cudaGetLastError();
-    }
+    const bool pdl = pl.pdl != 0;
+    if (!pl.fuse_scan)
+        e = launch(scan_kernel, p, 1, 1024, 0, stream, pdl);
     if (e == cudaSuccess) {
         const int grid = pl.grid, block = pl.block, sm = (int)smem;
         if (path == MRR_PATH_BULK)
-            e = pl.fuse_scan ? launch_copy<true, true>(p, grid, block, sm, stream, device)
-                             : launch_copy<true, false>(p, grid, block, sm, stream, device);
+            e = pl.fuse_scan ? launch_copy<true, true>(p, grid, block, sm, stream, device, pdl)
+                             : launch_copy<true, false>(p, grid, block, sm, stream, device, pdl);
         else
-            e = pl.fuse_scan ? launch_copy<false, true>(p, grid, block, sm, stream, device)
-                             : launch_copy<false, false>(p, grid, block, sm, stream, device);
+            e = pl.fuse_scan ? launch_copy<false, true>(p, grid, block, sm, stream, device, pdl)
+                             : launch_copy<false, false>(p, grid, block, sm, stream, device, pdl);
     }
     if (e != cudaSuccess) {
         (void)cudaGetLastError();

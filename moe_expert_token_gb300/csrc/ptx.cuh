@@ -18,6 +18,16 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Wait until the grids this launch depends on (the previous kernel on the stream, when this one
+// was launched with programmatic stream serialization) have completed and their memory is
+// visible.  Returns at once when there is no such dependency.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next programmatically serialized launch on the stream to be scheduled early.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)

@@ -63,6 +63,7 @@ class mrr_v2_plan_t(ctypes.Structure):
         ("fuse_scan", ctypes.c_int32), ("path", ctypes.c_int32), ("grid", ctypes.c_int32),
         ("block", ctypes.c_int32), ("chunk_bytes", ctypes.c_int32), ("stages", ctypes.c_int32),
         ("hints", ctypes.c_int32), ("sched", ctypes.c_int32), ("static_chunks", ctypes.c_int32),
+        ("pdl", ctypes.c_int32),
         ("smem_bytes", ctypes.c_int32), ("num_sms", ctypes.c_int32),
     ]
 

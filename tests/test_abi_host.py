@@ -156,5 +156,5 @@ def test_run_plan_rejects_null_plan(lib):
 
 
 def test_plan_struct_layout_matches_header():
-    # 7 int64 fields followed by 15 int32 fields, padded to 8 bytes
-    assert ctypes.sizeof(m.mrr_v2_plan_t) == 7 * 8 + 15 * 4 + 4
+    # 7 int64 fields followed by 16 int32 fields
+    assert ctypes.sizeof(m.mrr_v2_plan_t) == 7 * 8 + 16 * 4

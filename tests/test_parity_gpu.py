@@ -137,6 +137,8 @@ STRESS_EDITS = [
     dict(sched=1, static_chunks=1, chunk_bytes=2048),  # almost everything from the counter
     dict(sched=1, static_chunks=64, chunk_bytes=1024), # static chunks cover the buffer
     dict(sched=1, static_chunks=1, chunk_bytes=16, stages=2, grid=7),
+    dict(pdl=0),
+    dict(pdl=0, sched=0, grid=300),
 ]
 
 
@@ -148,7 +150,7 @@ def test_bulk_pipeline_stress(edit, shape):
                                token_dtype="bfloat16", scale_layout="f32_as", scale_cols=4)
     ref = oracle.run_problem(p)
     assert_bit_exact(run_gpu(p, path=m.MRR_PATH_BULK, edit=edit), ref, p)
-    vec_edit = {k: v for k, v in edit.items() if k in ("grid", "block", "hints", "sched")}
+    vec_edit = {k: v for k, v in edit.items() if k in ("grid", "block", "hints", "sched", "pdl")}
     assert_bit_exact(run_gpu(p, path=m.MRR_PATH_VECTOR, edit=vec_edit), ref, p)
 
 
