@@ -66,6 +66,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.mrr_oracle_validate.argtypes = [P, ctypes.c_int, I64, I64, I64]
     lib.mrr_oracle_offsets.restype = None
     lib.mrr_oracle_offsets.argtypes = [P, ctypes.c_int, I64, I64, P, P]
+    lib.mrr_oracle_unroute.restype = ctypes.c_int
+    lib.mrr_oracle_unroute.argtypes = [P, I64, I64, P, ctypes.c_int, I64, I64, P, I64, P, P, P, P]
     return lib
 
 
@@ -144,3 +146,32 @@ def run(tokens: np.ndarray, counts: np.ndarray, *, scales: Optional[np.ndarray] 
 def run_problem(p, lib: Optional[ctypes.CDLL] = None) -> dict:
     """Run the oracle on a ``workloads.Problem``."""
     return run(p.tokens, p.counts, scales=p.scales, topk=p.topk, idx_type=p.idx_type, lib=lib)
+
+
+def unroute(permute_tokens: np.ndarray, counts: np.ndarray, *, permute_scales: Optional[np.ndarray] = None,
+            permute_topk: Optional[np.ndarray] = None, lib: Optional[ctypes.CDLL] = None) -> dict:
+    """The inverse move: expert-major byte rows back to rank-major order.
+
+    Returns a dict with tokens ([A, row_bytes] uint8), scales (None when permute_scales is None)
+    and topk_weight ([A] float32 or None).  Raises OracleError when the counts are invalid.
+    """
+    lib = lib or load()
+    pt = np.ascontiguousarray(permute_tokens, dtype=np.uint8)
+    if pt.ndim != 2:
+        raise ValueError("permute_tokens must be [A, row_bytes] bytes")
+    A, rb = pt.shape
+    c = np.ascontiguousarray(counts)
+    if c.dtype not in (np.int32, np.int64) or c.ndim != 2:
+        raise ValueError("counts must be a 2-D int32/int64 array")
+    N, E = c.shape
+    out_tok = np.empty_like(pt)
+    ps = None if permute_scales is None else np.ascontiguousarray(permute_scales, dtype=np.uint8)
+    sb = 0 if ps is None else ps.shape[1]
+    out_sc = None if ps is None else np.empty_like(ps)
+    pw = None if permute_topk is None else np.ascontiguousarray(permute_topk, dtype=np.float32).reshape(-1)
+    out_w = None if pw is None else np.empty_like(pw)
+    rc = lib.mrr_oracle_unroute(_ptr(pt), A, rb, _ptr(c), int(c.dtype == np.int64), N, E, _ptr(ps), sb,
+                                _ptr(pw), _ptr(out_tok), _ptr(out_sc), _ptr(out_w))
+    if rc != ORC_OK:
+        raise OracleError(rc)
+    return {"tokens": out_tok, "scales": out_sc, "topk_weight": out_w}

@@ -165,3 +165,63 @@ int mrr_oracle_run(const uint8_t *tokens, int64_t A, int64_t row_bytes,
     free(dst_off);
     return ORC_OK;
 }
+
+/*
+ * The inverse move, for the combine side of the MoE layer: rows that sit expert-major (as the
+ * forward op left them) go back to the rank-major order they arrived in, so they can be
+ * returned to their source ranks.  The pages place the op just before the expert FFN and name
+ * finalize/combine ops after it ("CANN ops-transformer MoeReRoutingV2" article, section
+ * 数据流定位); the inverse reuses the same segments: for every (i,j) and 0 <= k < counts[i,j],
+ *   tokens[SrcOffset(i,j) + k] = permute_tokens[DstOffset(i,j) + k]
+ * and the same for the scale rows and top-k weights.  Same validation as mrr_oracle_run; on
+ * any error nothing is written.
+ */
+int mrr_oracle_unroute(const uint8_t *permute_tokens, int64_t A, int64_t row_bytes,
+                       const void *counts, int count_is_i64, int64_t N, int64_t E,
+                       const uint8_t *permute_scales, int64_t scale_row_bytes,
+                       const float *permute_topk_w,
+                       uint8_t *tokens, uint8_t *scales, float *topk_w)
+{
+    int rc;
+    int64_t *src_off, *dst_off;
+
+    if (!counts && N * E > 0)
+        return ORC_ERR_ARG;
+    if (row_bytes <= 0 || (A > 0 && (!permute_tokens || !tokens)))
+        return ORC_ERR_ARG;
+    if ((permute_topk_w == NULL) != (topk_w == NULL))
+        return ORC_ERR_ARG;
+    if (permute_scales && (!scales || scale_row_bytes <= 0))
+        return ORC_ERR_ARG;
+    rc = mrr_oracle_validate(counts, count_is_i64, N, E, A);
+    if (rc != ORC_OK)
+        return rc;
+
+    src_off = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N * E + 1));
+    dst_off = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N * E + 1));
+    if (!src_off || !dst_off) {
+        free(src_off);
+        free(dst_off);
+        return ORC_ERR_ARG;
+    }
+    mrr_oracle_offsets(counts, count_is_i64, N, E, src_off, dst_off);
+
+    for (int64_t i = 0; i < N; ++i)
+        for (int64_t j = 0; j < E; ++j) {
+            int64_t n = count_at(counts, count_is_i64, E, i, j);
+            for (int64_t k = 0; k < n; ++k) {
+                int64_t s = src_off[i * E + j] + k;   /* rank-major position  */
+                int64_t d = dst_off[i * E + j] + k;   /* expert-major position */
+                memcpy(tokens + s * row_bytes, permute_tokens + d * row_bytes, (size_t)row_bytes);
+                if (permute_scales)
+                    memcpy(scales + s * scale_row_bytes, permute_scales + d * scale_row_bytes,
+                           (size_t)scale_row_bytes);
+                if (permute_topk_w)
+                    topk_w[s] = permute_topk_w[d];
+            }
+        }
+
+    free(src_off);
+    free(dst_off);
+    return ORC_OK;
+}

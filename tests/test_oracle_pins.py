@@ -145,6 +145,31 @@ def check_invariants(lib, problem):
         assert np.array_equal(gather[pos], np.arange(starts[q], starts[q + 1]))
 
 
+def check_unroute_hand_examples(lib):
+    """Inverse move: rank-major row s takes expert-major row scatter[s] (hand-derived scatter)."""
+    data = json.load(open(GOLDEN))
+    for case in data["cases"]:
+        c = np.array(case["counts"], dtype=np.int32)
+        y = row_payload(case["A"], 6)                      # an expert-major buffer
+        out = oracle.unroute(y, c, permute_topk=np.arange(case["A"], dtype=np.float32), lib=lib)
+        sc = np.array(case["scatter"])
+        assert np.array_equal(out["tokens"], y[sc]), case["name"]
+        assert np.array_equal(out["topk_weight"], sc.astype(np.float32)), case["name"]
+
+
+def check_unroute_brute_force(lib, max_dim=3, max_count=2):
+    for N in range(1, max_dim + 1):
+        for E in range(1, max_dim + 1):
+            for flat in itertools.product(range(1, max_count + 1), repeat=N * E):
+                c = np.array(flat, dtype=np.int64).reshape(N, E)
+                A = int(c.sum())
+                y = row_payload(A, 3)
+                sc = inverse(brute_force_gather(c))
+                out = oracle.unroute(y, c, permute_scales=y[:, :2], lib=lib)
+                assert np.array_equal(out["tokens"], y[sc]), c
+                assert np.array_equal(out["scales"], y[sc][:, :2]), c
+
+
 # ----------------------------------------------------------------------------- tests on the real oracle
 
 def test_hand_examples(oracle_lib):
@@ -177,6 +202,43 @@ def test_invariants_random(oracle_lib, seed, N, E, A, dtype, layout, cols):
                                count_dtype=np.int64 if seed % 2 else np.int32,
                                scale_layout=layout, scale_cols=cols, has_topk=True)
     check_invariants(oracle_lib, p)
+
+
+def test_unroute_hand_examples(oracle_lib):
+    check_unroute_hand_examples(oracle_lib)
+
+
+def test_unroute_brute_force(oracle_lib):
+    check_unroute_brute_force(oracle_lib, max_dim=3, max_count=3)
+
+
+@pytest.mark.parametrize("seed,N,E,A", [(11, 4, 4, 64), (12, 8, 32, 900), (13, 64, 64, 5000), (14, 1, 7, 30),
+                                        (15, 9, 1, 40)])
+def test_unroute_inverts_the_forward_move(oracle_lib, seed, N, E, A):
+    rng = np.random.default_rng(seed)
+    p = workloads.make_problem(rng, A=A, H=40, N=N, E=E, token_dtype="bfloat16",
+                               count_dtype=np.int64 if seed % 2 else np.int32,
+                               scale_layout="e8m0", scale_cols=6, has_topk=True)
+    fwd = oracle.run_problem(p, lib=oracle_lib)
+    back = oracle.unroute(fwd["permute_tokens"], p.counts, permute_scales=fwd["permute_scales"],
+                          permute_topk=fwd["permute_topk_weight"], lib=oracle_lib)
+    assert np.array_equal(back["tokens"], p.tokens)
+    assert np.array_equal(back["scales"], p.scales)
+    assert np.array_equal(back["topk_weight"].view(np.uint32), p.topk.view(np.uint32))
+    # and the other way round: route(unroute(y)) == y
+    y = rng.integers(0, 256, size=(A, 17), dtype=np.uint16).astype(np.uint8)
+    again = oracle.run(oracle.unroute(y, p.counts, lib=oracle_lib)["tokens"], p.counts, lib=oracle_lib)
+    assert np.array_equal(again["permute_tokens"], y)
+
+
+def test_unroute_rejects_invalid_counts():
+    c = np.array([[1, 0], [2, 3]], np.int32)
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.unroute(row_payload(6, 4), c)
+    assert e.value.code == oracle.ORC_ERR_COUNT_NONPOS
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.unroute(row_payload(7, 4), np.array([[1, 1], [2, 2]], np.int32))
+    assert e.value.code == oracle.ORC_ERR_COUNT_SUM
 
 
 def test_workload_c1_invariants(oracle_lib):
@@ -256,13 +318,26 @@ MUTANTS = {
         "total += count_at(counts, count_is_i64, E, j < N ? j : 0, i < E ? i : 0);"),
     # the move reads the destination offset on the source side
     "move_src_from_dst": (
-        "int64_t s = src_off[i * E + j] + k;", "int64_t s = dst_off[i * E + j] + k;"),
+        "int64_t s = src_off[i * E + j] + k;\n                int64_t d = dst_off[i * E + j] + k;\n"
+        "                memcpy(permute_tokens",
+        "int64_t s = dst_off[i * E + j] + k;\n                int64_t d = dst_off[i * E + j] + k;\n"
+        "                memcpy(permute_tokens"),
     # the zero-count check dropped
     "no_nonpos_check": ("            if (c <= 0)\n                return ORC_ERR_COUNT_NONPOS;\n", ""),
+    # inverse move: source and destination positions swapped
+    "unroute_swapped": (
+        "memcpy(tokens + s * row_bytes, permute_tokens + d * row_bytes, (size_t)row_bytes);",
+        "memcpy(tokens + d * row_bytes, permute_tokens + s * row_bytes, (size_t)row_bytes);"),
+    # inverse move: top-k weights taken from the rank-major position
+    "unroute_topk_from_src": ("topk_w[s] = permute_topk_w[d];", "topk_w[s] = permute_topk_w[s];"),
+    # inverse move: scale rows moved with the token row size
+    "unroute_scale_stride": ("scales + s * scale_row_bytes, permute_scales + d * scale_row_bytes,",
+                             "scales + s * scale_row_bytes, permute_scales + d * row_bytes,"),
 }
 
 PINS = [check_hand_examples, check_transpose_closed_form,
-        lambda lib: check_brute_force(lib, max_dim=2, max_count=2)]
+        lambda lib: check_brute_force(lib, max_dim=2, max_count=2),
+        check_unroute_hand_examples, lambda lib: check_unroute_brute_force(lib, max_dim=2, max_count=2)]
 
 
 def _nonpos_pin(lib):
