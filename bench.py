@@ -45,6 +45,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", type=int, default=2, help="workload 1..5 (2 is the headline)")
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--op", choices=["route", "unroute"], default="route",
+                    help="route: rank-major -> expert-major (the op); unroute: the inverse move")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU oracle baseline budget (seconds of oracle work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -93,9 +95,10 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(config: int):
+def profiled_traffic(config: int, op: str = "route"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
-    path = os.path.join(ROOT, "profiles", f"reroute_kernel_C{config}.md")
+    name = f"reroute_kernel_C{config}.md" if op == "route" else f"reroute_kernel_inverse_C{config}.md"
+    path = os.path.join(ROOT, "profiles", name)
     try:
         text = open(path, encoding="utf-8").read()
     except OSError:
@@ -197,27 +200,44 @@ def row_sample(p, frac: float):
     return q
 
 
-def time_oracle(p, budget_s: float, max_reps: int = 1000):
+def op_bytes(p, op: str) -> int:
+    """Algorithmic bytes of one step.  The inverse move writes no index and no per-expert counts."""
+    if op == "route":
+        return p.algorithmic_bytes()
+    return p.algorithmic_bytes() - 4 * p.A - p.E * p.counts.dtype.itemsize
+
+
+def oracle_step(p, op: str, lib):
+    import oracle
+
+    if op == "route":
+        return oracle.run_problem(p, lib=lib)
+    # the workload's payloads stand for the expert-major rows the inverse move reads
+    return oracle.unroute(p.tokens, p.counts, permute_scales=p.scales, permute_topk=p.topk, lib=lib)
+
+
+def time_oracle(p, budget_s: float, op: str = "route", max_reps: int = 1000):
     """Run the oracle on ``p`` repeatedly for about ``budget_s`` seconds; (GB/s, reps, s)."""
     import oracle
 
     lib = oracle.load()
-    oracle.run_problem(p, lib=lib)  # warm (page in the library and the inputs)
+    oracle_step(p, op, lib)  # warm (page in the library and the inputs)
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.run_problem(p, lib=lib)
+        oracle_step(p, op, lib)
         reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s or reps >= max_reps:
             break
-    return p.algorithmic_bytes() * reps / el / 1e9, reps, el
+    return op_bytes(p, op) * reps / el / 1e9, reps, el
 
 
-def config_dict(p, k, extra=None):
-    d = {"workload": p.name, "A": p.A, "H": p.H, "N": p.N, "E": p.E, "token_dtype": p.token_dtype,
+def config_dict(p, k, extra=None, op="route"):
+    d = {"workload": p.name if op == "route" else "inverse move of " + p.name, "op": op,
+         "A": p.A, "H": p.H, "N": p.N, "E": p.E, "token_dtype": p.token_dtype,
          "count_dtype": str(p.counts.dtype), "scales": p.scale_layout, "scale_cols": p.scale_cols,
          "topk": p.topk is not None, "idx_type": p.idx_type, "expert_token_num_type": 1,
-         "bytes_per_step": p.algorithmic_bytes()}
+         "bytes_per_step": op_bytes(p, op)}
     d.update(extra or {})
     return d
 
@@ -235,24 +255,24 @@ def run_reference(args):
     t_full = time.perf_counter()
     import oracle
 
-    oracle.run_problem(p)
+    lib = oracle.load()
+    oracle_step(p, args.op, lib)
     t_full = time.perf_counter() - t_full
     frac = min(1.0, 120.0 / max(1e-9, t_full * (args.steps + args.warmup)))
     q = row_sample(p, frac)
-    lib = oracle.load()
     for _ in range(args.warmup):
-        oracle.run_problem(q, lib=lib)
+        oracle_step(q, args.op, lib)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.run_problem(q, lib=lib)
+        oracle_step(q, args.op, lib)
     el = time.perf_counter() - t0
-    value = q.algorithmic_bytes() * args.steps / el / 1e9
+    value = op_bytes(q, args.op) * args.steps / el / 1e9
     sample = f"first {q.A} of {p.A} rows per step (counts scaled to sum to {q.A})"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
-        "data": "synthetic", "config": config_dict(p, args.config, {"sample_rows": q.A}),
+        "data": "synthetic", "config": config_dict(p, args.config, {"sample_rows": q.A}, args.op),
         "tokens_per_s": q.A * args.steps / el,
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": sample},
@@ -292,12 +312,16 @@ def run_gpu(args):
     sl = m.SCALE_CODES[p.scale_layout]
     A, H, N, E = p.A, p.H, p.N, p.E
     i64 = p.counts.dtype == np.int64
-    st, plan = m.mrr_v2_plan(A, H, code, N, E, i64, sl, p.scale_cols, p.topk is not None, 1,
-                             p.idx_type, local_rank)
+    if args.op == "route":
+        st, plan = m.mrr_v2_plan(A, H, code, N, E, i64, sl, p.scale_cols, p.topk is not None, 1,
+                                 p.idx_type, local_rank)
+    else:
+        st, plan = m.mrr_v2_unroute_plan(A, H, code, N, E, i64, sl, p.scale_cols, p.topk is not None,
+                                         local_rank)
     if st != m.MRR_OK:
         raise SystemExit(m.mrr_status_str(st))
     launches_per_step = 1 if plan.fuse_scan else 2
-    bytes_step = p.algorithmic_bytes()
+    bytes_step = op_bytes(p, args.op)
 
     def dev_bytes(arr):
         if arr is None:
@@ -316,8 +340,9 @@ def run_gpu(args):
         s["out_scales"] = (None if p.scales is None
                            else torch.empty(A * p.scale_row_bytes, dtype=torch.uint8, device=dev))
         s["out_topk"] = None if p.topk is None else torch.empty(4 * A, dtype=torch.uint8, device=dev)
-        s["idx"] = torch.empty(A, dtype=torch.int32, device=dev)
-        s["etn"] = torch.empty(E * p.counts.dtype.itemsize, dtype=torch.uint8, device=dev)
+        inv = args.op == "unroute"   # the inverse move writes no index and no per-expert counts
+        s["idx"] = None if inv else torch.empty(A, dtype=torch.int32, device=dev)
+        s["etn"] = None if inv else torch.empty(E * p.counts.dtype.itemsize, dtype=torch.uint8, device=dev)
         s["ws"] = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
         sets.append(s)
     stream = torch.cuda.current_stream(dev)
@@ -327,10 +352,15 @@ def run_gpu(args):
         return None if t is None else t.data_ptr()
 
     def launch(s, on_stream):
-        st = m.mrr_v2_run(P(s["tokens"]), code, A, H, P(s["counts"]), i64, N, E, P(s["scales"]), sl,
-                          p.scale_cols, P(s["topk"]), P(s["out_tokens"]), P(s["out_scales"]),
-                          P(s["idx"]), P(s["etn"]), P(s["out_topk"]), 1, p.idx_type, P(s["ws"]),
-                          s["ws"].numel(), on_stream.cuda_stream)
+        if args.op == "route":
+            st = m.mrr_v2_run(P(s["tokens"]), code, A, H, P(s["counts"]), i64, N, E, P(s["scales"]), sl,
+                              p.scale_cols, P(s["topk"]), P(s["out_tokens"]), P(s["out_scales"]),
+                              P(s["idx"]), P(s["etn"]), P(s["out_topk"]), 1, p.idx_type, P(s["ws"]),
+                              s["ws"].numel(), on_stream.cuda_stream)
+        else:  # the inverse move: the "tokens" buffers hold the expert-major rows
+            st = m.mrr_v2_unroute(P(s["tokens"]), code, A, H, P(s["counts"]), i64, N, E, P(s["scales"]),
+                                  sl, p.scale_cols, P(s["topk"]), P(s["out_tokens"]), P(s["out_scales"]),
+                                  P(s["out_topk"]), P(s["ws"]), s["ws"].numel(), on_stream.cuda_stream)
         if st != m.MRR_OK:
             raise RuntimeError(m.mrr_status_str(st))
 
@@ -343,8 +373,9 @@ def run_gpu(args):
         st = m.mrr_v2_read_status(P(s["ws"]), s["ws"].numel(), sp)
         if st != m.MRR_OK:
             raise RuntimeError(m.mrr_status_str(st))
-    idx_sorted = torch.sort(sets[0]["idx"].to(torch.int64)).values
-    assert torch.equal(idx_sorted, torch.arange(A, device=dev)), "index is not a permutation"
+    if args.op == "route":
+        idx_sorted = torch.sort(sets[0]["idx"].to(torch.int64)).values
+        assert torch.equal(idx_sorted, torch.arange(A, device=dev)), "index is not a permutation"
 
     for k in range(args.warmup):
         step(sets[k % R])
@@ -385,7 +416,7 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        gbs, reps, el = time_oracle(p, args.cpu_seconds)
+        gbs, reps, el = time_oracle(p, args.cpu_seconds, args.op)
         cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": f"the full workload, {reps} runs in {el:.1f} s, single thread"}
 
@@ -396,7 +427,7 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded numpy draws shaped like the pages' workload)",
-        "config": config_dict(p, args.config, {
+        "config": config_dict(p, args.config, op=args.op, extra={
             "l2": f"{R} rotating buffer sets, {R * footprint / 1e6:.0f} MB > 4x L2 ({l2 / 1e6:.0f} MB)",
             "path": {1: "bulk", 2: "vector"}[plan.path], "grid": plan.grid, "block": plan.block,
             "chunk_bytes": plan.chunk_bytes, "stages": plan.stages, "fused_scan": bool(plan.fuse_scan),
@@ -405,7 +436,7 @@ def run_gpu(args):
         "tokens_per_s": world * A * K / (elapsed_ms * 1e-3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
-                     "traffic": profiled_traffic(args.config),
+                     "traffic": profiled_traffic(args.config, args.op),
                      "kernel": "mrr::reroute_kernel", "bytes_per_launch": bytes_step,
                      "mean_launch_us": mean_launch_ms * 1e3,
                      "timing": "CUDA events around the K back-to-back launches on the launching stream; per launch = region / K"},

@@ -122,6 +122,8 @@ typedef struct mrr_v2_plan {
     int32_t pdl;              /* 1: launch with programmatic stream serialization, so the next
                                  launch on the stream is scheduled while this one drains; the
                                  kernels wait for their predecessor before any global access */
+    int32_t direction;        /* 0: rank-major -> expert-major (mrr_v2_plan);
+                                 1: expert-major -> rank-major (mrr_v2_unroute_plan)          */
     int32_t smem_bytes;       /* dynamic shared memory per CTA                                */
     int32_t num_sms;          /* SMs on the device the plan was made for                      */
 } mrr_v2_plan_t;
@@ -192,6 +194,42 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan,
  * workspace_bytes must be >= 4096.
  */
 mrr_status mrr_v2_read_status(const void *workspace, size_t workspace_bytes, mrr_stream_t stream);
+
+/*
+ * mrr_v2_unroute_plan -- host only: the launch plan of mrr_v2_unroute, which moves the rows
+ * back (direction 1).  Same argument checks as mrr_v2_plan; no attributes (the inverse move
+ * writes no index and no per-expert counts).
+ */
+mrr_status mrr_v2_unroute_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int64_t E,
+                               int count_is_i64, mrr_scale_layout sl, int64_t scale_cols, int has_topk,
+                               int device, mrr_v2_plan_t *out);
+
+/*
+ * mrr_v2_unroute -- the inverse move, for the combine side of the MoE layer: rows laid out
+ * expert-major (by mrr_v2_run, or expert outputs in that order) go back to the rank-major order
+ * they arrived in, so they can be returned to their source ranks.  The pages place the op before
+ * the expert FFN and name finalize/combine ops after it ("CANN ops-transformer MoeReRoutingV2"
+ * article, section 数据流定位); the inverse reuses the same segments and offsets (section
+ * 计算公式):  tokens[SrcOffset(i,j) + k] = permute_tokens[DstOffset(i,j) + k],  and the same for
+ * the scale rows and top-k weights, 0 <= k < counts[i,j].
+ *   permute_tokens  [A, H] dt, expert-major                              (read)
+ *   counts          [N, E] int32 or int64, the same matrix as the forward move (read)
+ *   permute_scales  per the layout, or NULL with MRR_SCALE_NONE          (read)
+ *   permute_topk_w  [A, 1] float32, or NULL                              (read)
+ *   tokens          [A, H] dt, rank-major                                (written)
+ *   scales          same shape as permute_scales; written when given
+ *   topk_w          [A, 1] float32; NULL exactly when permute_topk_w is NULL
+ *   workspace       >= plan.workspace_bytes of mrr_v2_unroute_plan (N*E > 4096 needs one more
+ *                   offset table than the forward move)
+ * Errors and status reporting are those of mrr_v2_run.  mrr_v2_run_plan also runs it, given a
+ * plan with direction 1: its tokens / scales / topk_w arguments are then the expert-major
+ * inputs, permute_* the rank-major outputs, and permute_token_idx / expert_token_num unused.
+ */
+mrr_status mrr_v2_unroute(const void *permute_tokens, mrr_token_dtype dt, int64_t A, int64_t H,
+                          const void *counts, int count_is_i64, int64_t N, int64_t E,
+                          const void *permute_scales, mrr_scale_layout sl, int64_t scale_cols,
+                          const float *permute_topk_w, void *tokens, void *scales, float *topk_w,
+                          void *workspace, size_t workspace_bytes, mrr_stream_t stream);
 
 /* mrr_status_str -- static, human-readable name of a status code (never NULL). */
 const char *mrr_status_str(mrr_status s);

@@ -8,9 +8,12 @@ from .mrr_v2 import (  # noqa: F401
     MrrError,
     load_library,
     moe_re_routing,
+    moe_re_routing_inverse,
     mrr_status_str,
     mrr_v2_plan,
     mrr_v2_read_status,
     mrr_v2_run,
     mrr_v2_run_plan,
+    mrr_v2_unroute,
+    mrr_v2_unroute_plan,
 )

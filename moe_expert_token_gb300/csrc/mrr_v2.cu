@@ -70,6 +70,8 @@ struct Params {
     uint32_t *status;
     uint32_t *g_row_ex;   // N*E > 4096: offsets scanned into the workspace
     uint32_t *g_dst_off;
+    uint32_t *g_col_ex;   // N*E > 4096, inverse move: column-major prefix by position (padded)
+    int inverse;          // 0: rank-major -> expert-major; 1: the inverse move (no index outputs)
     int chunk_bytes;
     int stages;
     int hints;            // bulk path: MRR_HINT_* bits (L2 evict-first policies)
@@ -109,11 +111,48 @@ __device__ __forceinline__ int find_seg(const uint32_t *row_ex, int NE, uint32_t
 __device__ __forceinline__ int pad32(int k) { return k + (k >> 5); }
 __host__ __device__ constexpr int64_t padded_len(int64_t n) { return n + (n >> 5) + 1; }
 
+// The segments of one direction of the move, numbered in the order they sit in the SOURCE.
+//   forward (rank-major -> expert-major): g = q = i*E + j; starts = SrcOffset (row_ex, dense),
+//     destinations = DstOffset (dst_off, padded by q);
+//   inverse (expert-major -> rank-major): g = pos = j*N + i; starts = DstOffset by position
+//     (col_ex, padded), destinations = SrcOffset of (i, j).
+// starts[NE] (at its index) is A.
+struct SegMap {
+    const uint32_t *row_ex;
+    const uint32_t *dst_off;
+    const uint32_t *col_ex;
+    int NE, N, E;
+    int inv;
+    __device__ __forceinline__ uint32_t begin(int g) const { return inv ? col_ex[pad32(g)] : row_ex[g]; }
+    __device__ __forceinline__ uint32_t dest(int g) const
+    {
+        if (!inv)
+            return dst_off[pad32(g)];
+        const int j = g / N;
+        return row_ex[(g - j * N) * E + j];
+    }
+    // the last g in [0, NE) with begin(g) <= s (starts strictly increase: every count > 0)
+    __device__ __forceinline__ int find(uint32_t s) const
+    {
+        if (!inv)
+            return find_seg(row_ex, NE, s);
+        int lo = 0, hi = NE;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (col_ex[pad32(mid)] <= s)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        return lo;
+    }
+};
+
 // Destination row of source row s.
-__device__ __forceinline__ int64_t dst_row(const uint32_t *row_ex, const uint32_t *dst_off, int NE, int64_t s)
+__device__ __forceinline__ int64_t dst_row(const SegMap &m, int64_t s)
 {
-    const int q = find_seg(row_ex, NE, (uint32_t)s);
-    return (int64_t)dst_off[pad32(q)] + (s - (int64_t)row_ex[q]);
+    const int g = m.find((uint32_t)s);
+    return (int64_t)m.dest(g) + (s - (int64_t)m.begin(g));
 }
 
 // Exclusive block-wide scan of one uint32 per thread (warp shuffles + one smem pass).
@@ -332,7 +371,11 @@ __device__ uint32_t cta_scan(const Params &p, CountBatch &cb, uint32_t *row_ex, 
             }
             cpos = pos;
             dst_off[pad32(ci * E + cj)] = v;
+            if (p.inverse)
+                cnt_t[pad32(pos)] = v;  // in place: the starts of the inverse move's source segments
         });
+    if (p.inverse && tid == 0)
+        cnt_t[pad32(NE)] = (uint32_t)p.A;
     __syncthreads();
     return 0u;
 }
@@ -411,8 +454,7 @@ constexpr int kSideBatch = 4;  // rows (or scale vectors) per thread with their 
 // Scale vectors of width W (16, 8 or 4 bytes, both pointers aligned to W) for source rows
 // [r_lo, r_hi): kSideBatch loads in flight per thread, then the stores.
 template <int W>
-__device__ void move_scales(const Params &p, const uint32_t *row_ex, const uint32_t *dst_off, int64_t r_lo,
-                            int64_t r_hi, int t0, int ts)
+__device__ void move_scales(const Params &p, const SegMap &m, int64_t r_lo, int64_t r_hi, int t0, int ts)
 {
     const int64_t sb = p.scale_row_bytes, vpr = sb / W;
     const int64_t items = (r_hi - r_lo) * vpr;
@@ -432,7 +474,7 @@ __device__ void move_scales(const Params &p, const uint32_t *row_ex, const uint3
 #pragma unroll
         for (int u = 0; u < kSideBatch; ++u) {
             if (t + (int64_t)u * ts < items) {
-                const int64_t d = dst_row(row_ex, dst_off, p.NE, s[u]);
+                const int64_t d = dst_row(m, s[u]);
                 Vec<W>::st(p.out_scales + d * sb + off[u], v[u]);
             }
         }
@@ -441,7 +483,7 @@ __device__ void move_scales(const Params &p, const uint32_t *row_ex, const uint3
 
 // Scale rows, top-k weights and the index for this CTA's share of the SOURCE rows,
 // processed by threads t0, t0 + ts, ... of the block.
-__device__ void side_arrays(const Params &p, const uint32_t *row_ex, const uint32_t *dst_off, int t0, int ts)
+__device__ void side_arrays(const Params &p, const SegMap &m, int t0, int ts)
 {
     const int64_t G = gridDim.x, b = blockIdx.x;
     const int64_t r_lo = b * p.A / G, r_hi = (b + 1) * p.A / G;
@@ -459,11 +501,14 @@ __device__ void side_arrays(const Params &p, const uint32_t *row_ex, const uint3
             const int64_t s = base + (int64_t)u * ts;
             if (s >= r_hi)
                 break;
-            const int64_t d = dst_row(row_ex, dst_off, p.NE, s);
-            if (p.idx_type == 0)
+            const int64_t d = dst_row(m, s);
+            if (p.inverse) {
+                // the inverse move writes no index
+            } else if (p.idx_type == 0) {
                 p.idx[d] = (int32_t)s;  // gather index: out[d] = in[idx[d]]
-            else
+            } else {
                 p.idx[s] = (int32_t)d;  // scatter index: out[idx[s]] = in[s]
+            }
             if (topk4)
                 reinterpret_cast<uint32_t *>(p.out_topk)[d] = w[u];
             else if (p.topk) {
@@ -476,13 +521,13 @@ __device__ void side_arrays(const Params &p, const uint32_t *row_ex, const uint3
         return;
     switch (p.scale_w) {
     case 16:
-        move_scales<16>(p, row_ex, dst_off, r_lo, r_hi, t0, ts);
+        move_scales<16>(p, m, r_lo, r_hi, t0, ts);
         break;
     case 8:
-        move_scales<8>(p, row_ex, dst_off, r_lo, r_hi, t0, ts);
+        move_scales<8>(p, m, r_lo, r_hi, t0, ts);
         break;
     case 4:
-        move_scales<4>(p, row_ex, dst_off, r_lo, r_hi, t0, ts);
+        move_scales<4>(p, m, r_lo, r_hi, t0, ts);
         break;
     default: {  // 1- or 2-byte aligned scale rows
         const int w = p.scale_w;
@@ -492,7 +537,7 @@ __device__ void side_arrays(const Params &p, const uint32_t *row_ex, const uint3
             const int64_t r = t / vpr;
             const int64_t v = t - r * vpr;
             const int64_t s = r_lo + r;
-            const int64_t d = dst_row(row_ex, dst_off, p.NE, s);
+            const int64_t d = dst_row(m, s);
             copy_unit(p.out_scales + d * sb + v * w, p.scales + s * sb + v * w, w);
         }
     }
@@ -548,20 +593,19 @@ __device__ __forceinline__ void copy_block(uint8_t *dst, const uint8_t *src, int
 
 // Walk the pieces of source byte range [lo, hi): each piece lies inside one segment, where the
 // destination is the source shifted by (DstOffset - SrcOffset) rows.
-__device__ void vector_copy(const Params &p, const uint32_t *row_ex, const uint32_t *dst_off, int64_t lo,
-                            int64_t hi, int tid, int nthr)
+__device__ void vector_copy(const Params &p, const SegMap &m, int64_t lo, int64_t hi, int tid, int nthr)
 {
     if (lo >= hi)
         return;
     const int64_t rb = p.row_bytes;
-    int q = find_seg(row_ex, p.NE, (uint32_t)(lo / rb));
-    int64_t seg_end = (int64_t)row_ex[q + 1] * rb;
-    int64_t delta = ((int64_t)dst_off[pad32(q)] - (int64_t)row_ex[q]) * rb;
+    int q = m.find((uint32_t)(lo / rb));
+    int64_t seg_end = (int64_t)m.begin(q + 1) * rb;
+    int64_t delta = ((int64_t)m.dest(q) - (int64_t)m.begin(q)) * rb;
     for (int64_t pos = lo; pos < hi;) {
         while (pos >= seg_end) {
             ++q;
-            seg_end = (int64_t)row_ex[q + 1] * rb;
-            delta = ((int64_t)dst_off[pad32(q)] - (int64_t)row_ex[q]) * rb;
+            seg_end = (int64_t)m.begin(q + 1) * rb;
+            delta = ((int64_t)m.dest(q) - (int64_t)m.begin(q)) * rb;
         }
         const int64_t pe = min(hi, seg_end);
         copy_block(p.out_tokens + pos + delta, p.tokens + pos, pe - pos, tid, nthr);
@@ -685,8 +729,8 @@ __device__ __forceinline__ void bulk_issue_load(const Params &p, BulkRing &r, in
     ++r.issued;
 }
 
-__device__ uint32_t bulk_driver(const Params &p, BulkRing &r, const uint32_t *row_ex, const uint32_t *dst_off,
-                                uint32_t flags, volatile uint32_t *s_first)
+__device__ uint32_t bulk_driver(const Params &p, BulkRing &r, const SegMap &m, uint32_t flags,
+                                volatile uint32_t *s_first)
 {
     const int S = p.stages;
     const int64_t rb = p.row_bytes;
@@ -711,10 +755,10 @@ __device__ uint32_t bulk_driver(const Params &p, BulkRing &r, const uint32_t *ro
             const int64_t c0 = r.stage_b0[st], c1 = r.stage_b1[st];
             const uint32_t sbase = smem_addr(r.base + (size_t)st * p.chunk_bytes);
             // one bulk store per piece: the part of the chunk inside one segment
-            int q = find_seg(row_ex, p.NE, (uint32_t)(c0 / rb));
+            int q = m.find((uint32_t)(c0 / rb));
             for (int64_t pos = c0; pos < c1; ++q) {
-                const int64_t seg_end = (int64_t)row_ex[q + 1] * rb;
-                const int64_t delta = ((int64_t)dst_off[pad32(q)] - (int64_t)row_ex[q]) * rb;
+                const int64_t seg_end = (int64_t)m.begin(q + 1) * rb;
+                const int64_t delta = ((int64_t)m.dest(q) - (int64_t)m.begin(q)) * rb;
                 const int64_t pe = min(c1, seg_end);
                 if (p.hints & MRR_HINT_STORE_EVICT_FIRST)
                     bulk_s2g_hint(p.out_tokens + pos + delta, sbase + (uint32_t)(pos - c0), (uint32_t)(pe - pos),
@@ -827,15 +871,20 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
     }
 
     uint32_t flags;
-    const uint32_t *row_ex, *dst_off;
+    SegMap m;
+    m.NE = p.NE;
+    m.N = p.N;
+    m.E = p.E;
+    m.inv = p.inverse;
     if (kFused) {
         uint32_t *rex = tab, *cnt_t = tab + p.NE + 1, *dof = cnt_t + padded_len(p.NE);
         flags = cta_scan(p, cb, rex, cnt_t, dof, s_warp, &s_flags, &s_sum);
-        row_ex = rex;
-        dst_off = dof;
+        m.row_ex = rex;
+        m.dst_off = dof;
+        m.col_ex = cnt_t;
         if (b == 0) {
-            if (!flags)
-                write_expert_token_num(p, dst_off, tid, nthr);
+            if (!flags && !p.inverse)
+                write_expert_token_num(p, dof, tid, nthr);
             if (tid == 0) {
                 p.status[0] = flags;
                 p.status[1] = (uint32_t)G;
@@ -844,8 +893,9 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
     } else {
         __syncthreads();  // s_first[1] cleared before warp 1 may set it
         flags = *reinterpret_cast<volatile uint32_t *>(p.status);  // written by the scan kernel
-        row_ex = p.g_row_ex;
-        dst_off = p.g_dst_off;
+        m.row_ex = p.g_row_ex;
+        m.dst_off = p.g_dst_off;
+        m.col_ex = p.g_col_ex;
         if (b == 0 && tid == 0)
             p.status[1] = (uint32_t)G;
     }
@@ -853,18 +903,18 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
     uint32_t tflag = 0u;
     if (kBulk) {
         if (tid == 0) {
-            tflag = bulk_driver(p, ring, row_ex, dst_off, flags, s_first);
+            tflag = bulk_driver(p, ring, m, flags, s_first);
         } else if (tid >= 32 && !flags) {
             if (tid == 32 && dynamic && ring.dyn_first >= 0) {
                 s_first[0] = claim_first_ticket(p.ticket, p.epoch);
                 __threadfence_block();
                 s_first[1] = 1u;
             }
-            side_arrays(p, row_ex, dst_off, tid - 32, nthr - 32);
+            side_arrays(p, m, tid - 32, nthr - 32);
         }
     } else if (!flags) {
-        vector_copy(p, row_ex, dst_off, lo, hi, tid, nthr);
-        side_arrays(p, row_ex, dst_off, tid, nthr);
+        vector_copy(p, m, lo, hi, tid, nthr);
+        side_arrays(p, m, tid, nthr);
     }
     if (tid == 0)
         p.status[2 + b] = tflag;
@@ -935,10 +985,15 @@ __global__ void __launch_bounds__(1024) scan_kernel(const Params p)
         const uint32_t ex = block_exscan(v, &total, s_warp);
         if (pos < NE)
             p.g_dst_off[pad32(q)] = carry + ex;
+        if (pos < NE && p.inverse)
+            p.g_col_ex[pad32(pos)] = carry + ex;
         carry += total;
     }
+    if (tid == 0 && p.inverse)
+        p.g_col_ex[pad32(NE)] = (uint32_t)p.A;
     __syncthreads();  // global writes of the block visible to the whole block
-    write_expert_token_num(p, p.g_dst_off, tid, nthr);
+    if (!p.inverse)
+        write_expert_token_num(p, p.g_dst_off, tid, nthr);
     if (tid == 0)
         p.status[0] = 0u;
 }
@@ -974,7 +1029,11 @@ int token_bits(int dt)
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
 // workspace bytes of the two offset tables for N*E > 4096: SrcOffset dense, DstOffset padded
-int64_t table_workspace_bytes(int64_t NE) { return round_up(4 * (NE + 1), 256) + round_up(4 * padded_len(NE), 256); }
+int64_t table_workspace_bytes(int64_t NE, int inverse)
+{
+    return round_up(4 * (NE + 1), 256) + round_up(4 * padded_len(NE), 256) +
+           (inverse ? round_up(4 * padded_len(NE), 256) : 0);
+}
 
 int widest_width(uintptr_t a, uintptr_t b, int64_t bytes, int cap)
 {
@@ -1037,20 +1096,25 @@ mrr_status check_shape(int64_t A, int64_t H, int dt, int64_t N, int64_t E, int c
 
 // pointer checks shared by run and run_plan (section 参数说明: the top-k input and output come
 // as a pair; scales need an output; index and counts are read/written as their int types)
+// (inverse: the move back to rank-major order, which writes no index and no counts)
 mrr_status check_buffers(int64_t NE, int64_t E, int cb, int sl, const void *tokens, const void *counts,
                          const void *scales, const void *topk_w, const void *permute_tokens,
                          const void *permute_scales, const void *idx, const void *etn, const void *permute_topk_w,
-                         const void *workspace, size_t workspace_bytes)
+                         const void *workspace, size_t workspace_bytes, int inverse = 0)
 {
+    if (inverse) {
+        idx = nullptr;
+        etn = nullptr;
+    }
     if ((topk_w == nullptr) != (permute_topk_w == nullptr))
         return MRR_ERR_TOPK_PAIR;
     if (sl != MRR_SCALE_NONE && (!scales || !permute_scales))
         return MRR_ERR_NULL;
     if (sl == MRR_SCALE_NONE && scales)
         return MRR_ERR_DTYPE;
-    if (E > 0 && !etn)
+    if (!inverse && E > 0 && !etn)
         return MRR_ERR_NULL;
-    if (NE > 0 && (!tokens || !counts || !permute_tokens || !idx))
+    if (NE > 0 && (!tokens || !counts || !permute_tokens || (!inverse && !idx)))
         return MRR_ERR_NULL;
     if (((uintptr_t)counts % cb) || ((uintptr_t)etn % cb) || ((uintptr_t)idx % 4))
         return MRR_ERR_ALIGN;
@@ -1165,9 +1229,13 @@ const char *mrr_status_str(mrr_status s)
     return "unknown mrr_status";
 }
 
-mrr_status mrr_v2_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int64_t E, int count_is_i64,
-                       mrr_scale_layout sl, int64_t scale_cols, int has_topk, int64_t expert_token_num_type,
-                       int64_t idx_type, int device, mrr_v2_plan_t *out)
+}  // extern "C"
+
+namespace {
+
+mrr_status make_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int64_t E, int count_is_i64,
+                     mrr_scale_layout sl, int64_t scale_cols, int has_topk, int64_t expert_token_num_type,
+                     int64_t idx_type, int device, int direction, mrr_v2_plan_t *out)
 {
     if (!out)
         return MRR_ERR_NULL;
@@ -1200,6 +1268,7 @@ mrr_status mrr_v2_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int6
     p.path = (rb % 16 == 0) ? MRR_PATH_BULK : MRR_PATH_VECTOR;
     p.num_sms = sms;
     p.pdl = 1;
+    p.direction = direction;
     const int64_t table_bytes = p.fuse_scan ? round_up(4 * (NE + 1 + 2 * padded_len(NE)), 128) : 0;
     if (p.path == MRR_PATH_BULK) {
         // the deepest ring shared memory allows: 3 x 64 KiB, else 3 x 48 KiB, else 4 x 32 KiB, ...
@@ -1236,9 +1305,28 @@ mrr_status mrr_v2_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int6
     }
     if (p.grid > kMaxGrid)
         p.grid = kMaxGrid;
-    p.workspace_bytes = kHeaderBytes + (p.fuse_scan ? 0 : table_workspace_bytes(NE));
+    p.workspace_bytes = kHeaderBytes + (p.fuse_scan ? 0 : table_workspace_bytes(NE, direction));
     *out = p;
     return MRR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mrr_status mrr_v2_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int64_t E, int count_is_i64,
+                       mrr_scale_layout sl, int64_t scale_cols, int has_topk, int64_t expert_token_num_type,
+                       int64_t idx_type, int device, mrr_v2_plan_t *out)
+{
+    return make_plan(A, H, dt, N, E, count_is_i64, sl, scale_cols, has_topk, expert_token_num_type, idx_type,
+                     device, 0, out);
+}
+
+mrr_status mrr_v2_unroute_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int64_t E, int count_is_i64,
+                               mrr_scale_layout sl, int64_t scale_cols, int has_topk, int device,
+                               mrr_v2_plan_t *out)
+{
+    return make_plan(A, H, dt, N, E, count_is_i64, sl, scale_cols, has_topk, 1, 0, device, 1, out);
 }
 
 mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_token_dtype dt, const void *counts,
@@ -1261,9 +1349,16 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
         return MRR_ERR_PLAN;
     const int64_t A = pl.A, N = pl.N, E = pl.E, NE = N * E;
     const int cb = pl.count_is_i64 ? 8 : 4;
+    if (pl.direction != 0 && pl.direction != 1)
+        return MRR_ERR_PLAN;
+    const int inverse = pl.direction;
+    if (inverse) {
+        permute_token_idx = nullptr;
+        expert_token_num = nullptr;
+    }
 
     st = check_buffers(NE, E, cb, pl.scale_layout, tokens, counts, scales, topk_w, permute_tokens, permute_scales,
-                       permute_token_idx, expert_token_num, permute_topk_w, workspace, workspace_bytes);
+                       permute_token_idx, expert_token_num, permute_topk_w, workspace, workspace_bytes, inverse);
     if (st != MRR_OK)
         return st;
     if ((topk_w != nullptr) != (pl.has_topk != 0))
@@ -1275,7 +1370,7 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
     const int64_t table_bytes = pl.fuse_scan ? round_up(4 * (NE + 1 + 2 * padded_len(NE)), 128) : 0;
     if (pl.fuse_scan != (NE <= kFusedMaxSegs ? 1 : 0))
         return MRR_ERR_PLAN;
-    if (pl.workspace_bytes < kHeaderBytes + (pl.fuse_scan ? 0 : table_workspace_bytes(NE)))
+    if (pl.workspace_bytes < kHeaderBytes + (pl.fuse_scan ? 0 : table_workspace_bytes(NE, inverse)))
         return MRR_ERR_PLAN;
     if (pl.grid < 1 || pl.grid > kMaxGrid || pl.block < 64 || pl.block > 1024 || pl.block % 32)
         return MRR_ERR_PLAN;
@@ -1324,7 +1419,7 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
     if (NE == 0) {
         // the empty problem: no rows; expert_token_num is all zero
         cudaError_t e = cudaSuccess;
-        if (E > 0)
+        if (E > 0 && !inverse)
             e = cudaMemsetAsync(expert_token_num, 0, (size_t)(E * cb), stream);
         if (e == cudaSuccess)
             e = cudaMemsetAsync(status, 0, 8, stream);
@@ -1357,6 +1452,7 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
     p.idx = permute_token_idx;
     p.idx_type = pl.idx_type;
     p.etn = expert_token_num;
+    p.inverse = inverse;
     p.status = status;
     p.chunk_bytes = pl.chunk_bytes;
     p.stages = pl.stages;
@@ -1369,6 +1465,9 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
         uint8_t *ws = static_cast<uint8_t *>(workspace) + kHeaderBytes;
         p.g_row_ex = reinterpret_cast<uint32_t *>(ws);
         p.g_dst_off = reinterpret_cast<uint32_t *>(ws + round_up(4 * (NE + 1), 256));
+        if (inverse)
+            p.g_col_ex = reinterpret_cast<uint32_t *>(ws + round_up(4 * (NE + 1), 256) +
+                                                      round_up(4 * padded_len(NE), 256));
     }
 
     cudaError_t e = cudaSuccess;
@@ -1424,6 +1523,36 @@ mrr_status mrr_v2_run(const void *tokens, mrr_token_dtype dt, int64_t A, int64_t
     return mrr_v2_run_plan(&plan, tokens, dt, counts, scales, topk_w, permute_tokens, permute_scales,
                            permute_token_idx, expert_token_num, permute_topk_w, expert_token_num_type, workspace,
                            workspace_bytes, stream);
+}
+
+mrr_status mrr_v2_unroute(const void *permute_tokens, mrr_token_dtype dt, int64_t A, int64_t H, const void *counts,
+                          int count_is_i64, int64_t N, int64_t E, const void *permute_scales, mrr_scale_layout sl,
+                          int64_t scale_cols, const float *permute_topk_w, void *tokens, void *scales,
+                          float *topk_w, void *workspace, size_t workspace_bytes, mrr_stream_t stream)
+{
+    int64_t rb = 0, sb = 0;
+    mrr_status st = check_shape(A, H, (int)dt, N, E, count_is_i64, (int)sl, scale_cols, 1, 0, &rb, &sb);
+    if (st != MRR_OK)
+        return st;
+    if (sl == MRR_SCALE_NONE)
+        permute_scales = nullptr;
+    st = check_buffers(N * E, E, count_is_i64 ? 8 : 4, (int)sl, permute_tokens, counts, permute_scales,
+                       permute_topk_w, tokens, scales, nullptr, nullptr, topk_w, workspace, workspace_bytes, 1);
+    if (st != MRR_OK)
+        return st;
+    int device = -1;
+    if (cudaGetDevice(&device) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return MRR_ERR_CUDA;
+    }
+    mrr_v2_plan_t plan;
+    st = mrr_v2_unroute_plan(A, H, dt, N, E, count_is_i64, sl, scale_cols, permute_topk_w != nullptr, device,
+                             &plan);
+    if (st != MRR_OK)
+        return st;
+    plan.path = MRR_PATH_AUTO;
+    return mrr_v2_run_plan(&plan, permute_tokens, dt, counts, permute_scales, permute_topk_w, tokens, scales,
+                           nullptr, nullptr, topk_w, 1, workspace, workspace_bytes, stream);
 }
 
 mrr_status mrr_v2_read_status(const void *workspace, size_t workspace_bytes, mrr_stream_t stream_)

@@ -63,7 +63,7 @@ class mrr_v2_plan_t(ctypes.Structure):
         ("fuse_scan", ctypes.c_int32), ("path", ctypes.c_int32), ("grid", ctypes.c_int32),
         ("block", ctypes.c_int32), ("chunk_bytes", ctypes.c_int32), ("stages", ctypes.c_int32),
         ("hints", ctypes.c_int32), ("sched", ctypes.c_int32), ("static_chunks", ctypes.c_int32),
-        ("pdl", ctypes.c_int32),
+        ("pdl", ctypes.c_int32), ("direction", ctypes.c_int32),
         ("smem_bytes", ctypes.c_int32), ("num_sms", ctypes.c_int32),
     ]
 
@@ -105,6 +105,12 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                                     P, P, P, P, P, I64, P, ctypes.c_size_t, P]
     lib.mrr_v2_read_status.restype = I32
     lib.mrr_v2_read_status.argtypes = [P, ctypes.c_size_t, P]
+    lib.mrr_v2_unroute_plan.restype = I32
+    lib.mrr_v2_unroute_plan.argtypes = [I64, I64, I32, I64, I64, I32, I32, I64, I32, I32,
+                                        ctypes.POINTER(mrr_v2_plan_t)]
+    lib.mrr_v2_unroute.restype = I32
+    lib.mrr_v2_unroute.argtypes = [P, I32, I64, I64, P, I32, I64, I64, P, I32, I64, P, P, P, P, P,
+                                   ctypes.c_size_t, P]
     lib.mrr_v2_run_noalloc.restype = I32
     lib.mrr_v2_run_noalloc.argtypes = [P, I32, I64, I64, P, I32, I64, I64, P, I32, I64, P,
                                        P, P, P, P, P, I64, I64, I32, P]
@@ -152,6 +158,23 @@ def mrr_v2_run_plan(plan: mrr_v2_plan_t, tokens, dt, counts, scales, topk_w, per
         ctypes.byref(plan), tokens, dt, counts, scales, topk_w, permute_tokens, permute_scales,
         permute_token_idx, expert_token_num, permute_topk_w, expert_token_num_type, workspace,
         workspace_bytes, stream)
+
+
+def mrr_v2_unroute_plan(A, H, dt, N, E, count_is_i64, sl, scale_cols, has_topk,
+                        device=0) -> Tuple[int, mrr_v2_plan_t]:
+    plan = mrr_v2_plan_t()
+    st = load_library().mrr_v2_unroute_plan(A, H, dt, N, E, int(count_is_i64), sl, scale_cols,
+                                            int(has_topk), device, ctypes.byref(plan))
+    return st, plan
+
+
+def mrr_v2_unroute(permute_tokens, dt, A, H, counts, count_is_i64, N, E, permute_scales, sl,
+                   scale_cols, permute_topk_w, tokens, scales, topk_w, workspace, workspace_bytes,
+                   stream) -> int:
+    """The inverse move (expert-major rows back to rank-major order); integer device addresses."""
+    return load_library().mrr_v2_unroute(
+        permute_tokens, dt, A, H, counts, int(count_is_i64), N, E, permute_scales, sl, scale_cols,
+        permute_topk_w, tokens, scales, topk_w, workspace, workspace_bytes, stream)
 
 
 def mrr_v2_read_status(workspace, workspace_bytes, stream) -> int:
@@ -279,3 +302,57 @@ def moe_re_routing(tokens, expert_token_num_per_rank, *, per_token_scales=None,
             if st != MRR_OK:
                 raise MrrError(st, "device")
     return out_tok, out_sc, idx, etn, out_tw
+
+
+def moe_re_routing_inverse(permute_tokens, expert_token_num_per_rank, *,
+                           permute_per_token_scales=None, permute_topk_weight=None,
+                           tokens_dtype: Optional[str] = None, workspace=None, stream=None,
+                           check_status: bool = False):
+    """Move expert-major rows back to the rank-major order they arrived in (the combine side).
+
+    ``expert_token_num_per_rank`` is the same count matrix the forward move used.  Returns
+    (tokens, per_token_scales, topk_weight); the last two are None when not given.
+    """
+    import torch
+
+    t, c = permute_tokens, expert_token_num_per_rank
+    if t.dim() != 2 or c.dim() != 2 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError("permute_tokens must be a contiguous 2-D CUDA tensor, counts 2-D")
+    if c.dtype not in (torch.int32, torch.int64):
+        raise TypeError("expert_token_num_per_rank must be int32 or int64")
+    dev = t.device
+    code, H = _torch_token_code(t, tokens_dtype)
+    A = t.shape[0]
+    N, E = c.shape
+    sl, scale_cols = _scale_layout(permute_per_token_scales)
+    for x in (c, permute_per_token_scales, permute_topk_weight):
+        if x is not None and (x.device != dev or not x.is_contiguous()):
+            raise ValueError("all tensors must be contiguous and on the tokens' device")
+    st, plan = mrr_v2_unroute_plan(A, H, code, N, E, c.dtype == torch.int64, sl, scale_cols,
+                                   permute_topk_weight is not None,
+                                   dev.index if dev.index is not None else torch.cuda.current_device())
+    if st != MRR_OK:
+        raise MrrError(st, "mrr_v2_unroute_plan")
+    out_tok = torch.empty_like(t)
+    out_sc = None if permute_per_token_scales is None else torch.empty_like(permute_per_token_scales)
+    out_tw = None if permute_topk_weight is None else torch.empty_like(permute_topk_weight)
+    if workspace is None or workspace.numel() < plan.workspace_bytes:
+        workspace = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+
+    def ptr(x):
+        return None if x is None else x.data_ptr()
+
+    with torch.cuda.device(dev):
+        st = mrr_v2_unroute(ptr(t), code, A, H, ptr(c), c.dtype == torch.int64, N, E,
+                            ptr(permute_per_token_scales), sl, scale_cols, ptr(permute_topk_weight),
+                            ptr(out_tok), ptr(out_sc), ptr(out_tw), workspace.data_ptr(),
+                            workspace.numel(), stream.cuda_stream)
+        if st != MRR_OK:
+            raise MrrError(st, "mrr_v2_unroute")
+        if check_status:
+            st = mrr_v2_read_status(workspace.data_ptr(), workspace.numel(), stream.cuda_stream)
+            if st != MRR_OK:
+                raise MrrError(st, "device")
+    return out_tok, out_sc, out_tw

@@ -137,3 +137,68 @@ def assert_bit_exact(gpu: dict, ref: dict, p) -> None:
     if p.topk is not None:
         assert np.array_equal(gpu["permute_topk_weight"].view(np.uint32),
                               ref["permute_topk_weight"].view(np.uint32)), "permute_topk_weight"
+
+
+def run_gpu_unroute(p, *, path: Optional[int] = None, edit: Optional[dict] = None,
+                    offsets: Optional[dict] = None, device="cuda:0",
+                    counts: Optional[np.ndarray] = None, workspace: Optional[DevBuf] = None,
+                    expect_host_status: int = m.MRR_OK) -> dict:
+    """Run the inverse move on the GPU through the C ABI.  The problem's tokens / scales / top-k
+    payloads serve as the EXPERT-MAJOR inputs; returns the rank-major outputs."""
+    import torch
+
+    offsets = offsets or {}
+    c = p.counts if counts is None else counts
+    code = m.DTYPE_CODES[p.token_dtype]
+    sl = m.SCALE_CODES[p.scale_layout]
+    A, H, (N, E) = p.A, p.H, c.shape
+    d = torch.device(device)
+    pt = DevBuf.of(p.tokens, d, offsets.get("permute_tokens", 0))
+    cnt = DevBuf.of(c, d, offsets.get("counts", 0))
+    ps = DevBuf.of(p.scales, d, offsets.get("permute_scales", 0))
+    pw = DevBuf.of(p.topk, d, offsets.get("permute_topk", 0))
+    out_tok = DevBuf(A * p.row_bytes, d, offsets.get("tokens", 0))
+    out_sc = None if p.scales is None else DevBuf(A * p.scale_row_bytes, d, offsets.get("scales", 0))
+    out_tw = None if p.topk is None else DevBuf(4 * A, d, offsets.get("topk", 0))
+    st, plan = m.mrr_v2_unroute_plan(A, H, code, N, E, c.dtype == np.int64, sl, p.scale_cols,
+                                     p.topk is not None, d.index or 0)
+    assert st == m.MRR_OK, m.mrr_status_str(st)
+    assert plan.direction == 1
+    if workspace is None:
+        workspace = DevBuf(plan.workspace_bytes, d, 0, fill=0x5A)
+    stream = torch.cuda.current_stream(d).cuda_stream
+    if path is None and not edit:
+        st = m.mrr_v2_unroute(ptr(pt), code, A, H, ptr(cnt), c.dtype == np.int64, N, E, ptr(ps), sl,
+                              p.scale_cols, ptr(pw), ptr(out_tok), ptr(out_sc), ptr(out_tw),
+                              workspace.ptr, workspace.n, stream)
+    else:
+        if path is not None:
+            plan.path = path
+        for k, v in (edit or {}).items():
+            setattr(plan, k, v)
+        st = m.mrr_v2_run_plan(plan, ptr(pt), code, ptr(cnt), ptr(ps), ptr(pw), ptr(out_tok),
+                               ptr(out_sc), None, None, ptr(out_tw), 1, workspace.ptr, workspace.n,
+                               stream)
+    assert st == expect_host_status, m.mrr_status_str(st)
+    out = {"host_status": st, "plan": plan.as_dict()}
+    if st != m.MRR_OK:
+        return out
+    out["status"] = m.mrr_v2_read_status(workspace.ptr, workspace.n, stream)
+    torch.cuda.synchronize(d)
+    out["tokens"] = out_tok.host().reshape(A, p.row_bytes)
+    out["scales"] = None if out_sc is None else out_sc.host().reshape(A, p.scale_row_bytes)
+    out["topk_weight"] = None if out_tw is None else out_tw.host().view(np.float32)
+    out["guards_intact"] = all(b.guards_intact() for b in (out_tok, out_sc, out_tw) if b is not None)
+    return out
+
+
+def assert_unroute_bit_exact(gpu: dict, ref: dict, p) -> None:
+    assert gpu["status"] == m.MRR_OK, m.mrr_status_str(gpu["status"])
+    assert gpu["guards_intact"], "an output guard band was overwritten"
+    if not np.array_equal(gpu["tokens"], ref["tokens"]):
+        bad = np.nonzero((gpu["tokens"] != ref["tokens"]).any(axis=1))[0]
+        raise AssertionError(f"tokens differ in {bad.size} rows, first {bad[:8].tolist()}")
+    if p.scales is not None:
+        assert np.array_equal(gpu["scales"], ref["scales"]), "scales"
+    if p.topk is not None:
+        assert np.array_equal(gpu["topk_weight"].view(np.uint32), ref["topk_weight"].view(np.uint32)), "topk"

@@ -25,7 +25,8 @@ def lib():
 def test_exports_every_header_function(lib):
     names = m.header_functions()
     assert set(names) == {"mrr_v2_plan", "mrr_v2_run", "mrr_v2_run_plan", "mrr_v2_read_status",
-                          "mrr_status_str", "mrr_v2_run_noalloc"}
+                          "mrr_status_str", "mrr_v2_run_noalloc", "mrr_v2_unroute_plan",
+                          "mrr_v2_unroute"}
     out = subprocess.run(["nm", "-D", "--defined-only", m.library_path()], capture_output=True,
                          text=True, check=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
@@ -156,5 +157,5 @@ def test_run_plan_rejects_null_plan(lib):
 
 
 def test_plan_struct_layout_matches_header():
-    # 7 int64 fields followed by 16 int32 fields
-    assert ctypes.sizeof(m.mrr_v2_plan_t) == 7 * 8 + 16 * 4
+    # 7 int64 fields followed by 17 int32 fields, padded to 8 bytes
+    assert ctypes.sizeof(m.mrr_v2_plan_t) == 7 * 8 + 17 * 4 + 4
