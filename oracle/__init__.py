@@ -66,6 +66,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.mrr_oracle_validate.argtypes = [P, ctypes.c_int, I64, I64, I64]
     lib.mrr_oracle_offsets.restype = None
     lib.mrr_oracle_offsets.argtypes = [P, ctypes.c_int, I64, I64, P, P]
+    lib.mrr_oracle_expert_token_num.restype = ctypes.c_int
+    lib.mrr_oracle_expert_token_num.argtypes = [P, ctypes.c_int, I64, I64, I64, P]
     lib.mrr_oracle_unroute.restype = ctypes.c_int
     lib.mrr_oracle_unroute.argtypes = [P, I64, I64, P, ctypes.c_int, I64, I64, P, I64, P, P, P, P]
     return lib
@@ -106,8 +108,22 @@ def validate(counts: np.ndarray, A: int, lib: Optional[ctypes.CDLL] = None) -> i
     return lib.mrr_oracle_validate(_ptr(c), int(c.dtype == np.int64), N, E, A)
 
 
+def expert_token_num(counts: np.ndarray, expert_token_num_type: int = 1,
+                     lib: Optional[ctypes.CDLL] = None) -> np.ndarray:
+    """expert_token_num in count mode (1) or inclusive cumsum mode (0), in the counts' dtype."""
+    lib = lib or load()
+    c = np.ascontiguousarray(counts)
+    N, E = c.shape
+    out = np.empty(E, c.dtype)
+    rc = lib.mrr_oracle_expert_token_num(_ptr(c), int(c.dtype == np.int64), N, E,
+                                         expert_token_num_type, _ptr(out))
+    if rc != ORC_OK:
+        raise OracleError(rc)
+    return out
+
+
 def run(tokens: np.ndarray, counts: np.ndarray, *, scales: Optional[np.ndarray] = None,
-        topk: Optional[np.ndarray] = None, idx_type: int = 0,
+        topk: Optional[np.ndarray] = None, idx_type: int = 0, expert_token_num_type: int = 1,
         lib: Optional[ctypes.CDLL] = None) -> dict:
     """Run the op on byte rows.
 
@@ -139,13 +155,16 @@ def run(tokens: np.ndarray, counts: np.ndarray, *, scales: Optional[np.ndarray] 
                             _ptr(etn), _ptr(out_tw), idx_type)
     if rc != ORC_OK:
         raise OracleError(rc)
+    if expert_token_num_type != 1:
+        etn = expert_token_num(c, expert_token_num_type, lib=lib)
     return {"permute_tokens": out_tok, "permute_scales": out_sc, "permute_token_idx": idx,
             "expert_token_num": etn, "permute_topk_weight": out_tw}
 
 
 def run_problem(p, lib: Optional[ctypes.CDLL] = None) -> dict:
     """Run the oracle on a ``workloads.Problem``."""
-    return run(p.tokens, p.counts, scales=p.scales, topk=p.topk, idx_type=p.idx_type, lib=lib)
+    return run(p.tokens, p.counts, scales=p.scales, topk=p.topk, idx_type=p.idx_type,
+               expert_token_num_type=p.expert_token_num_type, lib=lib)
 
 
 def unroute(permute_tokens: np.ndarray, counts: np.ndarray, *, permute_scales: Optional[np.ndarray] = None,

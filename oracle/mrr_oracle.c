@@ -225,3 +225,32 @@ int mrr_oracle_unroute(const uint8_t *permute_tokens, int64_t A, int64_t row_byt
     free(dst_off);
     return ORC_OK;
 }
+
+/*
+ * expert_token_num in either mode ("CANN ops-transformer MoeReRoutingV2" article, section
+ * 参数说明: 0 = cumsum mode, 1 = count mode; the dispatch page, parameter
+ * expert_token_nums_type: 0 = prefix sum of the tokens each expert received, 1 = the count).
+ *   count mode:  out[j] = sum over ranks i of counts[i][j]
+ *   cumsum mode: out[j] = sum over experts j' <= j of the count-mode value (inclusive, so the
+ *                last entry is A)
+ * Written in the counts' integer type.  Returns ORC_ERR_ARG for a mode other than 0 or 1.
+ */
+int mrr_oracle_expert_token_num(const void *counts, int count_is_i64, int64_t N, int64_t E,
+                                int64_t expert_token_num_type, void *out)
+{
+    int64_t running = 0;
+    if (expert_token_num_type != 0 && expert_token_num_type != 1)
+        return ORC_ERR_ARG;
+    for (int64_t j = 0; j < E; ++j) {
+        int64_t total = 0;
+        for (int64_t i = 0; i < N; ++i)
+            total += count_at(counts, count_is_i64, E, i, j);
+        running += total;
+        const int64_t v = expert_token_num_type == 1 ? total : running;
+        if (count_is_i64)
+            ((int64_t *)out)[j] = v;
+        else
+            ((int32_t *)out)[j] = (int32_t)v;
+    }
+    return ORC_OK;
+}

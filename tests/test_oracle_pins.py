@@ -241,6 +241,29 @@ def test_unroute_rejects_invalid_counts():
     assert e.value.code == oracle.ORC_ERR_COUNT_SUM
 
 
+@pytest.mark.parametrize("seed,N,E,dt", [(21, 4, 4, np.int32), (22, 8, 32, np.int64), (23, 1, 9, np.int32),
+                                         (24, 13, 1, np.int64)])
+def test_expert_token_num_modes(oracle_lib, seed, N, E, dt):
+    """Count mode = numpy column sums; cumsum mode = numpy's (inclusive) cumsum of them, last = A."""
+    c = workloads.counts_uniform(np.random.default_rng(seed), N, E, N * E * 5, dt)
+    count = oracle.expert_token_num(c, 1, lib=oracle_lib)
+    cum = oracle.expert_token_num(c, 0, lib=oracle_lib)
+    assert count.dtype == dt and cum.dtype == dt
+    assert np.array_equal(count, c.sum(axis=0))
+    assert np.array_equal(cum, np.cumsum(c.sum(axis=0)))
+    assert int(cum[-1]) == N * E * 5
+    run0 = oracle.run(row_payload(N * E * 5, 2), c, expert_token_num_type=0, lib=oracle_lib)
+    assert np.array_equal(run0["expert_token_num"], cum)
+    with pytest.raises(oracle.OracleError):
+        oracle.expert_token_num(c, 2, lib=oracle_lib)
+
+
+def check_cumsum_mode(lib):
+    c = np.array([[1, 2], [3, 1]], np.int32)          # hand example: column sums 4, 3
+    assert oracle.expert_token_num(c, 0, lib=lib).tolist() == [4, 7]
+    assert oracle.expert_token_num(c, 1, lib=lib).tolist() == [4, 3]
+
+
 def test_workload_c1_invariants(oracle_lib):
     check_invariants(oracle_lib, workloads.config(1))
 
@@ -314,8 +337,12 @@ MUTANTS = {
         "permute_token_idx[s] = (int32_t)d;", "permute_token_idx[d] = (int32_t)s;"),
     # expert_token_num as row sums (a transposed operand)
     "etn_row_sums": (
-        "total += count_at(counts, count_is_i64, E, i, j);",
-        "total += count_at(counts, count_is_i64, E, j < N ? j : 0, i < E ? i : 0);"),
+        "total += count_at(counts, count_is_i64, E, i, j);\n        if (count_is_i64)",
+        "total += count_at(counts, count_is_i64, E, j < N ? j : 0, i < E ? i : 0);\n        if (count_is_i64)"),
+    # the same transposition in the two-mode expert_token_num
+    "etn_modes_row_sums": (
+        "total += count_at(counts, count_is_i64, E, i, j);\n        running += total;",
+        "total += count_at(counts, count_is_i64, E, j < N ? j : 0, i < E ? i : 0);\n        running += total;"),
     # the move reads the destination offset on the source side
     "move_src_from_dst": (
         "int64_t s = src_off[i * E + j] + k;\n                int64_t d = dst_off[i * E + j] + k;\n"
@@ -331,13 +358,17 @@ MUTANTS = {
     # inverse move: top-k weights taken from the rank-major position
     "unroute_topk_from_src": ("topk_w[s] = permute_topk_w[d];", "topk_w[s] = permute_topk_w[s];"),
     # inverse move: scale rows moved with the token row size
+    # cumsum mode made exclusive (the running total taken before adding the expert's count)
+    "cumsum_exclusive": ("        running += total;\n        const int64_t v = expert_token_num_type == 1 ? total : running;",
+                         "        const int64_t v = expert_token_num_type == 1 ? total : running;\n        running += total;"),
     "unroute_scale_stride": ("scales + s * scale_row_bytes, permute_scales + d * scale_row_bytes,",
                              "scales + s * scale_row_bytes, permute_scales + d * row_bytes,"),
 }
 
 PINS = [check_hand_examples, check_transpose_closed_form,
         lambda lib: check_brute_force(lib, max_dim=2, max_count=2),
-        check_unroute_hand_examples, lambda lib: check_unroute_brute_force(lib, max_dim=2, max_count=2)]
+        check_unroute_hand_examples, lambda lib: check_unroute_brute_force(lib, max_dim=2, max_count=2),
+        check_cumsum_mode]
 
 
 def _nonpos_pin(lib):
