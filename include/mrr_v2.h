@@ -16,7 +16,7 @@
  *     idx_type 0 = gather index (permute_token_idx[d] = s), 1 = scatter index
  *     (permute_token_idx[s] = d); expert_token_num_type 1 = per-expert count.
  *   - section 约束说明 (constraints): Sum(counts) = A, 0 < H < 16384, every count > 0,
- *     only expert_token_num_type = 1 is supported.
+ *     only expert_token_num_type = 1 is supported (this library also offers 0, cumsum mode).
  *   - section 算子 IR 原型: permute_token_idx is INT32; attribute defaults
  *     expert_token_num_type = 1, idx_type = 0.
  *   - section InferShape 与 InferDtype: output shapes/dtypes follow the inputs; absent scales
@@ -53,7 +53,7 @@ typedef enum mrr_status {
     MRR_ERR_SHAPE = 2,         /* A, H, N, E, scale_cols out of range (see mrr_v2_plan)         */
     MRR_ERR_DTYPE = 3,         /* unknown token dtype or scale layout code                     */
     MRR_ERR_ATTR = 4,          /* expert_token_num_type or idx_type not in {0, 1}              */
-    MRR_ERR_UNSUPPORTED = 5,   /* expert_token_num_type = 0 (cumsum mode; pages: unsupported)  */
+    MRR_ERR_UNSUPPORTED = 5,   /* an option the v1 entry point does not support                */
     MRR_ERR_TOPK_PAIR = 6,     /* exactly one of expert_topk_weight / permute_topk_weight given */
     MRR_ERR_WORKSPACE = 7,     /* workspace NULL, misaligned or smaller than workspace_bytes   */
     MRR_ERR_CUDA = 8,          /* a CUDA runtime call failed (no device, launch error, ...)    */
@@ -138,7 +138,9 @@ typedef struct mrr_v2_plan {
  *   count_is_i64: counts are int64 (1) or int32 (0); expert_token_num has the same type;
  *   sl, scale_cols: the scale layout and elements per scale row (see mrr_scale_layout);
  *   has_topk: expert_topk_weight / permute_topk_weight given;
- *   expert_token_num_type must be 1 (0 -> MRR_ERR_UNSUPPORTED); idx_type 0 or 1.
+ *   expert_token_num_type: 1 = per-expert count, 0 = cumsum mode (an extension: the pages list
+ *   it but support only 1; here it is the inclusive prefix over experts, last entry A);
+ *   idx_type 0 or 1.
  *   Returns MRR_ERR_CUDA when the device cannot be queried (e.g. no GPU).
  */
 mrr_status mrr_v2_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int64_t E,
@@ -194,6 +196,23 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan,
  * workspace_bytes must be >= 4096.
  */
 mrr_status mrr_v2_read_status(const void *workspace, size_t workspace_bytes, mrr_stream_t stream);
+
+/*
+ * mrr_v1_run -- the v1 op (torch_npu.npu_moe_re_routing page: 接口原型, 参数说明, 输出说明): the
+ * same move restricted to what v1 supports, with four outputs and no top-k weights.
+ *   tokens            [A, H] float16 / bfloat16 / int8 only (else MRR_ERR_DTYPE)
+ *   per_token_scales  [A] float32, or NULL; permute_per_token_scales [A] float32, written only
+ *                     when per_token_scales is given (the page: otherwise the output is invalid)
+ *   expert_token_num_type must be 1 and idx_type 0 (other values in {0, 1}:
+ *   MRR_ERR_UNSUPPORTED, as the page states only these are supported).
+ * Workspace: plan.workspace_bytes of mrr_v2_plan for the same shapes.  Otherwise as mrr_v2_run.
+ */
+mrr_status mrr_v1_run(const void *tokens, mrr_token_dtype dt, int64_t A, int64_t H, const void *counts,
+                      int count_is_i64, int64_t N, int64_t E, const float *per_token_scales,
+                      void *permute_tokens, float *permute_per_token_scales,
+                      int32_t *permute_token_idx, void *expert_token_num,
+                      int64_t expert_token_num_type, int64_t idx_type,
+                      void *workspace, size_t workspace_bytes, mrr_stream_t stream);
 
 /*
  * mrr_v2_unroute_plan -- host only: the launch plan of mrr_v2_unroute, which moves the rows

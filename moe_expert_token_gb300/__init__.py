@@ -9,6 +9,8 @@ from .mrr_v2 import (  # noqa: F401
     load_library,
     moe_re_routing,
     moe_re_routing_inverse,
+    moe_re_routing_v1,
+    mrr_v1_run,
     mrr_status_str,
     mrr_v2_plan,
     mrr_v2_read_status,

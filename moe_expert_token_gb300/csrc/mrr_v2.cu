@@ -72,6 +72,7 @@ struct Params {
     uint32_t *g_dst_off;
     uint32_t *g_col_ex;   // N*E > 4096, inverse move: column-major prefix by position (padded)
     int inverse;          // 0: rank-major -> expert-major; 1: the inverse move (no index outputs)
+    int etn_type;         // expert_token_num: 1 per-expert count, 0 inclusive cumsum over experts
     int chunk_bytes;
     int stages;
     int hints;            // bulk path: MRR_HINT_* bits (L2 evict-first policies)
@@ -380,14 +381,15 @@ __device__ uint32_t cta_scan(const Params &p, CountBatch &cb, uint32_t *row_ex, 
     return 0u;
 }
 
-// expert_token_num[j] (count mode) = size of expert j's block in the destination
+// expert_token_num[j], count mode  = size of expert j's block in the destination
 //                                  = DstOffset(0, j+1) - DstOffset(0, j)   (A for the last one)
+//                     cumsum mode = end of expert j's block = DstOffset(0, j+1) (inclusive)
 __device__ __forceinline__ void write_expert_token_num(const Params &p, const uint32_t *dst_off, int t0,
                                                        int ts)
 {
     for (int j = t0; j < p.E; j += ts) {
         const uint32_t next = (j + 1 < p.E) ? dst_off[pad32(j + 1)] : (uint32_t)p.A;
-        const uint32_t v = next - dst_off[pad32(j)];
+        const uint32_t v = p.etn_type == 0 ? next : next - dst_off[pad32(j)];
         if (p.count_is_i64)
             reinterpret_cast<long long *>(p.etn)[j] = (long long)v;
         else
@@ -1055,8 +1057,6 @@ mrr_status check_shape(int64_t A, int64_t H, int dt, int64_t N, int64_t E, int c
         return MRR_ERR_ATTR;
     if (idx_type != 0 && idx_type != 1)
         return MRR_ERR_ATTR;
-    if (etn_type == 0)
-        return MRR_ERR_UNSUPPORTED;
     // section 约束说明: 0 < H < 16384; A = Sum(counts) with every count > 0 (so N*E <= A);
     // the index output is int32, so A <= INT32_MAX
     if (H <= 0 || H >= 16384 || (bits == 4 && (H & 1)))
@@ -1453,6 +1453,7 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
     p.idx_type = pl.idx_type;
     p.etn = expert_token_num;
     p.inverse = inverse;
+    p.etn_type = (int)expert_token_num_type;
     p.status = status;
     p.chunk_bytes = pl.chunk_bytes;
     p.stages = pl.stages;
@@ -1523,6 +1524,26 @@ mrr_status mrr_v2_run(const void *tokens, mrr_token_dtype dt, int64_t A, int64_t
     return mrr_v2_run_plan(&plan, tokens, dt, counts, scales, topk_w, permute_tokens, permute_scales,
                            permute_token_idx, expert_token_num, permute_topk_w, expert_token_num_type, workspace,
                            workspace_bytes, stream);
+}
+
+mrr_status mrr_v1_run(const void *tokens, mrr_token_dtype dt, int64_t A, int64_t H, const void *counts,
+                      int count_is_i64, int64_t N, int64_t E, const float *per_token_scales, void *permute_tokens,
+                      float *permute_per_token_scales, int32_t *permute_token_idx, void *expert_token_num,
+                      int64_t expert_token_num_type, int64_t idx_type, void *workspace, size_t workspace_bytes,
+                      mrr_stream_t stream)
+{
+    // the v1 subset ("torch_npu.npu_moe_re_routing" page, section 参数说明)
+    if (dt != MRR_F16 && dt != MRR_BF16 && dt != MRR_I8)
+        return MRR_ERR_DTYPE;
+    if ((expert_token_num_type != 0 && expert_token_num_type != 1) || (idx_type != 0 && idx_type != 1))
+        return MRR_ERR_ATTR;
+    if (expert_token_num_type != 1 || idx_type != 0)
+        return MRR_ERR_UNSUPPORTED;
+    const bool sc = per_token_scales != nullptr;
+    return mrr_v2_run(tokens, dt, A, H, counts, count_is_i64, N, E, per_token_scales,
+                      sc ? MRR_SCALE_F32_A : MRR_SCALE_NONE, sc ? 1 : 0, nullptr, permute_tokens,
+                      sc ? permute_per_token_scales : nullptr, permute_token_idx, expert_token_num, nullptr, 1, 0,
+                      workspace, workspace_bytes, stream);
 }
 
 mrr_status mrr_v2_unroute(const void *permute_tokens, mrr_token_dtype dt, int64_t A, int64_t H, const void *counts,

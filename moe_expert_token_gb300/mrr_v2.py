@@ -111,6 +111,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.mrr_v2_unroute.restype = I32
     lib.mrr_v2_unroute.argtypes = [P, I32, I64, I64, P, I32, I64, I64, P, I32, I64, P, P, P, P, P,
                                    ctypes.c_size_t, P]
+    lib.mrr_v1_run.restype = I32
+    lib.mrr_v1_run.argtypes = [P, I32, I64, I64, P, I32, I64, I64, P, P, P, P, P, I64, I64, P,
+                               ctypes.c_size_t, P]
     lib.mrr_v2_run_noalloc.restype = I32
     lib.mrr_v2_run_noalloc.argtypes = [P, I32, I64, I64, P, I32, I64, I64, P, I32, I64, P,
                                        P, P, P, P, P, I64, I64, I32, P]
@@ -158,6 +161,16 @@ def mrr_v2_run_plan(plan: mrr_v2_plan_t, tokens, dt, counts, scales, topk_w, per
         ctypes.byref(plan), tokens, dt, counts, scales, topk_w, permute_tokens, permute_scales,
         permute_token_idx, expert_token_num, permute_topk_w, expert_token_num_type, workspace,
         workspace_bytes, stream)
+
+
+def mrr_v1_run(tokens, dt, A, H, counts, count_is_i64, N, E, per_token_scales, permute_tokens,
+               permute_per_token_scales, permute_token_idx, expert_token_num, expert_token_num_type,
+               idx_type, workspace, workspace_bytes, stream) -> int:
+    """The v1 op (float16/bfloat16/int8 tokens, [A] fp32 scales, count mode, gather index)."""
+    return load_library().mrr_v1_run(
+        tokens, dt, A, H, counts, int(count_is_i64), N, E, per_token_scales, permute_tokens,
+        permute_per_token_scales, permute_token_idx, expert_token_num, expert_token_num_type,
+        idx_type, workspace, workspace_bytes, stream)
 
 
 def mrr_v2_unroute_plan(A, H, dt, N, E, count_is_i64, sl, scale_cols, has_topk,
@@ -356,3 +369,51 @@ def moe_re_routing_inverse(permute_tokens, expert_token_num_per_rank, *,
             if st != MRR_OK:
                 raise MrrError(st, "device")
     return out_tok, out_sc, out_tw
+
+
+def moe_re_routing_v1(tokens, expert_token_num_per_rank, *, per_token_scales=None,
+                      expert_token_num_type: int = 1, idx_type: int = 0, workspace=None,
+                      stream=None, check_status: bool = False):
+    """The v1 call (torch_npu.npu_moe_re_routing): float16/bfloat16/int8 tokens, optional [A]
+    float32 scales, count mode and a gather index only; returns (permute_tokens,
+    permute_per_token_scales, permute_token_idx, expert_token_num)."""
+    import torch
+
+    t, c = tokens, expert_token_num_per_rank
+    if t.dim() != 2 or c.dim() != 2 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError("tokens must be a contiguous 2-D CUDA tensor, counts 2-D")
+    codes = {torch.float16: MRR_F16, torch.bfloat16: MRR_BF16, torch.int8: MRR_I8}
+    if t.dtype not in codes:
+        raise TypeError("v1 supports float16, bfloat16 and int8 tokens")
+    if per_token_scales is not None and (per_token_scales.dtype != torch.float32 or per_token_scales.dim() != 1):
+        raise TypeError("v1 per_token_scales are [A] float32")
+    dev = t.device
+    A, H = t.shape
+    N, E = c.shape
+    st, plan = mrr_v2_plan(A, H, codes[t.dtype], N, E, c.dtype == torch.int64,
+                           MRR_SCALE_F32_A if per_token_scales is not None else MRR_SCALE_NONE,
+                           1 if per_token_scales is not None else 0, False, 1, 0,
+                           dev.index if dev.index is not None else torch.cuda.current_device())
+    if st != MRR_OK:
+        raise MrrError(st, "mrr_v2_plan")
+    out_tok = torch.empty_like(t)
+    out_sc = torch.empty(A, dtype=torch.float32, device=dev)
+    idx = torch.empty(A, dtype=torch.int32, device=dev)
+    etn = torch.empty(E, dtype=c.dtype, device=dev)
+    if workspace is None or workspace.numel() < plan.workspace_bytes:
+        workspace = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        st = mrr_v1_run(t.data_ptr(), codes[t.dtype], A, H, c.data_ptr(), c.dtype == torch.int64, N, E,
+                        None if per_token_scales is None else per_token_scales.data_ptr(),
+                        out_tok.data_ptr(), out_sc.data_ptr(), idx.data_ptr(), etn.data_ptr(),
+                        expert_token_num_type, idx_type, workspace.data_ptr(), workspace.numel(),
+                        stream.cuda_stream)
+        if st != MRR_OK:
+            raise MrrError(st, "mrr_v1_run")
+        if check_status:
+            st = mrr_v2_read_status(workspace.data_ptr(), workspace.numel(), stream.cuda_stream)
+            if st != MRR_OK:
+                raise MrrError(st, "device")
+    return out_tok, out_sc, idx, etn

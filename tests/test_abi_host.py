@@ -26,7 +26,7 @@ def test_exports_every_header_function(lib):
     names = m.header_functions()
     assert set(names) == {"mrr_v2_plan", "mrr_v2_run", "mrr_v2_run_plan", "mrr_v2_read_status",
                           "mrr_status_str", "mrr_v2_run_noalloc", "mrr_v2_unroute_plan",
-                          "mrr_v2_unroute"}
+                          "mrr_v2_unroute", "mrr_v1_run"}
     out = subprocess.run(["nm", "-D", "--defined-only", m.library_path()], capture_output=True,
                          text=True, check=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
@@ -74,7 +74,6 @@ def plan(**kw):
     (dict(sl=m.MRR_SCALE_F32_A, scale_cols=2), m.MRR_ERR_SHAPE),
     (dict(sl=m.MRR_SCALE_F32_AS, scale_cols=0), m.MRR_ERR_SHAPE),
     (dict(sl=m.MRR_SCALE_E8M0_AK2, scale_cols=3), m.MRR_ERR_SHAPE),
-    (dict(expert_token_num_type=0), m.MRR_ERR_UNSUPPORTED),
     (dict(expert_token_num_type=2), m.MRR_ERR_ATTR),
     (dict(idx_type=2), m.MRR_ERR_ATTR),
     (dict(idx_type=-1), m.MRR_ERR_ATTR),
@@ -129,7 +128,7 @@ def run(**kw):
     (dict(workspace_bytes=1024), m.MRR_ERR_WORKSPACE),
     (dict(workspace_bytes=4096), m.MRR_ERR_WORKSPACE),                # status, but no counter
     (dict(H=16384), m.MRR_ERR_SHAPE),
-    (dict(expert_token_num_type=0), m.MRR_ERR_UNSUPPORTED),
+    (dict(expert_token_num_type=-1), m.MRR_ERR_ATTR),
     (dict(idx_type=3), m.MRR_ERR_ATTR),
     (dict(dt=42), m.MRR_ERR_DTYPE),
 ])
@@ -159,3 +158,32 @@ def test_run_plan_rejects_null_plan(lib):
 def test_plan_struct_layout_matches_header():
     # 7 int64 fields followed by 17 int32 fields, padded to 8 bytes
     assert ctypes.sizeof(m.mrr_v2_plan_t) == 7 * 8 + 17 * 4 + 4
+
+
+def test_cumsum_mode_passes_the_host_checks(lib):
+    import torch
+
+    st = plan(expert_token_num_type=0)
+    assert st == (m.MRR_OK if torch.cuda.is_available() else m.MRR_ERR_CUDA)
+
+
+def v1(**kw):
+    a = dict(tokens=T, dt=m.MRR_I8, A=64, H=128, counts=C, count_is_i64=0, N=4, E=4,
+             per_token_scales=S, permute_tokens=O1, permute_per_token_scales=O2,
+             permute_token_idx=I, expert_token_num=X, expert_token_num_type=1, idx_type=0,
+             workspace=WS, workspace_bytes=1 << 20, stream=None)
+    a.update(kw)
+    return m.mrr_v1_run(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dt=m.MRR_F8E4M3FN), m.MRR_ERR_DTYPE),      # v1: float16, bfloat16, int8 only
+    (dict(dt=m.MRR_F4E2M1), m.MRR_ERR_DTYPE),
+    (dict(idx_type=1), m.MRR_ERR_UNSUPPORTED),       # v1: gather index only
+    (dict(expert_token_num_type=0), m.MRR_ERR_UNSUPPORTED),
+    (dict(idx_type=2), m.MRR_ERR_ATTR),
+    (dict(permute_token_idx=None), m.MRR_ERR_NULL),
+    (dict(H=0), m.MRR_ERR_SHAPE),
+])
+def test_v1_rejects(lib, kw, code):
+    assert v1(**kw) == code
