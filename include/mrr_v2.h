@@ -62,7 +62,8 @@ typedef enum mrr_status {
     /* found on the GPU; reported by mrr_v2_read_status */
     MRR_ERR_COUNT_NONPOS = 16, /* some counts[i,j] <= 0                                        */
     MRR_ERR_COUNT_SUM = 17,    /* Sum(counts) != A (or a single count > A)                     */
-    MRR_ERR_TIMEOUT = 18       /* a bounded wait inside the copy kernel gave up                */
+    MRR_ERR_TIMEOUT = 18,      /* a bounded wait inside the copy kernel gave up                */
+    MRR_ERR_INDEX = 19         /* gating top-k: an input_ids / tid2eid value out of range     */
 } mrr_status;
 
 /* Token element types (section 参数说明).  Only the width matters: rows move as bytes.

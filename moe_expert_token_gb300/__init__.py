@@ -10,6 +10,8 @@ from .mrr_v2 import (  # noqa: F401
     moe_re_routing,
     moe_re_routing_inverse,
     moe_re_routing_v1,
+    moe_gating_top_k,
+    mrr_gating_topk_run,
     mrr_v1_run,
     mrr_status_str,
     mrr_v2_plan,

@@ -45,6 +45,7 @@ constexpr int kHeaderBytes = kStatusBytes + 256;   // status region + counter; o
 constexpr int kMaxGrid = kStatusWords - 2;
 constexpr int64_t kFusedMaxSegs = 4096;            // N*E scanned inside every CTA up to this
 constexpr uint32_t kFlagNonPos = 1u, kFlagSum = 2u, kFlagTimeout = 4u;
+constexpr uint32_t kFlagBadIndex = 8u;  // set by the gating kernel (gating.cu)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // bound on any single mbarrier wait: 2 s
 constexpr int kMaxStages = 8;
 
@@ -1225,6 +1226,8 @@ const char *mrr_status_str(mrr_status s)
         return "MRR_ERR_COUNT_SUM: the counts do not sum to A";
     case MRR_ERR_TIMEOUT:
         return "MRR_ERR_TIMEOUT: a bounded wait in the copy kernel gave up";
+    case MRR_ERR_INDEX:
+        return "MRR_ERR_INDEX: an input_ids or tid2eid value is out of range";
     }
     return "unknown mrr_status";
 }
@@ -1601,6 +1604,8 @@ mrr_status mrr_v2_read_status(const void *workspace, size_t workspace_bytes, mrr
         return MRR_ERR_COUNT_SUM;
     if (flags & kFlagTimeout)
         return MRR_ERR_TIMEOUT;
+    if (flags & kFlagBadIndex)
+        return MRR_ERR_INDEX;
     return MRR_OK;
 }
 

@@ -32,6 +32,8 @@ MRR_ERR_PLAN = 10
 MRR_ERR_COUNT_NONPOS = 16
 MRR_ERR_COUNT_SUM = 17
 MRR_ERR_TIMEOUT = 18
+MRR_ERR_INDEX = 19
+MRR_GATE_F16, MRR_GATE_BF16, MRR_GATE_F32 = 0, 1, 2
 
 MRR_F16, MRR_BF16, MRR_I8, MRR_F8E5M2, MRR_F8E4M3FN, MRR_HIF8, MRR_F4E2M1, MRR_F4E1M2 = range(8)
 MRR_SCALE_NONE, MRR_SCALE_F32_A, MRR_SCALE_F32_AS, MRR_SCALE_E8M0_AK2 = range(4)
@@ -114,6 +116,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.mrr_v1_run.restype = I32
     lib.mrr_v1_run.argtypes = [P, I32, I64, I64, P, I32, I64, I64, P, P, P, P, P, I64, I64, P,
                                ctypes.c_size_t, P]
+    lib.mrr_gating_topk_run.restype = I32
+    lib.mrr_gating_topk_run.argtypes = [P, I32, I64, I64, I64, P, P, P, I64, P, P, I64, I64,
+                                        ctypes.c_float, ctypes.c_float, I64, I64, I64, P, P, P, P,
+                                        ctypes.c_size_t, P]
     lib.mrr_v2_run_noalloc.restype = I32
     lib.mrr_v2_run_noalloc.argtypes = [P, I32, I64, I64, P, I32, I64, I64, P, I32, I64, P,
                                        P, P, P, P, P, I64, I64, I32, P]
@@ -123,10 +129,15 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
 
 
 def header_functions() -> list:
-    """Names of the functions include/mrr_v2.h declares."""
-    text = open(os.path.join(_build.INCLUDE, "mrr_v2.h"), encoding="utf-8").read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_]\w*\s*\*?\s*(mrr_\w+)\s*\(", text, flags=re.M)))
+    """Names of the functions the headers in include/ declare."""
+    names = set()
+    for h in sorted(os.listdir(_build.INCLUDE)):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(_build.INCLUDE, h), encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_]\w*\s*\*?\s*(mrr_\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
 
 
 # ---------------------------------------------------------------------------- C functions, same names
@@ -417,3 +428,71 @@ def moe_re_routing_v1(tokens, expert_token_num_per_rank, *, per_token_scales=Non
             if st != MRR_OK:
                 raise MrrError(st, "device")
     return out_tok, out_sc, idx, etn
+
+
+def mrr_gating_topk_run(x, dt, T, e, k, bias, input_ids, tid2eid, n_vocab, additional_bias,
+                        additional_token_mask, k_group, group_count, routed_scaling_factor, eps,
+                        group_select_mode, renorm, norm_type, y_out, expert_idx, norm_out,
+                        workspace, workspace_bytes, stream) -> int:
+    """MoE gating top-k (include/mrr_gating.h); integer device addresses or None."""
+    return load_library().mrr_gating_topk_run(
+        x, dt, T, e, k, bias, input_ids, tid2eid, n_vocab, additional_bias, additional_token_mask,
+        k_group, group_count, routed_scaling_factor, eps, group_select_mode, renorm, norm_type,
+        y_out, expert_idx, norm_out, workspace, workspace_bytes, stream)
+
+
+def moe_gating_top_k(x, k: int, *, bias=None, input_ids=None, tid2eid=None, additional_bias=None,
+                     additional_token_mask=None, k_group: int = 1, group_count: int = 1,
+                     routed_scaling_factor: float = 1.0, eps: float = 1e-20,
+                     group_select_mode: int = 0, renorm: int = 0, norm_type: int = 0,
+                     out_flag: bool = False, workspace=None, stream=None, check_status: bool = False):
+    """The torch-level call of the gating op, with the page's signature (npu_moe_gating_top_k):
+    returns (y, expert_idx, out); out is the float32 normalised scores when out_flag, else None.
+    x may be [T, e] or [b, s, e]; outputs keep the leading dimensions."""
+    import torch
+
+    if not x.is_cuda or not x.is_contiguous() or x.dim() not in (2, 3):
+        raise ValueError("x must be a contiguous 2-D or 3-D CUDA tensor")
+    codes = {torch.float16: MRR_GATE_F16, torch.bfloat16: MRR_GATE_BF16, torch.float32: MRR_GATE_F32}
+    if x.dtype not in codes:
+        raise TypeError("x must be float16, bfloat16 or float32")
+    lead = tuple(x.shape[:-1])
+    e = x.shape[-1]
+    T = 1
+    for d in lead:
+        T *= d
+    dev = x.device
+    for b in (bias, additional_bias):
+        if b is not None and (b.dtype != x.dtype or b.numel() != e or b.device != dev):
+            raise ValueError("bias / additional_bias must be [e] in x's dtype on x's device")
+    mask = None
+    if additional_token_mask is not None:
+        if additional_token_mask.dtype != torch.bool or additional_token_mask.numel() != T:
+            raise ValueError("additional_token_mask must be [T] bool")
+        mask = additional_token_mask.contiguous().view(torch.uint8)
+    ids = None if input_ids is None else input_ids.to(torch.int64).contiguous()
+    tab = None if tid2eid is None else tid2eid.to(torch.int32).contiguous()
+    y = torch.empty(*lead, k, dtype=x.dtype, device=dev)
+    idx = torch.empty(*lead, k, dtype=torch.int32, device=dev)
+    out = torch.empty(*lead, e, dtype=torch.float32, device=dev) if out_flag else None
+    if workspace is None:
+        workspace = torch.empty(4096, dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+
+    def ptr(t):
+        return None if t is None else t.data_ptr()
+
+    with torch.cuda.device(dev):
+        st = mrr_gating_topk_run(ptr(x), codes[x.dtype], T, e, k, ptr(bias), ptr(ids), ptr(tab),
+                                 0 if tab is None else tab.shape[0], ptr(additional_bias), ptr(mask),
+                                 k_group, group_count, routed_scaling_factor, eps, group_select_mode,
+                                 renorm, norm_type, ptr(y), ptr(idx), ptr(out), workspace.data_ptr(),
+                                 workspace.numel(), stream.cuda_stream)
+        if st != MRR_OK:
+            raise MrrError(st, "mrr_gating_topk_run")
+        if check_status:
+            st = mrr_v2_read_status(workspace.data_ptr(), workspace.numel(), stream.cuda_stream)
+            if st != MRR_OK:
+                raise MrrError(st, "device")
+    return y, idx, out

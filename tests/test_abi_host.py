@@ -26,7 +26,7 @@ def test_exports_every_header_function(lib):
     names = m.header_functions()
     assert set(names) == {"mrr_v2_plan", "mrr_v2_run", "mrr_v2_run_plan", "mrr_v2_read_status",
                           "mrr_status_str", "mrr_v2_run_noalloc", "mrr_v2_unroute_plan",
-                          "mrr_v2_unroute", "mrr_v1_run"}
+                          "mrr_v2_unroute", "mrr_v1_run", "mrr_gating_topk_run"}
     out = subprocess.run(["nm", "-D", "--defined-only", m.library_path()], capture_output=True,
                          text=True, check=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
@@ -44,7 +44,7 @@ def test_library_has_sm103a_code():
 
 
 def test_status_strings(lib):
-    for code in list(range(0, 11)) + [16, 17, 18]:
+    for code in list(range(0, 11)) + [16, 17, 18, 19]:
         s = m.mrr_status_str(code)
         assert s.startswith("MRR_"), (code, s)
     assert m.mrr_status_str(12345) == "unknown mrr_status"
@@ -187,3 +187,34 @@ def v1(**kw):
 ])
 def test_v1_rejects(lib, kw, code):
     assert v1(**kw) == code
+
+
+def gate(**kw):
+    a = dict(x=T, dt=m.MRR_GATE_F16, T=16, e=384, k=6, bias=None, input_ids=None, tid2eid=None,
+             n_vocab=0, additional_bias=None, additional_token_mask=None, k_group=1, group_count=1,
+             routed_scaling_factor=1.0, eps=1e-20, group_select_mode=0, renorm=0, norm_type=1,
+             y_out=O1, expert_idx=I, norm_out=None, workspace=WS, workspace_bytes=4096, stream=None)
+    a.update(kw)
+    return m.mrr_gating_topk_run(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dt=7), m.MRR_ERR_DTYPE),
+    (dict(renorm=1), m.MRR_ERR_ATTR),                       # the page: renorm supports 0 only
+    (dict(norm_type=3), m.MRR_ERR_ATTR),
+    (dict(group_select_mode=2), m.MRR_ERR_ATTR),
+    (dict(input_ids=C), m.MRR_ERR_TOPK_PAIR),               # input_ids and tid2eid together
+    (dict(k=65), m.MRR_ERR_SHAPE),                          # k <= 64
+    (dict(k=0), m.MRR_ERR_SHAPE),
+    (dict(e=2048), m.MRR_ERR_SHAPE),                        # this implementation: e <= 1024
+    (dict(group_count=5), m.MRR_ERR_SHAPE),                 # e must divide into the groups
+    (dict(group_count=4, k_group=5), m.MRR_ERR_SHAPE),
+    (dict(group_count=64, k_group=1, k=7), m.MRR_ERR_SHAPE),  # k <= e / group_count * k_group
+    (dict(group_count=384, group_select_mode=1), m.MRR_ERR_SHAPE),
+    (dict(input_ids=C, tid2eid=S, n_vocab=0), m.MRR_ERR_SHAPE),
+    (dict(x=None), m.MRR_ERR_NULL),
+    (dict(expert_idx=None), m.MRR_ERR_NULL),
+    (dict(workspace_bytes=100), m.MRR_ERR_WORKSPACE),
+])
+def test_gating_rejects(lib, kw, code):
+    assert gate(**kw) == code

@@ -1,0 +1,211 @@
+"""GPU parity of the MoE gating top-k op (mrr_gating_topk_run) against the CPU oracle.
+
+Integer results (expert_idx) must equal the oracle's wherever the choice is unique.  Both sides
+decide on float32 scores, but the GPU computes the normalisation with float32 exp/log while the
+oracle rounds a float64 result, so two scores within a few float32 ulps may order differently.
+In such rows the GPU's experts must still be a valid top-k under the oracle's scores (their
+scores equal the oracle's chosen scores within that margin).  Floating outputs: y_out within
+the rounding of its dtype (float16 2^-10, bfloat16 2^-7, float32 1e-5, relative) plus 1e-6;
+norm_out (float32) within 2e-5 relative.
+
+Source: "CANN 自定义算子详解：npu_moe_gating_top_k" (m.qwbw.cn/news/316089), sections 归一化公式,
+分组排序公式, 专家选择公式, 路由权重缩放公式 and 调用示例 (the shapes of its test cases).
+"""
+import numpy as np
+import pytest
+
+from oracle import gating
+import moe_expert_token_gb300.mrr_v2 as m
+from harness import DevBuf
+
+pytestmark = pytest.mark.gpu
+
+RTOL = {"float16": 2.0 ** -10, "bfloat16": 2.0 ** -7, "float32": 1e-5}
+CODE = {"float16": m.MRR_GATE_F16, "bfloat16": m.MRR_GATE_BF16, "float32": m.MRR_GATE_F32}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from moe_expert_token_gb300 import build
+
+    build.build()
+    m.load_library()
+
+
+def as_dtype(a: np.ndarray, dt: str) -> np.ndarray:
+    """Round float32 values to dt and return them as float32 (what both sides read)."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(a, np.float32))
+    return t.to(getattr(torch, dt)).to(torch.float32).numpy()
+
+
+def raw(a: np.ndarray, dt: str) -> np.ndarray:
+    import torch
+
+    if a.size == 0:
+        return np.zeros(0, np.uint8)
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(getattr(torch, dt)).view(torch.uint8).numpy()
+
+
+def run_gpu_gating(x32, dt, k, *, bias=None, input_ids=None, tid2eid=None, extra_bias=None, mask=None,
+                   out_flag=True, expect=m.MRR_OK, **kw):
+    import torch
+
+    d = torch.device("cuda:0")
+    T, e = x32.shape
+    xb = DevBuf.of(raw(x32, dt), d)
+    bb = None if bias is None else DevBuf.of(raw(bias, dt), d)
+    eb = None if extra_bias is None else DevBuf.of(raw(extra_bias, dt), d)
+    mb = None if mask is None else DevBuf.of(np.asarray(mask, np.uint8), d)
+    ib = None if input_ids is None else DevBuf.of(np.asarray(input_ids, np.int64), d)
+    tb = None if tid2eid is None else DevBuf.of(np.asarray(tid2eid, np.int32), d)
+    esz = {"float16": 2, "bfloat16": 2, "float32": 4}[dt]
+    y = DevBuf(T * k * esz, d)
+    idx = DevBuf(T * k * 4, d)
+    out = DevBuf(T * e * 4, d) if out_flag else None
+    ws = DevBuf(4096, d, fill=0x5A)
+    args = dict(k_group=1, group_count=1, routed_scaling_factor=1.0, eps=1e-20, group_select_mode=0,
+                renorm=0, norm_type=0)
+    args.update(kw)
+    s = torch.cuda.current_stream().cuda_stream
+    P = lambda b: None if b is None else b.ptr
+    st = m.mrr_gating_topk_run(xb.ptr, CODE[dt], T, e, k, P(bb), P(ib), P(tb),
+                               0 if tid2eid is None else len(tid2eid), P(eb), P(mb), args["k_group"],
+                               args["group_count"], args["routed_scaling_factor"], args["eps"],
+                               args["group_select_mode"], args["renorm"], args["norm_type"], y.ptr,
+                               idx.ptr, P(out), ws.ptr, ws.n, s)
+    assert st == expect, m.mrr_status_str(st)
+    if st != m.MRR_OK:
+        return None
+    res = {"status": m.mrr_v2_read_status(ws.ptr, ws.n, s)}
+    torch.cuda.synchronize()
+    if T == 0:
+        res["guards"] = all(b.guards_intact() for b in (y, idx, out) if b is not None)
+        return res
+    yh = y.host()
+    res["y_out"] = (torch.from_numpy(yh.copy()).view(getattr(torch, dt)).float().numpy().reshape(T, k))
+    res["expert_idx"] = idx.host().view(np.int32).reshape(T, k)
+    res["norm_out"] = None if out is None else out.host().view(np.float32).reshape(T, e)
+    res["guards"] = all(b.guards_intact() for b in (y, idx, out) if b is not None)
+    return res
+
+
+def check_against_oracle(gpu, ref, dt, max_tie_rows=0.02):
+    assert gpu["status"] == m.MRR_OK
+    assert gpu["guards"]
+    T, k = ref["expert_idx"].shape
+    s = ref["norm_out"].astype(np.float64)
+    tie_rows = 0
+    for t in range(T):
+        gi, ri = gpu["expert_idx"][t], ref["expert_idx"][t]
+        if np.array_equal(gi, ri):
+            assert np.allclose(gpu["y_out"][t], ref["y_out"][t], rtol=RTOL[dt], atol=1e-6), t
+            continue
+        # a near-tie: the GPU's experts must be a valid choice under the oracle's scores
+        tie_rows += 1
+        assert len(set(gi.tolist())) == k and gi.min() >= 0 and gi.max() < s.shape[1], t
+        margin = 8 * np.finfo(np.float32).eps * max(1.0, np.abs(s[t]).max())
+        assert np.allclose(np.sort(s[t, gi]), np.sort(s[t, ri]), atol=margin), t
+    assert tie_rows <= max(1, int(max_tie_rows * T)), f"{tie_rows} of {T} rows differ"
+    if gpu["norm_out"] is not None:
+        assert np.allclose(gpu["norm_out"], ref["norm_out"], rtol=2e-5, atol=1e-6)
+
+
+def test_page_example_384_experts_top6():
+    """The page's basic case: 16 tokens, 384 experts, top-6, sigmoid, float16, no groups."""
+    rng = np.random.default_rng(1)
+    x = as_dtype(rng.standard_normal((16, 384)), "float16")
+    ref = gating.gating_topk(x, 6, norm_type=1, eps=1e-6)
+    check_against_oracle(run_gpu_gating(x, "float16", 6, norm_type=1, eps=1e-6), ref, "float16")
+
+
+@pytest.mark.parametrize("dt", ["float16", "bfloat16", "float32"])
+@pytest.mark.parametrize("norm_type", [0, 1, 2])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_grouped_with_bias(dt, norm_type, mode):
+    """Grouped ranking (256 experts, 8 groups, keep 4, top-8) with a bias, all norms and dtypes."""
+    rng = np.random.default_rng(10 * norm_type + mode)
+    T, e = 512, 256
+    x = as_dtype(rng.standard_normal((T, e)) * 2, dt)
+    bias = as_dtype(rng.standard_normal(e) * 0.05, dt)
+    kw = dict(k_group=4, group_count=8, group_select_mode=mode, norm_type=norm_type,
+              routed_scaling_factor=2.5, eps=1e-20)
+    ref = gating.gating_topk(x, 8, bias=bias, **kw)
+    check_against_oracle(run_gpu_gating(x, dt, 8, bias=bias, **kw), ref, dt)
+
+
+@pytest.mark.parametrize("norm_type", [0, 1, 2])
+def test_additional_bias_rows(norm_type):
+    """The page's additional_bias case: every other token uses additional_bias instead of bias."""
+    rng = np.random.default_rng(20 + norm_type)
+    T, e = 64, 384
+    x = as_dtype(rng.standard_normal((T, e)), "float16")
+    bias = as_dtype(rng.random(e), "float16")
+    extra = as_dtype(rng.random(e), "float16")
+    mask = np.zeros(T, bool)
+    mask[::2] = True
+    ref = gating.gating_topk(x, 6, bias=bias, additional_bias=extra, additional_token_mask=mask,
+                             norm_type=norm_type, eps=1e-6)
+    gpu = run_gpu_gating(x, "float16", 6, bias=bias, extra_bias=extra, mask=mask, norm_type=norm_type, eps=1e-6)
+    check_against_oracle(gpu, ref, "float16")
+
+
+@pytest.mark.parametrize("dt", ["float16", "bfloat16", "float32"])
+def test_hash_routing(dt):
+    """The page's hash case: 100-entry vocabulary, tid2eid [100, k]."""
+    rng = np.random.default_rng(30)
+    T, e, k, n = 128, 384, 6, 100
+    x = as_dtype(rng.standard_normal((T, e)), dt)
+    ids = rng.integers(0, n, size=T)
+    tab = rng.integers(0, e, size=(n, k)).astype(np.int32)
+    ref = gating.gating_topk(x, k, input_ids=ids, tid2eid=tab, norm_type=1, eps=1e-6)
+    gpu = run_gpu_gating(x, dt, k, input_ids=ids, tid2eid=tab, norm_type=1, eps=1e-6)
+    assert np.array_equal(gpu["expert_idx"], ref["expert_idx"])
+    check_against_oracle(gpu, ref, dt, max_tie_rows=0)
+
+
+def test_hash_index_out_of_range_is_reported():
+    rng = np.random.default_rng(31)
+    x = as_dtype(rng.standard_normal((8, 64)), "float32")
+    ids = np.array([0, 1, 2, 5, 0, 1, 2, 3])                 # 5 is outside a 4-entry table
+    tab = rng.integers(0, 64, size=(4, 4)).astype(np.int32)
+    tab[2, 1] = 64                                           # an expert id outside [0, e)
+    gpu = run_gpu_gating(x, "float32", 4, input_ids=ids, tid2eid=tab, norm_type=1)
+    assert gpu["status"] == m.MRR_ERR_INDEX
+    assert gpu["guards"]
+
+
+@pytest.mark.parametrize("T,e,k,G,kg", [(3, 1024, 64, 1, 1), (257, 33, 5, 1, 1), (40, 1024, 16, 32, 8),
+                                        (100, 64, 64, 1, 1), (16384, 256, 8, 8, 4), (5, 2, 2, 2, 2)])
+def test_shapes(T, e, k, G, kg):
+    rng = np.random.default_rng(T + e)
+    x = as_dtype(rng.standard_normal((T, e)), "bfloat16")
+    ref = gating.gating_topk(x, k, k_group=kg, group_count=G, norm_type=0, eps=1e-9)
+    gpu = run_gpu_gating(x, "bfloat16", k, k_group=kg, group_count=G, norm_type=0, eps=1e-9,
+                         out_flag=(T * e <= 1 << 20))
+    check_against_oracle(gpu, ref, "bfloat16")
+
+
+def test_no_tokens():
+    gpu = run_gpu_gating(np.zeros((0, 16), np.float32), "float32", 2, norm_type=1)
+    assert gpu["status"] == m.MRR_OK and gpu["guards"]
+
+
+def test_torch_level_call_3d_input():
+    import torch
+
+    rng = np.random.default_rng(40)
+    x = as_dtype(rng.standard_normal((2, 8, 256)), "float32")
+    xt = torch.from_numpy(x).cuda()
+    y, idx, out = m.moe_gating_top_k(xt, 8, k_group=4, group_count=8, group_select_mode=1, norm_type=1,
+                                     out_flag=True, check_status=True)
+    assert tuple(y.shape) == (2, 8, 8) and tuple(idx.shape) == (2, 8, 8) and tuple(out.shape) == (2, 8, 256)
+    ref = gating.gating_topk(x.reshape(16, 256), 8, k_group=4, group_count=8, group_select_mode=1, norm_type=1)
+    check_against_oracle({"status": m.MRR_OK, "guards": True, "y_out": y.reshape(16, 8).cpu().numpy(),
+                          "expert_idx": idx.reshape(16, 8).cpu().numpy(),
+                          "norm_out": out.reshape(16, 256).cpu().numpy()}, ref, "float32")
