@@ -45,8 +45,9 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", type=int, default=2, help="workload 1..5 (2 is the headline)")
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--op", choices=["route", "unroute"], default="route",
-                    help="route: rank-major -> expert-major (the op); unroute: the inverse move")
+    ap.add_argument("--op", choices=["route", "unroute", "gating"], default="route",
+                    help="route: rank-major -> expert-major (the op); unroute: the inverse move; "
+                         "gating: the upstream gating top-k op (--config 1 or 2)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU oracle baseline budget (seconds of oracle work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -524,10 +525,206 @@ def run_e2e(args, p, sets, launch, dev, bytes_step, world, dist):
             "how": "pinned host buffers; upload, run and read-back on three streams, two device sets"}
 
 
+# ----------------------------------------------------------------------------- gating top-k
+
+GATING_METRIC = "effective HBM GB/s (read+write) and tokens/sec of MoE gating top-k"
+
+
+def gating_bytes(w) -> int:
+    """x read once, bias read, y (x's dtype) and int32 expert_idx written."""
+    T, e = w["x"].shape
+    xb = 4 if w["dtype"] == "float32" else 2
+    return T * e * xb + (0 if w["bias"] is None else e * xb) + T * w["k"] * (xb + 4)
+
+
+def gating_oracle_rows(w, rows: int):
+    from oracle import gating
+
+    return gating.gating_topk(w["x"][:rows], w["k"], bias=w["bias"], k_group=w["k_group"],
+                              group_count=w["group_count"], group_select_mode=w["group_select_mode"],
+                              norm_type=w["norm_type"], routed_scaling_factor=w["routed_scaling_factor"],
+                              eps=w["eps"])
+
+
+def gating_config_dict(w, k, extra=None):
+    T, e = w["x"].shape
+    d = {"workload": w["name"], "op": "gating", "T": T, "e": e, "k": w["k"], "dtype": w["dtype"],
+         "group_count": w["group_count"], "k_group": w["k_group"], "norm_type": w["norm_type"],
+         "group_select_mode": w["group_select_mode"], "bias": w["bias"] is not None,
+         "bytes_per_step": gating_bytes(w)}
+    d.update(extra or {})
+    return d
+
+
+def time_gating_oracle(w, budget_s: float, rows: int = 256):
+    gating_oracle_rows(w, 8)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        gating_oracle_rows(w, rows)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    T = w["x"].shape[0]
+    return gating_bytes(w) * rows / T * reps / el / 1e9, rows * reps / el, reps, el
+
+
+def run_gating_reference(args, w):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    rows = 64
+    for _ in range(args.warmup):
+        gating_oracle_rows(w, rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        gating_oracle_rows(w, rows)
+    el = time.perf_counter() - t0
+    T = w["x"].shape[0]
+    value = gating_bytes(w) * rows / T * args.steps / el / 1e9
+    sample = f"first {rows} of {T} token rows per step"
+    print(json.dumps({
+        "impl": "reference", "metric": GATING_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": gating_config_dict(w, args.config, {"sample_rows": rows}),
+        "tokens_per_s": rows * args.steps / el,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
+    return 0
+
+
+def run_gating(args):
+    import numpy as np
+    import torch
+    import workloads
+    from moe_expert_token_gb300 import build as mbuild
+    import moe_expert_token_gb300.mrr_v2 as m
+
+    w = workloads.gating_config(args.config)
+    if args.impl == "reference":
+        return run_gating_reference(args, w)
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0:
+        mbuild.build()
+    if dist is not None:
+        dist.barrier()
+    m.load_library()
+    tdt = getattr(torch, w["dtype"])
+    code = {"float16": m.MRR_GATE_F16, "bfloat16": m.MRR_GATE_BF16, "float32": m.MRR_GATE_F32}[w["dtype"]]
+    T, e = w["x"].shape
+    k = w["k"]
+    B = gating_bytes(w)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    R = max(2, -(-4 * l2 // B))
+    x_host = torch.from_numpy(w["x"]).to(tdt)
+    bias = None if w["bias"] is None else torch.from_numpy(w["bias"]).to(tdt).to(dev)
+    sets = [dict(x=x_host.to(dev), y=torch.empty(T, k, dtype=tdt, device=dev),
+                 idx=torch.empty(T, k, dtype=torch.int32, device=dev)) for _ in range(R)]
+    ws = torch.empty(4096, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def launch(s, st):
+        r = m.mrr_gating_topk_run(s["x"].data_ptr(), code, T, e, k, None if bias is None else bias.data_ptr(),
+                                  None, None, 0, None, None, w["k_group"], w["group_count"],
+                                  w["routed_scaling_factor"], w["eps"], w["group_select_mode"], 0,
+                                  w["norm_type"], s["y"].data_ptr(), s["idx"].data_ptr(), None,
+                                  ws.data_ptr(), ws.numel(), st.cuda_stream)
+        if r != m.MRR_OK:
+            raise RuntimeError(m.mrr_status_str(r))
+
+    for s in sets:
+        launch(s, stream)
+    if m.mrr_v2_read_status(ws.data_ptr(), ws.numel(), stream.cuda_stream) != m.MRR_OK:
+        raise RuntimeError("gating reported a device error")
+    for i in range(args.warmup):
+        launch(sets[i % R], stream)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    K = args.steps
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.t_start = time.time()
+    a.record(stream)
+    for i in range(K):
+        launch(sets[i % R], stream)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.t_end = time.time()
+    time.sleep(0.2)
+    clocks.stop()
+    local_ms = a.elapsed_time(b)
+    ms = max_over_ranks(local_ms, dist, dev)
+    value = throughput_gbs(world, B, K, ms)
+    peak, peak_kind = measured_peak()
+    achieved = B / (local_ms / K * 1e-3) / 1e9
+
+    # end to end: x uploaded from pinned host memory, y and expert_idx read back, every step
+    x_pin = x_host.view(torch.uint8).reshape(-1).pin_memory()
+    y_pin = torch.empty(T * k * sets[0]["y"].element_size(), dtype=torch.uint8).pin_memory()
+    i_pin = torch.empty(T * k * 4, dtype=torch.uint8).pin_memory()
+    s0 = sets[0]
+
+    def e2e_step():
+        s0["x"].view(torch.uint8).reshape(-1).copy_(x_pin, non_blocking=True)
+        launch(s0, stream)
+        y_pin.copy_(s0["y"].view(torch.uint8).reshape(-1), non_blocking=True)
+        i_pin.copy_(s0["idx"].view(torch.uint8).reshape(-1), non_blocking=True)
+
+    e2e = None
+    if not args.no_e2e:
+        KE = max(3, min(K, 200))
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for _ in range(KE):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ems = max_over_ranks(a.elapsed_time(b), dist, dev)
+        e2e = {"value": throughput_gbs(world, B, KE, ems), "unit": "GB/s", "h2d_bytes_per_step": x_pin.numel(),
+               "d2h_bytes_per_step": y_pin.numel() + i_pin.numel(), "steps": KE, "ms_per_step": ems / KE}
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, tok_s, reps, el = time_gating_oracle(w, min(args.cpu_seconds, 10.0))
+        cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"the first 256 token rows, {reps} runs in {el:.1f} s, single thread",
+               "tokens_per_s": tok_s}
+    if rank == 0:
+        print(json.dumps({
+            "metric": GATING_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded numpy draws shaped like the page's cases)",
+            "config": gating_config_dict(w, args.config, {
+                "l2": f"{R} rotating buffer sets, {R * B / 1e6:.0f} MB > 4x L2 ({l2 / 1e6:.0f} MB)"}),
+            "pct_of_peak": 100.0 * value / world / peak, "tokens_per_s": world * T * K / (ms * 1e-3),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_kind, "traffic": None,
+                         "kernel": "mrr_gate::gating_kernel", "bytes_per_launch": B,
+                         "mean_launch_us": local_ms / K * 1e3},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K, "clocks": clocks.summary()}), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
+    if args.op == "gating":
+        return run_gating(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

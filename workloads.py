@@ -226,3 +226,37 @@ def config(k: int, idx_type: Optional[int] = None) -> Problem:
     if idx_type is not None:
         p.idx_type = idx_type
     return p
+
+
+# ----------------------------------------------------------------------------- gating top-k inputs
+# Source for the shapes: "CANN 自定义算子详解：npu_moe_gating_top_k" (m.qwbw.cn/news/316089),
+# section 调用示例: x ~ randn(batch, 384) float16, top-6, sigmoid; bias / additional_bias ~ rand(e).
+
+GATING_NAMES = {
+    1: "gating: T=16384 tokens x 384 experts fp16, top-6, sigmoid, no groups",
+    2: "gating: T=16384 tokens x 256 experts bf16, 8 groups keep 4, top-8, sigmoid + bias, top-2 group scores",
+}
+
+
+def gating_config(k: int) -> dict:
+    """Gating workload k (1, 2), drawn with numpy default_rng(2000 + k).  x and bias are float32
+    arrays holding values already rounded to the workload's dtype."""
+    import torch
+
+    rng = np.random.default_rng(2000 + k)
+
+    def rounded(a, dt):
+        return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dt).to(torch.float32).numpy()
+
+    if k == 1:
+        T, e = 16384, 384
+        x = rounded(rng.standard_normal((T, e)), torch.float16)
+        return dict(name=GATING_NAMES[1], dtype="float16", x=x, k=6, bias=None, k_group=1, group_count=1,
+                    group_select_mode=0, norm_type=1, routed_scaling_factor=1.0, eps=1e-6)
+    if k == 2:
+        T, e = 16384, 256
+        x = rounded(rng.standard_normal((T, e)), torch.bfloat16)
+        bias = rounded(rng.random(e) * 0.1, torch.bfloat16)
+        return dict(name=GATING_NAMES[2], dtype="bfloat16", x=x, k=8, bias=bias, k_group=4, group_count=8,
+                    group_select_mode=1, norm_type=1, routed_scaling_factor=2.5, eps=1e-20)
+    raise ValueError(f"no gating workload {k}")
