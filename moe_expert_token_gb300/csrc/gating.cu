@@ -6,11 +6,18 @@
 // k best experts inside the k_group best groups (or a table lookup for hash routing), and the
 // chosen scores scaled to sum to routed_scaling_factor.
 //
-// GB300 design: the op reads T*e scores once and writes T*k results, so it is bound by memory
-// and latency, not arithmetic.  One warp owns one row: lane l holds experts l, l+32, ... in
-// registers (coalesced loads of the row), the scores are also staged in shared memory for the
-// group statistics and table lookups, and every selection is a warp-wide arg-max by shuffles
-// (ties to the lower index).  A grid of a few CTAs per SM strides over the rows.
+// GB300 design.  The op reads T*e scores once and writes T*k results; its k picks per row make it
+// bound by instruction issue long before HBM, so the kernel is built to spend few warp
+// instructions per row:
+//  * one warp owns one row; lane l holds the contiguous run of experts [l*VPL, (l+1)*VPL) in
+//    registers, read with 16-, 8- or 4-byte loads where the row alignment allows;
+//  * scores become order-preserving 32-bit keys, so an arg-max over the row is two redux.sync
+//    instructions (the largest key, then the lowest expert index among the lanes holding it);
+//  * each lane caches its two best remaining candidates and rescans its run only when both are
+//    used, so a pick costs a handful of instructions instead of a pass over the row;
+//  * group scores come from a shuffle butterfly when each group is an aligned block of lanes,
+//    else from the row staged in shared memory;
+//  * 8 warps per CTA, shared memory sized to the call, as many CTAs as fit on the SMs.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -23,30 +30,52 @@
 
 namespace mrr_gate {
 
-constexpr int kWarps = 4;                       // rows per CTA per iteration
+constexpr int kWarps = 8;                       // rows in flight per CTA
+constexpr int kThreads = 32 * kWarps;
 constexpr int kStatusWords = 1024;              // the status region shared with mrr_v2_read_status
 constexpr int kMaxGrid = kStatusWords - 2;
 constexpr uint32_t kFlagBadIndex = 8u;          // an input_ids / tid2eid value out of range
-constexpr int kMaxExperts = MRR_GATE_MAX_EXPERTS;
+constexpr uint32_t kFull = 0xffffffffu;
+constexpr uint32_t kNoIndex = 0xffffffffu;
+constexpr int kSmemOptIn = 100 * 1024;          // the largest call needs 78,848 bytes
+
+enum GroupPath { kNoGroups = 0, kLaneGroups = 1, kSmemGroups = 2 };
 
 struct Params {
     const void *x;
-    int dt;
-    int T, e, k;
+    int dt, T, e, k;
+    int vec_bytes;            // widest row load (16, 8, 4; 0 = one element at a time) x allows
     const void *bias;
     const long long *input_ids;
     const int *tid2eid;
     long long n_vocab;
     const void *extra_bias;
     const uint8_t *extra_mask;
-    int k_group, group_count, group_size;
+    int k_group, group_count, group_size, group_path, lanes_per_group, lpg_shift;
     float rsf, eps;
     int select_mode, norm_type;
+    int out_vec;              // norm_out rows may be written with 16-byte stores
+    // dynamic shared memory, offsets in 4-byte words (-1 = not allocated)
+    int sm_bias, sm_extra, sm_rows, sm_gkey, sm_kept;
     void *y_out;
     int *expert_idx;
     float *norm_out;
     uint32_t *status;
 };
+
+// Order-preserving map of a float score to a 32-bit key: a larger float gives a larger key, equal
+// floats equal keys (-0 is folded into +0 first).  Every score, -inf included, maps above 0, which
+// therefore marks "no candidate".
+__device__ __forceinline__ uint32_t order_key(float f)
+{
+    const uint32_t b = __float_as_uint(f + 0.0f);
+    return b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u);   // negative: all bits flip
+}
+
+__device__ __forceinline__ float key_value(uint32_t key)
+{
+    return __uint_as_float(key ^ ((uint32_t)((int32_t)~key >> 31) | 0x80000000u));
+}
 
 __device__ __forceinline__ float load_as_float(const void *p, int dt, long long i)
 {
@@ -55,6 +84,14 @@ __device__ __forceinline__ float load_as_float(const void *p, int dt, long long 
     if (dt == MRR_GATE_BF16)
         return __bfloat162float(__ldg(static_cast<const __nv_bfloat16 *>(p) + i));
     return __half2float(__ldg(static_cast<const __half *>(p) + i));
+}
+
+template <int DT>
+__device__ __forceinline__ float bits16_to_float(uint32_t h)
+{
+    if (DT == MRR_GATE_BF16)
+        return __uint_as_float(h << 16);
+    return __half2float(__ushort_as_half((unsigned short)(h & 0xffffu)));
 }
 
 __device__ __forceinline__ void store_from_float(void *p, int dt, long long i, float v)
@@ -67,108 +104,239 @@ __device__ __forceinline__ void store_from_float(void *p, int dt, long long i, f
         static_cast<__half *>(p)[i] = __float2half_rn(v);
 }
 
-// warp-wide arg-max: the larger value wins, equal values go to the lower index
-__device__ __forceinline__ void warp_argmax(float &v, int &j)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-        const int oj = __shfl_xor_sync(0xffffffffu, j, o);
-        if (ov > v || (ov == v && oj < j)) {
-            v = ov;
-            j = oj;
-        }
-    }
-}
-
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
-        v += __shfl_xor_sync(0xffffffffu, v, o);
+        v += __shfl_xor_sync(kFull, v, o);
     return v;
 }
 
-__device__ __forceinline__ float warp_max(float v)
+// this lane's run of row `row`, experts [j0, j0 + VPL), as floats; experts at or past e read -inf
+template <int VPL, int DT>
+__device__ __forceinline__ void load_run(float (&v)[VPL], const Params &p, long long row, int j0)
 {
+    const int nv = p.e - j0;
+    if (DT == MRR_GATE_F32) {
+        const float *src = static_cast<const float *>(p.x) + row * p.e + j0;
+        if (VPL % 4 == 0 && nv >= VPL && p.vec_bytes >= 16) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
+            for (int c = 0; c < VPL / 4; ++c) {
+                const float4 q = __ldg(reinterpret_cast<const float4 *>(src) + c);
+                v[4 * c] = q.x;
+                v[4 * c + 1] = q.y;
+                v[4 * c + 2] = q.z;
+                v[4 * c + 3] = q.w;
+            }
+        } else if (VPL % 2 == 0 && nv >= VPL && p.vec_bytes >= 8) {
+#pragma unroll
+            for (int c = 0; c < VPL / 2; ++c) {
+                const float2 q = __ldg(reinterpret_cast<const float2 *>(src) + c);
+                v[2 * c] = q.x;
+                v[2 * c + 1] = q.y;
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < VPL; ++u)
+                v[u] = u < nv ? __ldg(src + u) : -INFINITY;
+        }
+        return;
+    }
+    const unsigned short *src = static_cast<const unsigned short *>(p.x) + row * p.e + j0;
+    if (VPL % 8 == 0 && nv >= VPL && p.vec_bytes >= 16) {
+#pragma unroll
+        for (int c = 0; c < VPL / 8; ++c) {
+            const uint4 q = __ldg(reinterpret_cast<const uint4 *>(src) + c);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int h = 0; h < 8; ++h)
+                v[8 * c + h] = bits16_to_float<DT>(w[h >> 1] >> (16 * (h & 1)));
+        }
+    } else if (VPL % 4 == 0 && nv >= VPL && p.vec_bytes >= 8) {
+#pragma unroll
+        for (int c = 0; c < VPL / 4; ++c) {
+            const uint2 q = __ldg(reinterpret_cast<const uint2 *>(src) + c);
+            const uint32_t w[2] = {q.x, q.y};
+#pragma unroll
+            for (int h = 0; h < 4; ++h)
+                v[4 * c + h] = bits16_to_float<DT>(w[h >> 1] >> (16 * (h & 1)));
+        }
+    } else if (VPL % 2 == 0 && nv >= VPL && p.vec_bytes >= 4) {
+#pragma unroll
+        for (int c = 0; c < VPL / 2; ++c) {
+            const uint32_t q = __ldg(reinterpret_cast<const unsigned int *>(src) + c);
+            v[2 * c] = bits16_to_float<DT>(q);
+            v[2 * c + 1] = bits16_to_float<DT>(q >> 16);
+        }
+    } else {
+#pragma unroll
+        for (int u = 0; u < VPL; ++u)
+            v[u] = u < nv ? bits16_to_float<DT>(__ldg(src + u)) : -INFINITY;
+    }
 }
 
-// VPL = values per lane: the row's e <= 32 * VPL experts live in registers, lane l holding
-// experts l + 32 v.
+// steps 1-2 of the page for this lane's run: normalise, then add the row's bias (from shared memory)
 template <int VPL>
-__global__ void __launch_bounds__(32 * kWarps) gating_kernel(const Params p)
+__device__ __forceinline__ void normalise_and_bias(float (&v)[VPL], int norm_type, int nv, const float *bias)
 {
-    extern __shared__ float smem[];
+    if (norm_type == 0) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < VPL; ++u)
+            mx = fmaxf(mx, v[u]);
+        mx = key_value(__reduce_max_sync(kFull, order_key(mx)));
+        float sum = 0.f;
+#pragma unroll
+        for (int u = 0; u < VPL; ++u) {
+            v[u] = expf(v[u] - mx);      // experts past e: exp(-inf) = 0
+            sum += v[u];
+        }
+        const float r = __frcp_rn(warp_sum(sum));
+#pragma unroll
+        for (int u = 0; u < VPL; ++u)
+            v[u] *= r;
+    } else if (norm_type == 1) {
+#pragma unroll
+        for (int u = 0; u < VPL; ++u)
+            v[u] = __frcp_rn(1.f + expf(-v[u]));
+    } else {
+#pragma unroll
+        for (int u = 0; u < VPL; ++u)
+            v[u] = v[u] > 20.f ? v[u] + log1pf(expf(-v[u])) : log1pf(expf(v[u]));
+    }
+    if (bias == nullptr)
+        return;
+    if (VPL % 4 == 0 && nv >= VPL) {
+#pragma unroll
+        for (int c = 0; c < VPL / 4; ++c) {
+            const float4 b = reinterpret_cast<const float4 *>(bias)[c];
+            v[4 * c] += b.x;
+            v[4 * c + 1] += b.y;
+            v[4 * c + 2] += b.z;
+            v[4 * c + 3] += b.w;
+        }
+    } else {
+#pragma unroll
+        for (int u = 0; u < VPL; ++u)
+            if (u < nv)
+                v[u] += bias[u];
+    }
+}
+
+// A lane's view of its run during the picks: the two best remaining keys (b1 >= b2, with their
+// slots), whether those two are all that remain, and the last key the lane gave up.  Keys leave
+// a lane in (key descending, slot ascending) order, so "remaining" means: below the last key
+// given up, or equal to it at a later slot.
+struct LaneCands {
+    uint32_t b1, b2, last_key;
+    int u1, u2, last_u;
+    bool complete;
+};
+
+// the lane's two best keys before any pick (equal keys: the earlier slot first)
+template <int VPL>
+__device__ __forceinline__ void first_scan(LaneCands &c, const uint32_t (&kv)[VPL])
+{
+    c.b1 = kv[0];
+    c.u1 = 0;
+    c.b2 = 0u;
+    c.u2 = 0;
+#pragma unroll
+    for (int u = 1; u < VPL; ++u) {
+        const uint32_t key = kv[u];
+        const bool over1 = key > c.b1, over2 = key > c.b2;
+        c.b2 = over1 ? c.b1 : (over2 ? key : c.b2);
+        c.u2 = over1 ? c.u1 : (over2 ? u : c.u2);
+        c.b1 = over1 ? key : c.b1;
+        c.u1 = over1 ? u : c.u1;
+    }
+    c.complete = c.b2 == 0u;
+    c.last_key = 0xffffffffu;
+    c.last_u = -1;
+}
+
+// the lane's two best remaining keys after some picks
+template <int VPL>
+__device__ __forceinline__ void rescan(LaneCands &c, const uint32_t (&kv)[VPL])
+{
+    c.b1 = c.b2 = 0u;
+    c.u1 = c.u2 = 0;
+#pragma unroll
+    for (int u = 0; u < VPL; ++u) {
+        uint32_t key = kv[u];
+        const bool live = key < c.last_key || (key == c.last_key && u > c.last_u);
+        key = live ? key : 0u;
+        const bool over1 = key > c.b1, over2 = key > c.b2;
+        c.b2 = over1 ? c.b1 : (over2 ? key : c.b2);
+        c.u2 = over1 ? c.u1 : (over2 ? u : c.u2);
+        c.b1 = over1 ? key : c.b1;
+        c.u1 = over1 ? u : c.u1;
+    }
+    c.complete = c.b2 == 0u;
+}
+
+// CTAs per SM each width is compiled for (its register budget: 48, 64 or 80 per thread)
+constexpr int min_ctas_per_sm(int vpl) { return vpl <= 8 ? 5 : (vpl <= 16 ? 4 : 3); }
+
+// VPL = experts per lane (the row's e <= 32 * VPL scores live in registers); DT = x's type.
+template <int VPL, int DT>
+__global__ void __launch_bounds__(kThreads, min_ctas_per_sm(VPL)) gating_kernel(const Params p)
+{
+    extern __shared__ __align__(16) float smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = p.e, k = p.k, G = p.group_count, gs = p.group_size;
-    float *s_score = smem + warp * (2 * kMaxExperts + 32);    // [e] scores of this warp's row
-    float *s_group = s_score + kMaxExperts;                    // [G] group scores
-    uint32_t *s_kept = reinterpret_cast<uint32_t *>(s_group + kMaxExperts);  // [32] kept-group bits
+    const int e = p.e, k = p.k, j0 = lane * VPL, nv = e - j0;
 
     // no global memory touched above: wait for the previous kernel on the stream, then let the
     // next launch be scheduled (programmatic stream serialization)
     mrr::grid_dependency_wait();
     mrr::grid_launch_dependents();
-    uint32_t flags = 0u;
-    const int rows_per_iter = gridDim.x * kWarps;
-    for (int t = blockIdx.x * kWarps + warp; t < p.T; t += rows_per_iter) {
-        // ---- steps 1-2: normalise, add the row's bias
-        float v[VPL];
-#pragma unroll
-        for (int u = 0; u < VPL; ++u) {
-            const int j = lane + 32 * u;
-            v[u] = j < e ? load_as_float(p.x, p.dt, (long long)t * e + j) : -INFINITY;
-        }
-        if (p.norm_type == 0) {
-            float mx = -INFINITY;
-#pragma unroll
-            for (int u = 0; u < VPL; ++u)
-                mx = fmaxf(mx, v[u]);
-            mx = warp_max(mx);
-            float sum = 0.f;
-#pragma unroll
-            for (int u = 0; u < VPL; ++u) {
-                v[u] = (lane + 32 * u < e) ? expf(v[u] - mx) : 0.f;
-                sum += v[u];
-            }
-            sum = warp_sum(sum);
-#pragma unroll
-            for (int u = 0; u < VPL; ++u)
-                v[u] = v[u] / sum;
-        } else if (p.norm_type == 1) {
-#pragma unroll
-            for (int u = 0; u < VPL; ++u)
-                v[u] = 1.f / (1.f + expf(-v[u]));
-        } else {
-#pragma unroll
-            for (int u = 0; u < VPL; ++u)
-                v[u] = v[u] > 20.f ? v[u] + log1pf(expf(-v[u])) : log1pf(expf(v[u]));
-        }
-        const bool extra = p.extra_bias && p.extra_mask && p.extra_mask[t];
-        const void *bsrc = extra ? p.extra_bias : p.bias;
-#pragma unroll
-        for (int u = 0; u < VPL; ++u) {
-            const int j = lane + 32 * u;
-            if (j < e) {
-                if (bsrc)
-                    v[u] = v[u] + load_as_float(bsrc, p.dt, j);
-                s_score[j] = v[u];
-                if (p.norm_out)
-                    p.norm_out[(long long)t * e + j] = v[u];
-            } else {
-                v[u] = -INFINITY;
-            }
-        }
-        __syncwarp();
 
-        // ---- step 3: choose the experts; lane i (and i + 32) keeps result i (k <= 64)
+    // the bias rows, once per CTA, as float
+    if (p.sm_bias >= 0)
+        for (int j = threadIdx.x; j < e; j += kThreads)
+            smem[p.sm_bias + j] = load_as_float(p.bias, DT, j);
+    if (p.sm_extra >= 0)
+        for (int j = threadIdx.x; j < e; j += kThreads)
+            smem[p.sm_extra + j] = load_as_float(p.extra_bias, DT, j);
+    __syncthreads();
+    float *s_row = p.sm_rows >= 0 ? smem + p.sm_rows + warp * e : nullptr;
+    uint32_t *s_gkey = p.sm_gkey >= 0 ? reinterpret_cast<uint32_t *>(smem) + p.sm_gkey + warp * p.group_count
+                                      : nullptr;
+    uint32_t *s_kept = p.sm_kept >= 0 ? reinterpret_cast<uint32_t *>(smem) + p.sm_kept + warp * 32 : nullptr;
+
+    uint32_t flags = 0u;
+    for (int t = blockIdx.x * kWarps + warp; t < p.T; t += gridDim.x * kWarps) {
+        // ---- steps 1-2
+        float v[VPL];
+        load_run<VPL, DT>(v, p, t, j0);
+        const bool extra = p.sm_extra >= 0 && p.extra_mask[t];
+        const float *bias = extra ? smem + p.sm_extra + j0 : (p.sm_bias >= 0 ? smem + p.sm_bias + j0 : nullptr);
+        normalise_and_bias<VPL>(v, p.norm_type, nv, bias);
+        if (p.norm_out) {
+            float *dst = p.norm_out + (long long)t * e + j0;
+            if (VPL % 4 == 0 && nv >= VPL && p.out_vec) {
+#pragma unroll
+                for (int c = 0; c < VPL / 4; ++c)
+                    reinterpret_cast<float4 *>(dst)[c] =
+                        make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+            } else {
+#pragma unroll
+                for (int u = 0; u < VPL; ++u)
+                    if (u < nv)
+                        dst[u] = v[u];
+            }
+        }
+
+        // ---- step 3: lane i keeps pick i in (y0, i0) and pick i + 32 in (y1, i1)
         float y0 = 0.f, y1 = 0.f;
-        int j0 = 0, j1 = 0;
+        uint32_t i0 = 0u, i1 = 0u;
         if (p.input_ids) {
+            // hash routing: the table row, scores looked up in the staged row
+#pragma unroll
+            for (int u = 0; u < VPL; ++u)
+                if (u < nv)
+                    s_row[j0 + u] = v[u];
+            __syncwarp();
             const long long id = p.input_ids[t];
             const bool ok = id >= 0 && id < p.n_vocab;
             for (int i = lane; i < k; i += 32) {
@@ -177,96 +345,151 @@ __global__ void __launch_bounds__(32 * kWarps) gating_kernel(const Params p)
                     flags |= kFlagBadIndex;
                     j = 0;
                 }
-                const float y = s_score[j];
                 if (i < 32) {
-                    y0 = y;
-                    j0 = j;
+                    y0 = s_row[j];
+                    i0 = (uint32_t)j;
                 } else {
-                    y1 = y;
-                    j1 = j;
+                    y1 = s_row[j];
+                    i1 = (uint32_t)j;
                 }
             }
-        } else {
-            // group scores: maximum, or sum of the two largest (in float32)
-            for (int g = lane; g < G; g += 32) {
-                float m1 = -INFINITY, m2 = -INFINITY;
-                for (int j = g * gs; j < (g + 1) * gs; ++j) {
-                    const float s = s_score[j];
-                    if (s > m1) {
-                        m2 = m1;
-                        m1 = s;
-                    } else if (s > m2) {
-                        m2 = s;
-                    }
-                }
-                s_group[g] = p.select_mode == 0 ? m1 : m1 + m2;
-            }
-            s_kept[lane] = 0u;
             __syncwarp();
-            for (int r = 0; r < p.k_group; ++r) {
-                float bv = -INFINITY;
-                int bg = 0x7fffffff;
-                for (int g = lane; g < G; g += 32) {
-                    const bool kept = (s_kept[g >> 5] >> (g & 31)) & 1u;
-                    const float s = s_group[g];
-                    if (!kept && (s > bv || (s == bv && g < bg))) {
-                        bv = s;
-                        bg = g;
-                    }
-                }
-                warp_argmax(bv, bg);
-                if (lane == 0)
-                    s_kept[bg >> 5] |= 1u << (bg & 31);
-                __syncwarp();
-            }
-            // the k largest scores among the kept groups' experts, in descending order
-            uint32_t taken = 0u;  // bit u: this lane's expert lane + 32u is chosen or excluded
+        } else {
+            uint32_t kv[VPL];
 #pragma unroll
-            for (int u = 0; u < VPL; ++u) {
-                const int j = lane + 32 * u;
-                if (j >= e || !((s_kept[(j / gs) >> 5] >> ((j / gs) & 31)) & 1u))
-                    taken |= 1u << u;
+            for (int u = 0; u < VPL; ++u)
+                kv[u] = order_key(v[u]);
+            if (nv < VPL) {          // experts past e are no candidates
+#pragma unroll
+                for (int u = 0; u < VPL; ++u)
+                    if (u >= nv)
+                        kv[u] = 0u;
             }
-            for (int i = 0; i < k; ++i) {
-                float bv = -INFINITY;
-                int bj = 0x7fffffff;
+
+            if (p.group_path == kLaneGroups) {
+                // each group is an aligned block of lanes_per_group lanes (a power of two)
+                const int lpg = p.lanes_per_group;
+                const int g = lane >> p.lpg_shift;
+                const bool member = g < p.group_count;
+                float m1 = v[0], m2 = -INFINITY;
+#pragma unroll
+                for (int u = 1; u < VPL; ++u) {
+                    m2 = fmaxf(m2, fminf(m1, v[u]));
+                    m1 = fmaxf(m1, v[u]);
+                }
+                for (int o = 1; o < lpg; o <<= 1) {
+                    const float o1 = __shfl_xor_sync(kFull, m1, o), o2 = __shfl_xor_sync(kFull, m2, o);
+                    m2 = fmaxf(fmaxf(m2, o2), fminf(m1, o1));
+                    m1 = fmaxf(m1, o1);
+                }
+                const uint32_t gkey = order_key(p.select_mode == 0 ? m1 : m1 + m2);
+                const bool leader = member && (lane & (lpg - 1)) == 0;
+                bool kept = false;
+                for (int r = 0; r < p.k_group; ++r) {
+                    const bool cand = leader && !kept;
+                    const uint32_t top = __reduce_max_sync(kFull, cand ? gkey : 0u);
+                    const uint32_t win = __reduce_min_sync(kFull, cand && gkey == top ? (uint32_t)g : kNoIndex);
+                    kept = kept || (member && (uint32_t)g == win);
+                }
+                if (!kept) {
+#pragma unroll
+                    for (int u = 0; u < VPL; ++u)
+                        kv[u] = 0u;
+                }
+            } else if (p.group_path == kSmemGroups) {
+                const int G = p.group_count, gs = p.group_size;
+#pragma unroll
+                for (int u = 0; u < VPL; ++u)
+                    if (u < nv)
+                        s_row[j0 + u] = v[u];
+                s_kept[lane] = 0u;
+                __syncwarp();
+                for (int g = lane; g < G; g += 32) {
+                    float m1 = -INFINITY, m2 = -INFINITY;
+                    for (int j = g * gs; j < (g + 1) * gs; ++j) {
+                        const float s = s_row[j];
+                        m2 = fmaxf(m2, fminf(m1, s));
+                        m1 = fmaxf(m1, s);
+                    }
+                    s_gkey[g] = order_key(p.select_mode == 0 ? m1 : m1 + m2);
+                }
+                __syncwarp();
+                for (int r = 0; r < p.k_group; ++r) {
+                    uint32_t best = 0u, bg = kNoIndex;
+                    for (int g = lane; g < G; g += 32) {   // g rises: the first of equal keys stays
+                        const uint32_t key = ((s_kept[g >> 5] >> (g & 31)) & 1u) ? 0u : s_gkey[g];
+                        if (key > best) {
+                            best = key;
+                            bg = (uint32_t)g;
+                        }
+                    }
+                    const uint32_t top = __reduce_max_sync(kFull, best);
+                    const uint32_t win = __reduce_min_sync(kFull, best == top ? bg : kNoIndex);
+                    if (lane == 0 && win < (uint32_t)G)
+                        s_kept[win >> 5] |= 1u << (win & 31);
+                    __syncwarp();
+                }
+                // experts of dropped groups leave the candidates
+                int g = j0 / gs, r = j0 - g * gs;
 #pragma unroll
                 for (int u = 0; u < VPL; ++u) {
-                    if (!((taken >> u) & 1u) && v[u] > bv) {  // lane's experts rise in index
-                        bv = v[u];
-                        bj = lane + 32 * u;
+                    if (u < nv && !((s_kept[g >> 5] >> (g & 31)) & 1u))
+                        kv[u] = 0u;
+                    if (++r == gs) {
+                        r = 0;
+                        ++g;
                     }
                 }
-                warp_argmax(bv, bj);
-                if (bj < e && (bj & 31) == lane)
-                    taken |= 1u << (bj >> 5);
-                if (lane == (i & 31)) {
-                    if (i < 32) {
-                        y0 = bv;
-                        j0 = bj;
-                    } else {
-                        y1 = bv;
-                        j1 = bj;
-                    }
-                }
+                __syncwarp();
             }
+
+            // the k picks: the largest remaining key, ties to the lower expert index
+            LaneCands c;
+            first_scan<VPL>(c, kv);
+            uint32_t k0 = 0u, k1 = 0u;
+            for (int i = 0; i < k; ++i) {
+                const uint32_t top = __reduce_max_sync(kFull, c.b1);
+                const uint32_t mine = (uint32_t)(j0 + c.u1);
+                const bool has_top = c.b1 == top;
+                const uint32_t win = __reduce_min_sync(kFull, has_top ? mine : kNoIndex);
+                if (i < 32) {
+                    k0 = lane == i ? top : k0;
+                    i0 = lane == i ? win : i0;
+                } else {
+                    k1 = lane == i - 32 ? top : k1;
+                    i1 = lane == i - 32 ? win : i1;
+                }
+                bool need = false;
+                if (has_top && mine == win) {   // this lane gave the pick
+                    c.last_key = c.b1;
+                    c.last_u = c.u1;
+                    c.b1 = c.b2;
+                    c.u1 = c.u2;
+                    c.b2 = 0u;
+                    need = !c.complete && c.b1 == 0u;
+                }
+                if (__any_sync(kFull, need) && need)
+                    rescan<VPL>(c, kv);
+            }
+            y0 = key_value(k0);
+            y1 = key_value(k1);
         }
 
         // ---- step 4: scale and write
-        const float ysum = warp_sum((lane < k ? y0 : 0.f) + (lane + 32 < k ? y1 : 0.f));
-        const float scale = p.rsf / (ysum + p.eps);
-        if (lane < k) {
-            store_from_float(p.y_out, p.dt, (long long)t * k + lane, y0 * scale);
-            p.expert_idx[(long long)t * k + lane] = j0;
+        const bool has0 = lane < k, has1 = lane + 32 < k;
+        const float ysum = warp_sum((has0 ? y0 : 0.f) + (has1 ? y1 : 0.f));
+        const float scale = p.rsf * __frcp_rn(ysum + p.eps);
+        if (has0) {
+            store_from_float(p.y_out, DT, (long long)t * k + lane, y0 * scale);
+            p.expert_idx[(long long)t * k + lane] = (int)i0;
         }
-        if (lane + 32 < k) {
-            store_from_float(p.y_out, p.dt, (long long)t * k + lane + 32, y1 * scale);
-            p.expert_idx[(long long)t * k + lane + 32] = j1;
+        if (has1) {
+            store_from_float(p.y_out, DT, (long long)t * k + lane + 32, y1 * scale);
+            p.expert_idx[(long long)t * k + lane + 32] = (int)i1;
         }
-        __syncwarp();
     }
     // per-CTA status word (plain stores: no clearing needed between calls)
-    flags = __reduce_or_sync(0xffffffffu, flags);
+    flags = __reduce_or_sync(kFull, flags);
     __shared__ uint32_t s_flags[kWarps];
     if (lane == 0)
         s_flags[warp] = flags;
@@ -289,15 +512,40 @@ using namespace mrr_gate;
 
 namespace {
 
-template <int VPL>
-cudaError_t launch_gating(const Params &p, int grid, cudaStream_t stream)
+constexpr int kVplChoices[] = {1, 2, 4, 6, 8, 12, 16, 24, 32};
+
+int choose_vpl(int64_t e)
 {
-    // 4 rows x (1024 scores + 1024 group scores + 32 words): 33,280 bytes, under the 48 KiB default
-    const size_t smem = (size_t)kWarps * (2 * kMaxExperts + 32) * sizeof(float);
+    const int64_t need = (e + 31) / 32;
+    for (int v : kVplChoices)
+        if (v >= need)
+            return v;
+    return 32;
+}
+
+template <int VPL, int DT>
+cudaError_t launch_gating_dt(const Params &p, size_t smem, int sms, cudaStream_t stream)
+{
+    if (smem > 48 * 1024) {
+        const cudaError_t err =
+            cudaFuncSetAttribute(gating_kernel<VPL, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOptIn);
+        if (err != cudaSuccess)
+            return err;
+    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gating_kernel<VPL, DT>, kThreads, smem) !=
+            cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    const int64_t want = ((int64_t)p.T + kWarps - 1) / kWarps;
+    int64_t cap = (int64_t)sms * per_sm;
+    if (cap > kMaxGrid)
+        cap = kMaxGrid;
+    const int grid = (int)(want < 1 ? 1 : (want > cap ? cap : want));
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(32 * kWarps);
+    cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -305,7 +553,17 @@ cudaError_t launch_gating(const Params &p, int grid, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gating_kernel<VPL>, p);
+    return cudaLaunchKernelEx(&cfg, gating_kernel<VPL, DT>, p);
+}
+
+template <int VPL>
+cudaError_t launch_gating(const Params &p, size_t smem, int sms, cudaStream_t stream)
+{
+    if (p.dt == MRR_GATE_F32)
+        return launch_gating_dt<VPL, MRR_GATE_F32>(p, smem, sms, stream);
+    if (p.dt == MRR_GATE_BF16)
+        return launch_gating_dt<VPL, MRR_GATE_BF16>(p, smem, sms, stream);
+    return launch_gating_dt<VPL, MRR_GATE_F16>(p, smem, sms, stream);
 }
 
 }  // namespace
@@ -373,25 +631,56 @@ extern "C" mrr_status mrr_gating_topk_run(const void *x, mrr_gate_dtype dt, int6
     p.norm_out = norm_out;
     p.status = static_cast<uint32_t *>(workspace);
 
-    int64_t want = (T + kWarps - 1) / kWarps;
-    int64_t cap = 4 * (int64_t)sms;
-    if (cap > kMaxGrid)
-        cap = kMaxGrid;
-    const int grid = (int)(want < 1 ? 1 : (want > cap ? cap : want));
-    const int vpl_needed = (int)((e + 31) / 32);
+    const int xb = dt == MRR_GATE_F32 ? 4 : 2;
+    const int vpl = choose_vpl(e);
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(x);
+    const int64_t row_bytes = e * xb;
+    p.vec_bytes = 0;
+    for (int w = 16; w >= 4; w >>= 1)
+        if (xa % w == 0 && row_bytes % w == 0) {
+            p.vec_bytes = w;
+            break;
+        }
+    p.out_vec = norm_out && reinterpret_cast<uintptr_t>(norm_out) % 16 == 0 && e % 4 == 0;
+    const int gs = (int)(e / group_count);
+    p.group_path = kNoGroups;
+    p.lanes_per_group = 0;
+    if (!hashing && group_count > 1 && k_group < group_count) {
+        const int lpg = gs / vpl;
+        if (gs % vpl == 0 && (lpg & (lpg - 1)) == 0) {
+            p.group_path = kLaneGroups;
+            p.lanes_per_group = lpg;
+            while ((1 << p.lpg_shift) < lpg)
+                ++p.lpg_shift;
+        } else {
+            p.group_path = kSmemGroups;
+        }
+    }
+    // shared memory: bias rows, then per-warp staging for hash lookups and smem group scores
+    int words = 0;
+    auto take = [&words](int64_t n) {
+        const int off = words;
+        words += (int)((n + 3) & ~int64_t(3));
+        return off;
+    };
+    p.sm_bias = bias ? take(e) : -1;
+    p.sm_extra = (additional_bias && additional_token_mask) ? take(e) : -1;
+    p.sm_rows = (hashing || p.group_path == kSmemGroups) ? take(kWarps * e) : -1;
+    p.sm_gkey = p.group_path == kSmemGroups ? take(kWarps * group_count) : -1;
+    p.sm_kept = p.group_path == kSmemGroups ? take(kWarps * 32) : -1;
+    const size_t smem = (size_t)words * 4;
     cudaError_t err;
-    if (vpl_needed <= 1)
-        err = launch_gating<1>(p, grid, stream);
-    else if (vpl_needed <= 2)
-        err = launch_gating<2>(p, grid, stream);
-    else if (vpl_needed <= 4)
-        err = launch_gating<4>(p, grid, stream);
-    else if (vpl_needed <= 8)
-        err = launch_gating<8>(p, grid, stream);
-    else if (vpl_needed <= 16)
-        err = launch_gating<16>(p, grid, stream);
-    else
-        err = launch_gating<32>(p, grid, stream);
+    switch (vpl) {
+    case 1: err = launch_gating<1>(p, smem, sms, stream); break;
+    case 2: err = launch_gating<2>(p, smem, sms, stream); break;
+    case 4: err = launch_gating<4>(p, smem, sms, stream); break;
+    case 6: err = launch_gating<6>(p, smem, sms, stream); break;
+    case 8: err = launch_gating<8>(p, smem, sms, stream); break;
+    case 12: err = launch_gating<12>(p, smem, sms, stream); break;
+    case 16: err = launch_gating<16>(p, smem, sms, stream); break;
+    case 24: err = launch_gating<24>(p, smem, sms, stream); break;
+    default: err = launch_gating<32>(p, smem, sms, stream); break;
+    }
     if (err != cudaSuccess) {
         (void)cudaGetLastError();
         return MRR_ERR_CUDA;

@@ -53,12 +53,12 @@ def raw(a: np.ndarray, dt: str) -> np.ndarray:
 
 
 def run_gpu_gating(x32, dt, k, *, bias=None, input_ids=None, tid2eid=None, extra_bias=None, mask=None,
-                   out_flag=True, expect=m.MRR_OK, **kw):
+                   out_flag=True, expect=m.MRR_OK, x_offset=0, out_offset=0, **kw):
     import torch
 
     d = torch.device("cuda:0")
     T, e = x32.shape
-    xb = DevBuf.of(raw(x32, dt), d)
+    xb = DevBuf.of(raw(x32, dt), d, offset=x_offset)
     bb = None if bias is None else DevBuf.of(raw(bias, dt), d)
     eb = None if extra_bias is None else DevBuf.of(raw(extra_bias, dt), d)
     mb = None if mask is None else DevBuf.of(np.asarray(mask, np.uint8), d)
@@ -67,7 +67,7 @@ def run_gpu_gating(x32, dt, k, *, bias=None, input_ids=None, tid2eid=None, extra
     esz = {"float16": 2, "bfloat16": 2, "float32": 4}[dt]
     y = DevBuf(T * k * esz, d)
     idx = DevBuf(T * k * 4, d)
-    out = DevBuf(T * e * 4, d) if out_flag else None
+    out = DevBuf(T * e * 4, d, offset=out_offset) if out_flag else None
     ws = DevBuf(4096, d, fill=0x5A)
     args = dict(k_group=1, group_count=1, routed_scaling_factor=1.0, eps=1e-20, group_select_mode=0,
                 renorm=0, norm_type=0)
@@ -181,7 +181,10 @@ def test_hash_index_out_of_range_is_reported():
 
 
 @pytest.mark.parametrize("T,e,k,G,kg", [(3, 1024, 64, 1, 1), (257, 33, 5, 1, 1), (40, 1024, 16, 32, 8),
-                                        (100, 64, 64, 1, 1), (16384, 256, 8, 8, 4), (5, 2, 2, 2, 2)])
+                                        (100, 64, 64, 1, 1), (16384, 256, 8, 8, 4), (5, 2, 2, 2, 2),
+                                        (64, 160, 5, 5, 2), (64, 1000, 16, 40, 7), (32, 1024, 8, 1024, 9),
+                                        (64, 384, 8, 8, 4), (64, 64, 4, 2, 1), (50, 96, 10, 6, 3),
+                                        (64, 200, 7, 10, 4), (64, 100, 5, 4, 2), (70, 512, 20, 16, 5)])
 def test_shapes(T, e, k, G, kg):
     rng = np.random.default_rng(T + e)
     x = as_dtype(rng.standard_normal((T, e)), "bfloat16")
@@ -209,3 +212,47 @@ def test_torch_level_call_3d_input():
     check_against_oracle({"status": m.MRR_OK, "guards": True, "y_out": y.reshape(16, 8).cpu().numpy(),
                           "expert_idx": idx.reshape(16, 8).cpu().numpy(),
                           "norm_out": out.reshape(16, 256).cpu().numpy()}, ref, "float32")
+
+
+@pytest.mark.parametrize("dt", ["float16", "bfloat16", "float32"])
+@pytest.mark.parametrize("e,k,G,kg,mode", [(384, 6, 1, 1, 0), (256, 8, 8, 4, 1), (160, 5, 5, 2, 1),
+                                            (1000, 16, 40, 7, 0), (64, 64, 1, 1, 0), (96, 10, 6, 3, 1)])
+def test_ties_go_to_the_lower_index(dt, e, k, G, kg, mode):
+    """Integer logits (many equal scores) and constant rows: equal scores must go to the lower
+    group / expert index, exactly as the oracle orders them."""
+    rng = np.random.default_rng(e + k + G)
+    x = rng.integers(-2, 3, size=(48, e)).astype(np.float32)
+    x[::7] = 0.5                                              # whole rows of equal scores
+    kw = dict(k_group=kg, group_count=G, group_select_mode=mode, norm_type=1, eps=1e-9)
+    ref = gating.gating_topk(x, k, **kw)
+    gpu = run_gpu_gating(x, dt, k, **kw)
+    assert np.array_equal(gpu["expert_idx"], ref["expert_idx"])
+    check_against_oracle(gpu, ref, dt, max_tie_rows=0)
+
+
+@pytest.mark.parametrize("dt", ["float16", "bfloat16", "float32"])
+@pytest.mark.parametrize("e", [256, 384, 96, 33])
+def test_misaligned_rows_use_narrower_loads(dt, e):
+    """x and norm_out at odd byte offsets: the kernel must fall back to narrower loads and stores."""
+    rng = np.random.default_rng(50 + e)
+    x = as_dtype(rng.standard_normal((40, e)), dt)
+    esz = 4 if dt == "float32" else 2
+    ref = gating.gating_topk(x, 6, k_group=1, group_count=1, norm_type=0, eps=1e-9)
+    for x_off, o_off in [(esz, 4), (2 * esz, 8), (4 * esz, 12)]:
+        gpu = run_gpu_gating(x, dt, 6, x_offset=x_off, out_offset=o_off, k_group=1, group_count=1,
+                             norm_type=0, eps=1e-9)
+        check_against_oracle(gpu, ref, dt)
+
+
+def test_grouped_additional_bias_and_norm_out():
+    """additional_bias rows together with grouped ranking (both group paths) and norm_out."""
+    rng = np.random.default_rng(60)
+    for e, G, kg, k in [(256, 8, 3, 6), (160, 5, 2, 4)]:
+        x = as_dtype(rng.standard_normal((64, e)), "bfloat16")
+        bias = as_dtype(rng.random(e) * 0.2, "bfloat16")
+        extra = as_dtype(rng.random(e) * 0.2, "bfloat16")
+        mask = rng.random(64) < 0.5
+        kw = dict(k_group=kg, group_count=G, group_select_mode=1, norm_type=2, routed_scaling_factor=1.5, eps=1e-9)
+        ref = gating.gating_topk(x, k, bias=bias, additional_bias=extra, additional_token_mask=mask, **kw)
+        gpu = run_gpu_gating(x, "bfloat16", k, bias=bias, extra_bias=extra, mask=mask, **kw)
+        check_against_oracle(gpu, ref, "bfloat16")
