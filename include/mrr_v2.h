@@ -127,6 +127,9 @@ typedef struct mrr_v2_plan {
                                  1: expert-major -> rank-major (mrr_v2_unroute_plan)          */
     int32_t smem_bytes;       /* dynamic shared memory per CTA                                */
     int32_t num_sms;          /* SMs on the device the plan was made for                      */
+    int32_t prefetch_chunks;  /* bulk path: chunks each CTA asks L2 to prefetch while it scans
+                                 the counts (its static chunks past the ring first, then its
+                                 share of the first counter-served chunks); 0 = none, <= 64   */
 } mrr_v2_plan_t;
 
 /*

@@ -98,6 +98,13 @@ __device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src_smem, uint32_t 
                  : "memory");
 }
 
+// ask L2 to fetch [src, src + bytes) ahead of use (16-byte aligned, size a multiple of 16); no
+// completion to wait for
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // L2 policy that marks lines as first candidates for eviction (data touched once)
 __device__ __forceinline__ uint64_t policy_evict_first()
 {

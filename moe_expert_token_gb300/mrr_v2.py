@@ -67,6 +67,7 @@ class mrr_v2_plan_t(ctypes.Structure):
         ("hints", ctypes.c_int32), ("sched", ctypes.c_int32), ("static_chunks", ctypes.c_int32),
         ("pdl", ctypes.c_int32), ("direction", ctypes.c_int32),
         ("smem_bytes", ctypes.c_int32), ("num_sms", ctypes.c_int32),
+        ("prefetch_chunks", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

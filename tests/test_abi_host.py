@@ -156,8 +156,8 @@ def test_run_plan_rejects_null_plan(lib):
 
 
 def test_plan_struct_layout_matches_header():
-    # 7 int64 fields followed by 17 int32 fields, padded to 8 bytes
-    assert ctypes.sizeof(m.mrr_v2_plan_t) == 7 * 8 + 17 * 4 + 4
+    # 7 int64 fields followed by 18 int32 fields: 128 bytes, no padding
+    assert ctypes.sizeof(m.mrr_v2_plan_t) == 7 * 8 + 18 * 4 == 128
 
 
 def test_cumsum_mode_passes_the_host_checks(lib):

@@ -139,6 +139,10 @@ STRESS_EDITS = [
     dict(sched=1, static_chunks=1, chunk_bytes=16, stages=2, grid=7),
     dict(pdl=0),
     dict(pdl=0, sched=0, grid=300),
+    dict(prefetch_chunks=1),                           # L2 prefetch of the next chunks
+    dict(prefetch_chunks=64, chunk_bytes=2048, stages=3, grid=9),
+    dict(prefetch_chunks=7, sched=0, chunk_bytes=1024),  # static slices: prefetch inside the slice
+    dict(prefetch_chunks=40, sched=1, static_chunks=1, chunk_bytes=16, stages=2, grid=7),
 ]
 
 
@@ -150,7 +154,7 @@ def test_bulk_pipeline_stress(edit, shape):
                                token_dtype="bfloat16", scale_layout="f32_as", scale_cols=4)
     ref = oracle.run_problem(p)
     assert_bit_exact(run_gpu(p, path=m.MRR_PATH_BULK, edit=edit), ref, p)
-    vec_edit = {k: v for k, v in edit.items() if k in ("grid", "block", "hints", "sched", "pdl")}
+    vec_edit = {k: v for k, v in edit.items() if k in ("grid", "block", "hints", "sched", "pdl", "prefetch_chunks")}
     assert_bit_exact(run_gpu(p, path=m.MRR_PATH_VECTOR, edit=vec_edit), ref, p)
 
 
@@ -311,3 +315,10 @@ def test_fp8_and_e8m0_torch_dtypes():
     ref = oracle.run_problem(p)
     assert np.array_equal(pt.view(torch.uint8).cpu().numpy(), ref["permute_tokens"])
     assert np.array_equal(ps.cpu().numpy().reshape(p.A, -1), ref["permute_scales"])
+
+
+@pytest.mark.parametrize("bad", [-1, 65])
+def test_plan_rejects_prefetch_out_of_range(bad):
+    p = workloads.make_problem(np.random.default_rng(5), A=64, H=128, N=4, E=4, token_dtype="bfloat16",
+                               scale_layout="none", scale_cols=0)
+    run_gpu(p, path=m.MRR_PATH_BULK, edit=dict(prefetch_chunks=bad), expect_host_status=m.MRR_ERR_PLAN)
