@@ -111,6 +111,30 @@ def profiled_traffic(config: int, op: str = "route"):
     return int(tr.group(1))
 
 
+GATING_PROFILES = {1: "gating_kernel_T16384_e384_top6.md", 2: "gating_kernel_T16384_e256_grouped_top8.md"}
+
+
+def gating_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in ("moe_expert_token_gb300/csrc/gating.cu", "moe_expert_token_gb300/csrc/ptx.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_gating_traffic(config: int):
+    """DRAM bytes per launch of the gating kernel from its committed ncu summary, if current."""
+    try:
+        text = open(os.path.join(ROOT, "profiles", GATING_PROFILES[config]), encoding="utf-8").read()
+    except (OSError, KeyError):
+        return None
+    src = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    if not src or not tr or src.group(1) != gating_source_hash():
+        return None
+    return int(tr.group(1))
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle samples, taken while the timed region runs."""
 
@@ -710,7 +734,8 @@ def run_gating(args):
                 "l2": f"{R} rotating buffer sets, {R * B / 1e6:.0f} MB > 4x L2 ({l2 / 1e6:.0f} MB)"}),
             "pct_of_peak": 100.0 * value / world / peak, "tokens_per_s": world * T * K / (ms * 1e-3),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_source": peak_kind, "traffic": None,
+                         "frac": achieved / peak, "peak_source": peak_kind,
+                         "traffic": profiled_gating_traffic(args.config),
                          "kernel": "mrr_gate::gating_kernel", "bytes_per_launch": B,
                          "mean_launch_us": local_ms / K * 1e3},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K, "clocks": clocks.summary()}), flush=True)
