@@ -631,15 +631,21 @@ constexpr int kTicketBits = 24;  // shared counter: [epoch of the launch | ticke
 constexpr unsigned long long kTicketMask = (1ull << kTicketBits) - 1;
 constexpr uint32_t kNoTicket = 0xFFFFFFFFu;
 
-// First claim of this launch on the shared counter.  The counter still holds the epoch of the
-// launch that used it last (or anything, in a fresh workspace); the first claimant installs
-// (epoch, 1) with a compare-and-swap and takes ticket 0, later claimants see the epoch and add.
-// Every launch has a different epoch, so no reset pass is needed.  Bounded: kNoTicket on failure.
-__device__ uint32_t claim_first_ticket(unsigned long long *ticket, unsigned long long epoch)
+// First claim of this launch on the shared counter, tagged with the host's launch epoch (a
+// per-process random seed plus a launch count).  The counter holds the tag of an older launch, or
+// anything in a fresh workspace; the first claimant installs (epoch, 1) with a compare-and-swap
+// and takes ticket 0, later claimants see the epoch and add.
+// A launch replayed from a CUDA graph keeps its parameters, epoch included, so it finds its own
+// tag left by the previous replay.  Every launch draws exactly last_claim + 1 values (each CTA its
+// tickets + 3), and a CTA's first claim comes before all its others, so a first claim can never
+// see its own launch's final count: a counter that reads (epoch, last_claim + 1) was finished by
+// an earlier run of this same launch and is installed afresh.  Bounded: kNoTicket on failure.
+__device__ uint32_t claim_first_ticket(unsigned long long *ticket, unsigned long long epoch, int64_t last_claim)
 {
+    const unsigned long long finished = (epoch << kTicketBits) | (unsigned long long)(last_claim + 1);
     unsigned long long cur = atomicAdd(ticket, 0ull);
     for (int it = 0; it < (1 << 16); ++it) {
-        if ((cur >> kTicketBits) == epoch)
+        if ((cur >> kTicketBits) == epoch && cur != finished)
             return (uint32_t)(atomicAdd(ticket, 1ull) & kTicketMask);
         const unsigned long long prev = atomicCAS(ticket, cur, (epoch << kTicketBits) | 1ull);
         if (prev == cur)
@@ -660,6 +666,7 @@ struct BulkRing {
     int64_t nch;                   // chunks in the whole token buffer
     uint32_t pending[2];           // the next two tickets, claimed ahead of use
     bool started;                  // the first ticket has been taken
+    int64_t last_claim;            // the launch's last ticket value: tickets + 3 * grid - 1
     int64_t tk_next, tk_end;       // chunk ids of the current ticket not yet served
     int per_ticket;                // consecutive chunks per ticket (about 64 KiB per claim)
 };
@@ -699,7 +706,9 @@ __device__ bool next_chunk(const Params &p, BulkRing &r, volatile uint32_t *s_fi
             r.pending[0] = r.pending[1];
             r.pending[1] = (uint32_t)(atomicAdd(p.ticket, 1ull) & kTicketMask);
         }
-        if (t == kNoTicket) {
+        if (t == kNoTicket || (int64_t)t > r.last_claim) {
+            // no ticket, or one no launch can draw: the counter was left by a run of this launch
+            // that never finished its claims (an error flagged at the time); flag it here too
             *tflag |= kFlagTimeout;
             r.dyn_first = -1;
             return false;
@@ -833,10 +842,15 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
         ring.next = min(p.total_bytes, b * span);
         ring.hi = min(p.total_bytes, (b + 1) * span);
         ring.dyn_first = (G * span < p.total_bytes) ? G * (int64_t)p.static_chunks : -1;
+        // Each CTA draws exactly its tickets + 3 values: the first ticket, the two claims kept in
+        // flight, and one claim per ticket it takes, the last of which is past the end.
+        const int64_t tickets = (ring.nch - ring.dyn_first + ring.per_ticket - 1) / ring.per_ticket;
+        ring.last_claim = ring.dyn_first >= 0 ? tickets + 3 * G - 1 : -1;
     } else {
         ring.next = lo;
         ring.hi = hi;
         ring.dyn_first = -1;
+        ring.last_claim = -1;
     }
     uint32_t *tab = reinterpret_cast<uint32_t *>(smem + (kBulk ? (size_t)p.stages * p.chunk_bytes : 0));
 
@@ -934,7 +948,7 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
             tflag = bulk_driver(p, ring, m, flags, s_first);
         } else if (tid >= 32 && !flags) {
             if (tid == 32 && dynamic && ring.dyn_first >= 0) {
-                s_first[0] = claim_first_ticket(p.ticket, p.epoch);
+                s_first[0] = claim_first_ticket(p.ticket, p.epoch, ring.last_claim);
                 __threadfence_block();
                 s_first[1] = 1u;
             }
@@ -1322,7 +1336,7 @@ mrr_status make_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int64_
         // into L2 meanwhile (measured: 4 chunks per CTA at 4096 segments, none below 1024)
         p.prefetch_chunks = (p.fuse_scan && NE > 1024) ? 4 : 0;
         const int64_t nch = (total + p.chunk_bytes - 1) / p.chunk_bytes;
-        p.sched = (nch + kMaxGrid < (int64_t)kTicketMask) ? 1 : 0;
+        p.sched = (nch + 3 * kMaxGrid < (int64_t)kTicketMask) ? 1 : 0;
         p.smem_bytes = (int32_t)((int64_t)p.stages * p.chunk_bytes + table_bytes);
         const int64_t want = (total + 65535) / 65536;
         p.grid = (int32_t)(want < 1 ? 1 : (want > sms ? sms : want));
@@ -1429,7 +1443,7 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
             return MRR_ERR_PLAN;
         if (pl.sched == 1) {
             const int64_t nch = (A * rb + pl.chunk_bytes - 1) / pl.chunk_bytes;
-            if (pl.static_chunks < 1 || pl.static_chunks > (1 << 20) || nch + kMaxGrid >= (int64_t)kTicketMask)
+            if (pl.static_chunks < 1 || pl.static_chunks > (1 << 20) || nch + 3 * kMaxGrid >= (int64_t)kTicketMask)
                 return MRR_ERR_PLAN;
         }
         smem += (int64_t)pl.stages * pl.chunk_bytes;
