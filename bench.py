@@ -52,6 +52,8 @@ def parse_args(argv=None):
                     help="CPU oracle baseline budget (seconds of oracle work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-detail", action="store_true",
+                    help="skip the batch spread, unrotated and CUDA-graph timings")
     return ap.parse_args(argv)
 
 
@@ -434,16 +436,26 @@ def run_gpu(args):
     achieved = bytes_step / (mean_launch_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
 
+    detail = None
+    if not args.no_detail:
+        detail = timing_detail(launch, sets, stream, launches_per_step)
+        for s in sets:   # the graph and unrotated runs left every set valid: check one status
+            st = m.mrr_v2_read_status(P(s["ws"]), s["ws"].numel(), sp)
+            if st != m.MRR_OK:
+                raise RuntimeError(m.mrr_status_str(st))
+
     # end to end through the C ABI from pinned host buffers: H2D inputs, run, D2H outputs
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, p, sets, launch, dev, bytes_step, world, dist)
 
-    cpu = None
+    cpu = cpu_par = None
     if rank == 0 and not args.no_cpu_baseline:
         gbs, reps, el = time_oracle(p, args.cpu_seconds, args.op)
         cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": f"the full workload, {reps} runs in {el:.1f} s, single thread"}
+        if args.op == "route":
+            cpu_par = time_cpu_parallel(p, min(args.cpu_seconds, 10.0))
 
     if rank != 0:
         return 0
@@ -466,6 +478,8 @@ def run_gpu(args):
                      "mean_launch_us": mean_launch_ms * 1e3,
                      "timing": "CUDA events around the K back-to-back launches on the launching stream; per launch = region / K"},
         "cpu_baseline": cpu,
+        "cpu_parallel": cpu_par,
+        "timing_detail": detail,
         "e2e": e2e,
         "gpu_launches": K * launches_per_step,
         "clocks": clocks.summary(),
@@ -474,6 +488,62 @@ def run_gpu(args):
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def time_cpu_parallel(p, budget_s: float):
+    """The multi-core CPU comparison program (OpenMP blocks of per-segment memcpy, not the oracle)
+    on the full workload, all host threads."""
+    try:
+        from oracle import parallel_baseline as pb
+
+        gbs, reps, el, threads, _ = pb.time_problem(p, budget_s)
+    except Exception as e:  # a host without OpenMP: report, do not fail the bench line
+        return {"value": None, "error": str(e)[:200]}
+    return {"value": gbs, "unit": "GB/s", "cores": threads,
+            "kind": "openmp blocks of per-segment memcpy (a plain parallel program, not the oracle)",
+            "sample": f"the full workload, {reps} runs in {el:.1f} s"}
+
+
+def timing_detail(launch, sets, stream, launches_per_step, batches=20, per_batch=50):
+    """Outside the timed region: the spread over batches of back-to-back launches (rotating sets),
+    the same launches on one unrotated buffer set, and the launches captured once in a CUDA graph
+    and replayed.  Microseconds per step."""
+    import numpy as np
+    import torch
+
+    R = len(sets)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn, n):
+        torch.cuda.synchronize()
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / n
+
+    per = []
+    for j in range(batches):
+        per.append(timed(lambda: [launch(sets[(j * per_batch + i) % R], stream) for i in range(per_batch)],
+                         per_batch))
+    unflushed = timed(lambda: [launch(sets[0], stream) for _ in range(per_batch)], per_batch)
+    out = {"batches": batches, "launches_per_batch": per_batch,
+           "batch_us": {q: float(np.percentile(per, v)) for q, v in (("p10", 10), ("p50", 50), ("p90", 90))},
+           "unflushed_us": unflushed}
+    try:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        with torch.cuda.graph(g, stream=cap):
+            for i in range(per_batch):
+                launch(sets[i % R], cap)
+        g.replay()
+        reps = 10
+        out["graph_us"] = timed(lambda: [g.replay() for _ in range(reps)], reps * per_batch)
+        out["graph_launches"] = per_batch * launches_per_step
+    except Exception as e:  # report, do not fail the bench line
+        out["graph_us"] = None
+        out["graph_error"] = str(e)[:200]
+    return out
 
 
 def run_e2e(args, p, sets, launch, dev, bytes_step, world, dist):
