@@ -44,6 +44,8 @@ constexpr int kTicketOffset = kStatusBytes;        // 8-byte shared chunk counte
 constexpr int kHeaderBytes = kStatusBytes + 256;   // status region + counter; offset tables follow
 constexpr int kMaxGrid = kStatusWords - 2;
 constexpr int64_t kFusedMaxSegs = 4096;            // N*E scanned inside every CTA up to this
+constexpr int64_t kSmemScanMaxSegs = 16384;        // above kFusedMaxSegs: the scan kernel scans in
+                                                   // shared memory up to this (about 200 KB)
 constexpr uint32_t kFlagNonPos = 1u, kFlagSum = 2u, kFlagTimeout = 4u;
 constexpr uint32_t kFlagBadIndex = 8u;  // set by the gating kernel (gating.cu)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // bound on any single mbarrier wait: 2 s
@@ -80,6 +82,7 @@ struct Params {
     int sched;            // bulk path: 0 static slices, 1 static chunks then shared-counter chunks
     int static_chunks;    // bulk path, sched 1: chunks each CTA takes before using the counter
     int prefetch_chunks;  // bulk path: chunks each CTA asks L2 to prefetch during the scan
+    int scan_in_smem;     // N*E > 4096: the scan kernel scans in smem (tables fit in one CTA)
     unsigned long long *ticket;  // sched 1: shared chunk counter in the workspace
     unsigned long long epoch;    // sched 1: this launch's tag for the counter (40 bits, nonzero)
 };
@@ -805,7 +808,10 @@ __device__ uint32_t bulk_driver(const Params &p, BulkRing &r, const SegMap &m, u
 // ------------------------------------------------------------------------------------------------
 // kernels
 
-template <bool kBulk, bool kFused>
+// kBulk: bulk-copy ring (rows a multiple of 16 bytes) or vector path; kFused: the counts are
+// scanned in every CTA (N*E <= 4096); kStage (N*E > 4096 only): the scan kernel's tables are
+// copied into shared memory first instead of being read from L2.
+template <bool kBulk, bool kFused, bool kStage>
 __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -938,6 +944,26 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
         m.row_ex = p.g_row_ex;
         m.dst_off = p.g_dst_off;
         m.col_ex = p.g_col_ex;
+        if (kStage && !flags) {
+            // Copy the two tables this direction uses from L2 into shared memory, so the driver's
+            // binary searches and per-piece lookups do not pay an L2 round trip each:
+            //   [0, NE]            SrcOffset (row-major starts)
+            //   then padded_len    DstOffset (forward) or the column-major starts (inverse)
+            // 16-byte copies; the workspace tables are 256-byte aligned and a few words longer.
+            uint32_t *rex = tab, *second = tab + ((p.NE + 1 + 3) & ~3);
+            const uint32_t *gsec = p.inverse ? p.g_col_ex : p.g_dst_off;
+            const int n1 = (p.NE + 1 + 3) >> 2, n2 = (int)((padded_len(p.NE) + 3) >> 2);
+#pragma unroll 1
+            for (int k = tid; k < n1; k += nthr)
+                reinterpret_cast<uint4 *>(rex)[k] = reinterpret_cast<const uint4 *>(p.g_row_ex)[k];
+#pragma unroll 1
+            for (int k = tid; k < n2; k += nthr)
+                reinterpret_cast<uint4 *>(second)[k] = reinterpret_cast<const uint4 *>(gsec)[k];
+            __syncthreads();
+            m.row_ex = rex;
+            m.dst_off = second;
+            m.col_ex = second;
+        }
         if (b == 0 && tid == 0)
             p.status[1] = (uint32_t)G;
     }
@@ -966,6 +992,7 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
 // global memory, tile by tile with a running carry.
 __global__ void __launch_bounds__(1024) scan_kernel(const Params p)
 {
+    extern __shared__ __align__(16) uint32_t sm_tab[];
     __shared__ uint32_t s_warp[32];
     __shared__ uint32_t s_flags;
     __shared__ unsigned long long s_sum;
@@ -977,6 +1004,34 @@ __global__ void __launch_bounds__(1024) scan_kernel(const Params p)
     }
     grid_dependency_wait();
     grid_launch_dependents();
+    if (p.scan_in_smem) {
+        // the same in-CTA scan the fused copy kernel runs, then the tables written out
+        uint32_t *rex = sm_tab, *cnt_t = sm_tab + NE + 1, *dof = cnt_t + padded_len(NE);
+        CountBatch cb;
+        if (p.count_is_i64)
+            issue_count_loads<long long>(p, 0, cb);
+        else
+            issue_count_loads<int>(p, 0, cb);
+        const uint32_t flags = cta_scan(p, cb, rex, cnt_t, dof, s_warp, &s_flags, &s_sum);
+        if (flags) {
+            if (tid == 0)
+                p.status[0] = flags;
+            return;
+        }
+        for (int k = tid; k <= NE; k += nthr)
+            p.g_row_ex[k] = rex[k];
+        const int np = (int)padded_len(NE);
+        for (int k = tid; k < np; k += nthr)
+            p.g_dst_off[k] = dof[k];
+        if (p.inverse)
+            for (int k = tid; k < np; k += nthr)
+                p.g_col_ex[k] = cnt_t[k];
+        else
+            write_expert_token_num(p, dof, tid, nthr);
+        if (tid == 0)
+            p.status[0] = 0u;
+        return;
+    }
     __syncthreads();
     uint32_t f = 0u;
     unsigned long long sum = 0ull;
@@ -1071,6 +1126,18 @@ int token_bits(int dt)
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
 // workspace bytes of the two offset tables for N*E > 4096: SrcOffset dense, DstOffset padded
+// Shared memory of the two tables the copy kernel stages when N*E > 4096 (see reroute_kernel).
+int64_t staged_table_bytes(int64_t NE)
+{
+    return 4 * (((NE + 1 + 3) & ~int64_t(3)) + ((padded_len(NE) + 3) & ~int64_t(3)));
+}
+
+// Shared memory of the scan kernel's in-CTA scan (row-major counts, column-major copy, DstOffset).
+int64_t scan_smem_bytes(int64_t NE)
+{
+    return 4 * (NE + 1 + 2 * padded_len(NE));
+}
+
 int64_t table_workspace_bytes(int64_t NE, int inverse)
 {
     return round_up(4 * (NE + 1), 256) + round_up(4 * padded_len(NE), 256) +
@@ -1184,13 +1251,13 @@ unsigned long long next_launch_epoch()
     }
 }
 
-constexpr int kNumKernels = 5;
+constexpr int kNumKernels = 9;
 bool g_smem_attr_set[64][kNumKernels];  // per device: max dynamic smem raised for each kernel
 
-template <bool kBulk, bool kFused>
+template <bool kBulk, bool kFused, bool kStage>
 int kernel_slot()
 {
-    return (kBulk ? 2 : 0) + (kFused ? 1 : 0);
+    return (kBulk ? 4 : 0) + (kFused ? 2 : 0) + (kStage ? 1 : 0);
 }
 
 // Launch with or without programmatic stream serialization (the kernels wait for their
@@ -1212,11 +1279,27 @@ cudaError_t launch(K kern, const Params &p, int grid, int block, int smem, cudaS
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <bool kBulk, bool kFused>
+cudaError_t launch_scan(const Params &p, int smem, cudaStream_t stream, int device, bool pdl)
+{
+    constexpr int slot = 8;
+    if (smem > 48 * 1024 && device >= 0 && device < 64 && !g_smem_attr_set[device][slot]) {
+        int optin = 0;
+        cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+        if (e != cudaSuccess)
+            return e;
+        e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - 1024);
+        if (e != cudaSuccess)
+            return e;
+        g_smem_attr_set[device][slot] = true;
+    }
+    return launch(scan_kernel, p, 1, 1024, smem, stream, pdl);
+}
+
+template <bool kBulk, bool kFused, bool kStage>
 cudaError_t launch_copy(const Params &p, int grid, int block, int smem, cudaStream_t stream, int device, bool pdl)
 {
-    auto kern = reroute_kernel<kBulk, kFused>;
-    const int slot = kernel_slot<kBulk, kFused>();
+    auto kern = reroute_kernel<kBulk, kFused, kStage>;
+    const int slot = kernel_slot<kBulk, kFused, kStage>();
     if (device >= 0 && device < 64 && !g_smem_attr_set[device][slot]) {
         int optin = 0;
         cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
@@ -1311,7 +1394,15 @@ mrr_status make_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int64_
     p.num_sms = sms;
     p.pdl = 1;
     p.direction = direction;
-    const int64_t table_bytes = p.fuse_scan ? round_up(4 * (NE + 1 + 2 * padded_len(NE)), 128) : 0;
+    // N*E > 4096: the copy kernel stages its two tables in shared memory when a ring of 3 x 48 KiB
+    // still fits beside them (up to about 10k segments; the ring below is sized around them).
+    // Measured on GB300: a smaller ring loses more than the L2 lookups cost (16384 segments:
+    // 2 x 44 KiB staged 147 us per copy launch, 3 x 64 KiB reading the tables from L2 about 105).
+    const int64_t stage = staged_table_bytes(NE);
+    const bool can_stage = !p.fuse_scan && (p.path == MRR_PATH_BULK ? stage + 3 * 49152 <= optin - 1024
+                                                                   : stage <= optin - 1024);
+    const int64_t table_bytes = p.fuse_scan ? round_up(4 * (NE + 1 + 2 * padded_len(NE)), 128)
+                                            : (can_stage ? stage : 0);
     if (p.path == MRR_PATH_BULK) {
         // the deepest ring shared memory allows: 3 x 64 KiB, else 3 x 48 KiB, else 4 x 32 KiB, ...
         // More threads when the in-CTA scan of many segments is long.
@@ -1433,6 +1524,7 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
     if (path != MRR_PATH_BULK && path != MRR_PATH_VECTOR)
         return MRR_ERR_PLAN;
     int64_t smem = table_bytes;
+    const int64_t stage = staged_table_bytes(NE);
     if (path == MRR_PATH_BULK) {
         if (pl.stages < 2 || pl.stages > kMaxStages || pl.chunk_bytes < 16 || pl.chunk_bytes % 16 ||
             pl.chunk_bytes > (1 << 20))
@@ -1462,6 +1554,11 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
     }
     if (smem > optin - 1024)
         return MRR_ERR_PLAN;
+    // N*E > 4096: stage the copy kernel's tables when they fit beside what the plan asks for
+    const bool stage_tables = !pl.fuse_scan && smem + stage <= optin - 1024;
+    if (stage_tables)
+        smem += stage;
+    const bool scan_in_smem = !pl.fuse_scan && NE <= kSmemScanMaxSegs && scan_smem_bytes(NE) <= optin - 1024;
 
     uint32_t *status = reinterpret_cast<uint32_t *>(workspace);
     if (NE == 0) {
@@ -1509,6 +1606,7 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
     p.sched = pl.sched;
     p.static_chunks = pl.static_chunks;
     p.prefetch_chunks = path == MRR_PATH_BULK ? pl.prefetch_chunks : 0;
+    p.scan_in_smem = scan_in_smem ? 1 : 0;
     p.ticket = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(workspace) + kTicketOffset);
     p.epoch = (path == MRR_PATH_BULK && pl.sched == 1) ? next_launch_epoch() : 0ull;
     if (!pl.fuse_scan) {
@@ -1523,15 +1621,17 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
     cudaError_t e = cudaSuccess;
     const bool pdl = pl.pdl != 0;
     if (!pl.fuse_scan)
-        e = launch(scan_kernel, p, 1, 1024, 0, stream, pdl);
+        e = launch_scan(p, scan_in_smem ? (int)scan_smem_bytes(NE) : 0, stream, device, pdl);
     if (e == cudaSuccess) {
         const int grid = pl.grid, block = pl.block, sm = (int)smem;
         if (path == MRR_PATH_BULK)
-            e = pl.fuse_scan ? launch_copy<true, true>(p, grid, block, sm, stream, device, pdl)
-                             : launch_copy<true, false>(p, grid, block, sm, stream, device, pdl);
+            e = pl.fuse_scan      ? launch_copy<true, true, false>(p, grid, block, sm, stream, device, pdl)
+                : stage_tables    ? launch_copy<true, false, true>(p, grid, block, sm, stream, device, pdl)
+                                  : launch_copy<true, false, false>(p, grid, block, sm, stream, device, pdl);
         else
-            e = pl.fuse_scan ? launch_copy<false, true>(p, grid, block, sm, stream, device, pdl)
-                             : launch_copy<false, false>(p, grid, block, sm, stream, device, pdl);
+            e = pl.fuse_scan      ? launch_copy<false, true, false>(p, grid, block, sm, stream, device, pdl)
+                : stage_tables    ? launch_copy<false, false, true>(p, grid, block, sm, stream, device, pdl)
+                                  : launch_copy<false, false, false>(p, grid, block, sm, stream, device, pdl);
     }
     if (e != cudaSuccess) {
         (void)cudaGetLastError();

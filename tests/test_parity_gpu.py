@@ -322,3 +322,29 @@ def test_plan_rejects_prefetch_out_of_range(bad):
     p = workloads.make_problem(np.random.default_rng(5), A=64, H=128, N=4, E=4, token_dtype="bfloat16",
                                scale_layout="none", scale_cols=0)
     run_gpu(p, path=m.MRR_PATH_BULK, edit=dict(prefetch_chunks=bad), expect_host_status=m.MRR_ERR_PLAN)
+
+
+# ------------------------------------------------------------------------------ many segments
+
+@pytest.mark.parametrize("N,E", [(64, 128), (128, 128), (100, 200), (256, 256)],
+                         ids=["8192-staged", "16384-staged", "20000-global-scan", "65536-global"])
+@pytest.mark.parametrize("i64", [False, True], ids=["i32", "i64"])
+def test_many_segments(N, E, i64):
+    """N*E above the fused-scan limit: the scan kernel scans in shared memory up to 16384
+    segments (one or two count batches), and the copy kernel stages its tables in shared memory
+    while they fit beside the ring; both the forward and the inverse move, bulk and vector paths."""
+    from harness import run_gpu_unroute, assert_unroute_bit_exact
+
+    p = workloads.make_problem(np.random.default_rng(N + E + i64), A=2 * N * E + 123, H=64, N=N, E=E,
+                               token_dtype="bfloat16", count_dtype=np.int64 if i64 else np.int32,
+                               scale_layout="f32_as", scale_cols=2, has_topk=True, idx_type=int(i64))
+    ref = oracle.run_problem(p)
+    gpu = run_gpu(p)
+    assert gpu["plan"]["fuse_scan"] == 0
+    assert_bit_exact(gpu, ref, p)
+    assert_bit_exact(run_gpu(p, path=m.MRR_PATH_VECTOR), ref, p)
+    uref = oracle.unroute(p.tokens, p.counts, permute_scales=p.scales, permute_topk=p.topk)
+    assert_unroute_bit_exact(run_gpu_unroute(p), uref, p)
+    assert_unroute_bit_exact(run_gpu_unroute(p, path=m.MRR_PATH_VECTOR), uref, p)
+    # a smaller ring leaves room to stage the tables of 20000 segments on the bulk path too
+    assert_bit_exact(run_gpu(p, path=m.MRR_PATH_BULK, edit=dict(chunk_bytes=16384, stages=2)), ref, p)
