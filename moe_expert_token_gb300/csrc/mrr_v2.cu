@@ -583,13 +583,98 @@ __device__ __forceinline__ void copy_run(uint8_t *dst, const uint8_t *src, int64
         dst[k] = __ldg(src + k);
 }
 
-__device__ __forceinline__ void copy_block(uint8_t *dst, const uint8_t *src, int64_t len, int tid, int nthr)
+// Realigning copy of nv 16-byte vectors: output vector k (16-byte aligned, at d + 16k) is bytes
+// [r, r + 16) of the 32 bytes at the aligned source blocks a0 + 16k and a0 + 16k + 16, where
+// r = 4*Q + shift_bits/8 (1..15).  Each output word is a funnel shift of two source words.
+template <int Q>
+__device__ __forceinline__ void copy_shift_run(uint8_t *d, const uint8_t *a0, int64_t nv, uint32_t shift_bits,
+                                               int tid, int nthr)
+{
+    constexpr int U = 2;
+    int64_t k = tid;
+    for (; k + (int64_t)(U - 1) * nthr < nv; k += (int64_t)U * nthr) {
+        uint4 x[U], y[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint8_t *src = a0 + (k + (int64_t)u * nthr) * 16;
+            x[u] = __ldg(reinterpret_cast<const uint4 *>(src));
+            y[u] = __ldg(reinterpret_cast<const uint4 *>(src + 16));
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t w[8] = {x[u].x, x[u].y, x[u].z, x[u].w, y[u].x, y[u].y, y[u].z, y[u].w};
+            uint4 o;
+            o.x = __funnelshift_r(w[Q], w[Q + 1], shift_bits);
+            o.y = __funnelshift_r(w[Q + 1], w[Q + 2], shift_bits);
+            o.z = __funnelshift_r(w[Q + 2], w[Q + 3], shift_bits);
+            o.w = __funnelshift_r(w[Q + 3], w[Q + 4], shift_bits);
+            st_v4(d + (k + (int64_t)u * nthr) * 16, o);
+        }
+    }
+    for (; k < nv; k += nthr) {
+        const uint4 x = __ldg(reinterpret_cast<const uint4 *>(a0 + k * 16));
+        const uint4 y = __ldg(reinterpret_cast<const uint4 *>(a0 + k * 16 + 16));
+        const uint32_t w[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+        uint4 o;
+        o.x = __funnelshift_r(w[Q], w[Q + 1], shift_bits);
+        o.y = __funnelshift_r(w[Q + 1], w[Q + 2], shift_bits);
+        o.z = __funnelshift_r(w[Q + 2], w[Q + 3], shift_bits);
+        o.w = __funnelshift_r(w[Q + 3], w[Q + 4], shift_bits);
+        st_v4(d + k * 16, o);
+    }
+}
+
+// Copy len bytes whose source and destination differ in alignment.  [buf_lo, buf_hi) is the whole
+// source buffer: the aligned 16-byte source blocks read must lie inside it, so the realigned
+// middle is clamped to its inner aligned part and everything else moves byte by byte.
+__device__ __forceinline__ void copy_realign(uint8_t *dst, const uint8_t *src, int64_t len, const uint8_t *buf_lo,
+                                             const uint8_t *buf_hi, int tid, int nthr)
+{
+    int64_t head = (int64_t)((16 - ((uintptr_t)dst & 15u)) & 15u);   // bytes until dst is aligned
+    if (head > len)
+        head = len;
+    const uint8_t *s1 = src + head;
+    const uint32_t r = (uint32_t)((uintptr_t)s1 & 15u);             // != 0: the alignments differ
+    const uint8_t *a0 = s1 - r;                                      // aligned block holding s1
+    int64_t nv = (len - head) / 16;
+    // first and last source blocks read: a0 and a0 + 16 * nv (the second block of the last vector)
+    const uintptr_t lo_ok = ((uintptr_t)buf_lo + 15u) & ~(uintptr_t)15u, hi_ok = (uintptr_t)buf_hi & ~(uintptr_t)15u;
+    int64_t skip = 0;  // vectors at the front whose first block would start before the buffer
+    if ((uintptr_t)a0 < lo_ok)
+        skip = (int64_t)((lo_ok - (uintptr_t)a0 + 15u) / 16u);
+    if (skip > nv)
+        skip = nv;
+    const int64_t fit = (int64_t)hi_ok >= (int64_t)((uintptr_t)a0 + 32u)
+                            ? ((int64_t)hi_ok - (int64_t)(uintptr_t)a0 - 16) / 16 : 0;  // vectors k < fit read in bounds
+    if (nv > fit)
+        nv = fit > skip ? fit : skip;
+    // bytes before the realigned middle (the head and any skipped vectors), one by one
+    const int64_t mid0 = head + skip * 16, mid1 = head + nv * 16;
+    for (int64_t i = tid; i < mid0; i += nthr)
+        dst[i] = __ldg(src + i);
+    uint8_t *d = dst + mid0;
+    const uint8_t *b0 = a0 + skip * 16;
+    const uint32_t sh = 8u * (r & 3u);
+    switch (r >> 2) {
+    case 0: copy_shift_run<0>(d, b0, nv - skip, sh, tid, nthr); break;
+    case 1: copy_shift_run<1>(d, b0, nv - skip, sh, tid, nthr); break;
+    case 2: copy_shift_run<2>(d, b0, nv - skip, sh, tid, nthr); break;
+    default: copy_shift_run<3>(d, b0, nv - skip, sh, tid, nthr); break;
+    }
+    for (int64_t i = mid1 + tid; i < len; i += nthr)
+        dst[i] = __ldg(src + i);
+}
+
+__device__ __forceinline__ void copy_block(uint8_t *dst, const uint8_t *src, int64_t len, const uint8_t *buf_lo,
+                                           const uint8_t *buf_hi, int tid, int nthr)
 {
     const uintptr_t mis = ((uintptr_t)dst ^ (uintptr_t)src) & 15u;
     if (mis == 0)
         copy_run<16>(dst, src, len, tid, nthr);
     else if ((mis & 7u) == 0)
         copy_run<8>(dst, src, len, tid, nthr);
+    else if (len >= 256)
+        copy_realign(dst, src, len, buf_lo, buf_hi, tid, nthr);
     else if ((mis & 3u) == 0)
         copy_run<4>(dst, src, len, tid, nthr);
     else if ((mis & 1u) == 0)
@@ -615,7 +700,8 @@ __device__ void vector_copy(const Params &p, const SegMap &m, int64_t lo, int64_
             delta = ((int64_t)m.dest(q) - (int64_t)m.begin(q)) * rb;
         }
         const int64_t pe = min(hi, seg_end);
-        copy_block(p.out_tokens + pos + delta, p.tokens + pos, pe - pos, tid, nthr);
+        copy_block(p.out_tokens + pos + delta, p.tokens + pos, pe - pos, p.tokens, p.tokens + p.total_bytes,
+                   tid, nthr);
         pos = pe;
     }
 }
