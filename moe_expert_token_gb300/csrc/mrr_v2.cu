@@ -684,9 +684,19 @@ __device__ __forceinline__ void copy_block(uint8_t *dst, const uint8_t *src, int
 }
 
 // Walk the pieces of source byte range [lo, hi): each piece lies inside one segment, where the
-// destination is the source shifted by (DstOffset - SrcOffset) rows.
+// destination is the source shifted by (DstOffset - SrcOffset) rows.  Every warp takes its own
+// contiguous sub-range (in 16-byte units), so a CTA has as many pieces in flight as it has warps:
+// a run of small segments is not copied one latency-bound piece at a time.
 __device__ void vector_copy(const Params &p, const SegMap &m, int64_t lo, int64_t hi, int tid, int nthr)
 {
+    const int nwarps = nthr >> 5, warp = tid >> 5;
+    const int64_t units = (hi - lo + 15) >> 4;
+    const int64_t wlo = min(hi, lo + ((warp * units / nwarps) << 4));
+    const int64_t whi = (warp == nwarps - 1) ? hi : min(hi, lo + (((warp + 1) * units / nwarps) << 4));
+    lo = wlo;
+    hi = whi;
+    tid &= 31;
+    nthr = 32;
     if (lo >= hi)
         return;
     const int64_t rb = p.row_bytes;
