@@ -130,13 +130,9 @@ struct SegMap {
     int NE, N, E;
     int inv;
     __device__ __forceinline__ uint32_t begin(int g) const { return inv ? col_ex[pad32(g)] : row_ex[g]; }
-    __device__ __forceinline__ uint32_t dest(int g) const
-    {
-        if (!inv)
-            return dst_off[pad32(g)];
-        const int j = g / N;
-        return row_ex[(g - j * N) * E + j];
-    }
+    // forward: DstOffset of segment g; inverse: SrcOffset of the segment at position g (the scan
+    // stores it by position, so neither direction divides here)
+    __device__ __forceinline__ uint32_t dest(int g) const { return dst_off[pad32(g)]; }
     // the last g in [0, NE) with begin(g) <= s (starts strictly increase: every count > 0)
     __device__ __forceinline__ int find(uint32_t s) const
     {
@@ -376,9 +372,12 @@ __device__ uint32_t cta_scan(const Params &p, CountBatch &cb, uint32_t *row_ex, 
                 ci = pos - cj * N;
             }
             cpos = pos;
-            dst_off[pad32(ci * E + cj)] = v;
-            if (p.inverse)
-                cnt_t[pad32(pos)] = v;  // in place: the starts of the inverse move's source segments
+            if (p.inverse) {
+                cnt_t[pad32(pos)] = v;                       // in place: the inverse move's source starts
+                dst_off[pad32(pos)] = row_ex[ci * E + cj];   // and its destinations, by position
+            } else {
+                dst_off[pad32(ci * E + cj)] = v;
+            }
         });
     if (p.inverse && tid == 0)
         cnt_t[pad32(NE)] = (uint32_t)p.A;
@@ -1043,22 +1042,23 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
         if (kStage && !flags) {
             // Copy the two tables this direction uses from L2 into shared memory, so the driver's
             // binary searches and per-piece lookups do not pay an L2 round trip each:
-            //   [0, NE]            SrcOffset (row-major starts)
-            //   then padded_len    DstOffset (forward) or the column-major starts (inverse)
+            //   the starts: SrcOffset [0, NE] (forward) or the column-major starts (inverse, padded)
+            //   the destinations: dst_off (padded; by segment forward, by position inverse)
             // 16-byte copies; the workspace tables are 256-byte aligned and a few words longer.
-            uint32_t *rex = tab, *second = tab + ((p.NE + 1 + 3) & ~3);
-            const uint32_t *gsec = p.inverse ? p.g_col_ex : p.g_dst_off;
-            const int n1 = (p.NE + 1 + 3) >> 2, n2 = (int)((padded_len(p.NE) + 3) >> 2);
+            const int n2 = (int)((padded_len(p.NE) + 3) >> 2);
+            const int n1 = p.inverse ? n2 : (p.NE + 1 + 3) >> 2;
+            uint32_t *first = tab, *second = tab + 4 * n1;
+            const uint32_t *gfirst = p.inverse ? p.g_col_ex : p.g_row_ex;
 #pragma unroll 1
             for (int k = tid; k < n1; k += nthr)
-                reinterpret_cast<uint4 *>(rex)[k] = reinterpret_cast<const uint4 *>(p.g_row_ex)[k];
+                reinterpret_cast<uint4 *>(first)[k] = reinterpret_cast<const uint4 *>(gfirst)[k];
 #pragma unroll 1
             for (int k = tid; k < n2; k += nthr)
-                reinterpret_cast<uint4 *>(second)[k] = reinterpret_cast<const uint4 *>(gsec)[k];
+                reinterpret_cast<uint4 *>(second)[k] = reinterpret_cast<const uint4 *>(p.g_dst_off)[k];
             __syncthreads();
-            m.row_ex = rex;
+            m.row_ex = first;
+            m.col_ex = first;
             m.dst_off = second;
-            m.col_ex = second;
         }
         if (b == 0 && tid == 0)
             p.status[1] = (uint32_t)G;
@@ -1170,16 +1170,19 @@ __global__ void __launch_bounds__(1024) scan_kernel(const Params p)
     }
     if (tid == 0)
         p.g_row_ex[NE] = (uint32_t)p.A;
+    __syncthreads();  // the row-major starts above, read by position below (inverse move)
     carry = 0u;
     for (int base = 0; base < NE; base += nthr) {
         const int pos = base + tid;
         const int q = pos < NE ? (pos % N) * E + pos / N : 0;
         const uint32_t v = pos < NE ? (uint32_t)load_count(p, q) : 0u;
         const uint32_t ex = block_exscan(v, &total, s_warp);
-        if (pos < NE)
+        if (pos < NE && !p.inverse)
             p.g_dst_off[pad32(q)] = carry + ex;
-        if (pos < NE && p.inverse)
+        if (pos < NE && p.inverse) {
             p.g_col_ex[pad32(pos)] = carry + ex;
+            p.g_dst_off[pad32(pos)] = p.g_row_ex[q];
+        }
         carry += total;
     }
     if (tid == 0 && p.inverse)
@@ -1225,7 +1228,7 @@ int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 // Shared memory of the two tables the copy kernel stages when N*E > 4096 (see reroute_kernel).
 int64_t staged_table_bytes(int64_t NE)
 {
-    return 4 * (((NE + 1 + 3) & ~int64_t(3)) + ((padded_len(NE) + 3) & ~int64_t(3)));
+    return 8 * ((padded_len(NE) + 3) & ~int64_t(3));  // two padded tables (the row-major one is shorter)
 }
 
 // Shared memory of the scan kernel's in-CTA scan (row-major counts, column-major copy, DstOffset).
