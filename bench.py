@@ -548,9 +548,7 @@ def timing_detail(launch, sets, stream, launches_per_step, batches=20, per_batch
 
 def run_e2e(args, p, sets, launch, dev, bytes_step, world, dist):
     """Same metric through the C ABI from pinned host buffers: every step uploads its inputs,
-    runs, and reads every output back.  Steps are pipelined over two device buffer sets and
-    three streams (upload / run / read-back, ordered by events), so the read-back of step k
-    overlaps the upload of step k+1 on the two copy directions."""
+    runs, and reads every output back (see pipelined_e2e)."""
     import numpy as np
     import torch
 
@@ -563,6 +561,17 @@ def run_e2e(args, p, sets, launch, dev, bytes_step, world, dist):
     h_in = {"tokens": pinned(p.tokens), "counts": pinned(p.counts), "scales": pinned(p.scales),
             "topk": pinned(p.topk)}
     outs = ["out_tokens", "out_scales", "out_topk", "idx", "etn"]
+    return pipelined_e2e(args, h_in, outs, sets, launch, dev, bytes_step, world, dist)
+
+
+def pipelined_e2e(args, h_in, outs, sets, launch, dev, bytes_step, world, dist):
+    """Every step uploads the pinned host inputs h_in (name -> uint8 tensor) into a device set,
+    runs launch(set, stream), and reads the outputs named in outs back to pinned host memory.
+    Steps are pipelined over two device buffer sets and three streams (upload / run / read-back,
+    ordered by events), so the read-back of step k overlaps the upload of step k+1 on the two
+    copy directions."""
+    import torch
+
     two = sets[:2]
     h_out = [{k: (None if s[k] is None else torch.empty(s[k].numel() * s[k].element_size(),
                                                          dtype=torch.uint8).pin_memory())
@@ -585,7 +594,7 @@ def run_e2e(args, p, sets, launch, dev, bytes_step, world, dist):
                 s_in.wait_event(run_done[k - 2])      # this set's inputs are no longer read
             for name, t in h_in.items():
                 if t is not None:
-                    s[name].copy_(t, non_blocking=True)
+                    s[name].view(torch.uint8).reshape(-1).copy_(t, non_blocking=True)
             up_done[k].record(s_in)
         s_run.wait_event(up_done[k])
         if k >= 2:
@@ -763,32 +772,11 @@ def run_gating(args):
     peak, peak_kind = measured_peak()
     achieved = B / (local_ms / K * 1e-3) / 1e9
 
-    # end to end: x uploaded from pinned host memory, y and expert_idx read back, every step
-    x_pin = x_host.view(torch.uint8).reshape(-1).pin_memory()
-    y_pin = torch.empty(T * k * sets[0]["y"].element_size(), dtype=torch.uint8).pin_memory()
-    i_pin = torch.empty(T * k * 4, dtype=torch.uint8).pin_memory()
-    s0 = sets[0]
-
-    def e2e_step():
-        s0["x"].view(torch.uint8).reshape(-1).copy_(x_pin, non_blocking=True)
-        launch(s0, stream)
-        y_pin.copy_(s0["y"].view(torch.uint8).reshape(-1), non_blocking=True)
-        i_pin.copy_(s0["idx"].view(torch.uint8).reshape(-1), non_blocking=True)
-
+    # end to end: x uploaded from pinned host memory, y_out and expert_idx read back, every step
     e2e = None
     if not args.no_e2e:
-        KE = max(3, min(K, 200))
-        for _ in range(3):
-            e2e_step()
-        torch.cuda.synchronize(dev)
-        a.record(stream)
-        for _ in range(KE):
-            e2e_step()
-        b.record(stream)
-        torch.cuda.synchronize(dev)
-        ems = max_over_ranks(a.elapsed_time(b), dist, dev)
-        e2e = {"value": throughput_gbs(world, B, KE, ems), "unit": "GB/s", "h2d_bytes_per_step": x_pin.numel(),
-               "d2h_bytes_per_step": y_pin.numel() + i_pin.numel(), "steps": KE, "ms_per_step": ems / KE}
+        x_pin = x_host.view(torch.uint8).reshape(-1).pin_memory()
+        e2e = pipelined_e2e(args, {"x": x_pin}, ["y", "idx"], sets, launch, dev, B, world, dist)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         gbs, tok_s, reps, el = time_gating_oracle(w, min(args.cpu_seconds, 10.0))
