@@ -33,6 +33,10 @@
  *     Errors that depend on the count VALUES (a count <= 0, Sum != A) are found on the GPU:
  *     the outputs are then left unspecified and mrr_v2_read_status reports the error.
  *   - Calls on different streams must use different workspaces.
+ *   - The calls may be captured in a CUDA graph (stream capture) and the graph replayed: each
+ *     replay moves every row again (the workspace's chunk counter recognises a finished earlier
+ *     run of the same captured launch).  After a replay that reported MRR_ERR_TIMEOUT, zero the
+ *     workspace's counter word (bytes 4096..4103) or use a fresh workspace before replaying.
  */
 #ifndef MRR_V2_H
 #define MRR_V2_H
@@ -166,7 +170,7 @@ mrr_status mrr_v2_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int6
  *   workspace       >= plan.workspace_bytes device bytes, 256-byte aligned, caller-owned;
  *                   it holds the status words read by mrr_v2_read_status, the chunk counter
  *                   of the bulk path and, for N*E > 4096, the scanned offsets.  It needs no
- *                   initialisation: each launch tags the counter with its own epoch.
+ *                   initialisation: each call tags the counter with its own epoch.
  * Host-side errors return before anything is enqueued.  The empty problem (N*E = 0, A = 0)
  * only zero-fills expert_token_num.
  */

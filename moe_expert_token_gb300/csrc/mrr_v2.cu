@@ -12,17 +12,20 @@
 //   * One kernel does everything for N*E <= 4096: each CTA scans the counts into shared
 //     memory (row-major and column-major exclusive prefixes, warp-shuffle block scans) while
 //     its first token chunks are already in flight, then streams its slice of the token bytes.
-//   * Work is split by SOURCE bytes: CTA b owns an equal, contiguous, 16-byte-aligned slice of
-//     the token buffer.  Source addresses need no offsets, so the bulk path issues its first
-//     loads before the scan and hides the scan behind them.  Inside a segment both sides are
-//     contiguous, so a slice maps to a few contiguous runs ("pieces"), each copied as a whole.
+//   * Work is split by SOURCE bytes.  Source addresses need no offsets, so the bulk path issues
+//     its first loads (and L2 prefetches of the next chunks) before the scan and hides the scan
+//     behind them.  Inside a segment both sides are contiguous, so a range of source bytes maps
+//     to a few contiguous runs ("pieces"), each copied as a whole.
 //   * Bulk path (rows a multiple of 16 bytes): one thread per CTA drives the bulk-copy engine:
 //     cp.async.bulk global->shared into a ring of `stages` chunks (completion on mbarriers),
-//     then one cp.async.bulk shared->global per piece.  The other warps move the scale rows,
-//     top-k weights and the index at the same time.
-//   * Vector path (any alignment): every thread copies pieces with the widest vector width the
-//     relative alignment of source and destination allows (16 B down to 1 B).
-//   * N*E > 4096: a one-CTA scan kernel writes the offsets into the workspace first.
+//     then one cp.async.bulk shared->global per piece.  Each CTA takes a few static chunks,
+//     then claims chunks from a counter in the workspace, so all CTAs finish together.  The
+//     other warps move the scale rows, top-k weights and the index at the same time.
+//   * Vector path (rows not a multiple of 16 bytes, or unaligned buffers): each warp walks the
+//     pieces of its own sub-range; pieces whose source and destination alignments differ are
+//     realigned in registers (funnel shifts) so that every access is 16 bytes wide.
+//   * N*E > 4096: a one-CTA scan kernel writes the offsets into the workspace first; the copy
+//     kernel stages them in shared memory when they fit beside its ring.
 //   * Data-dependent errors (count <= 0, Sum != A) set flags in a status word in the
 //     workspace; every CTA then skips its stores.  Every wait is bounded in time; a timeout
 //     sets a flag, drains the copies in flight and returns (no trap, no assert).
