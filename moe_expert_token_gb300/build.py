@@ -24,7 +24,8 @@ LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libmrr_v2.so")
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]
+COMPILE_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]
+LINK_FLAGS = ["-shared"]
 
 
 def nvcc_path() -> str:
@@ -61,17 +62,40 @@ def is_stale() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile the library if it is missing or older than its sources; return its path."""
+    """Compile the library if it is missing or older than its sources; return its path.
+
+    Each source compiles to an object in its own nvcc process (in parallel), then one nvcc call
+    links the shared library.
+    """
     if not force and not is_stale():
         return LIB_PATH
     os.makedirs(LIB_DIR, exist_ok=True)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc_path(), *ARCH_FLAGS, *NVCC_FLAGS, "-I", INCLUDE, "-o", tmp, *SOURCES]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-        print(" ".join(cmd), file=sys.stderr)
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB_PATH)
+    tag = f".tmp{os.getpid()}"
+    nvcc = nvcc_path()
+    objs, procs = [], []
+    try:
+        for src in SOURCES:
+            obj = os.path.join(LIB_DIR, os.path.splitext(os.path.basename(src))[0] + tag + ".o")
+            cmd = [nvcc, *ARCH_FLAGS, *COMPILE_FLAGS, "-I", INCLUDE, "-c", "-o", obj, src]
+            if verbose:
+                cmd.insert(1, "-Xptxas=-v")
+                print(" ".join(cmd), file=sys.stderr)
+            objs.append(obj)
+            procs.append((cmd, subprocess.Popen(cmd)))
+        failed = [cmd for cmd, proc in procs if proc.wait() != 0]
+        if failed:
+            raise subprocess.CalledProcessError(1, failed[0])
+        tmp = LIB_PATH + tag
+        subprocess.run([nvcc, *ARCH_FLAGS, *LINK_FLAGS, "-o", tmp, *objs], check=True)
+        os.replace(tmp, LIB_PATH)
+    finally:
+        for _, proc in procs:
+            if proc.poll() is None:
+                proc.kill()
+                proc.wait()
+        for obj in objs:
+            if os.path.exists(obj):
+                os.remove(obj)
     return LIB_PATH
 
 

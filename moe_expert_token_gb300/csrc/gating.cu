@@ -175,6 +175,15 @@ __device__ __forceinline__ void load_run(float (&v)[VPL], const Params &p, long 
     }
 }
 
+// The two element-wise normalisations.  Both rank-by-logit rows and fully evaluated rows call
+// these, so a score is the same float whichever path computed it.
+__device__ __forceinline__ float sigmoid_score(float x) { return __frcp_rn(1.f + expf(-x)); }
+
+__device__ __forceinline__ float softplus_score(float x)
+{
+    return x > 20.f ? x + log1pf(expf(-x)) : log1pf(expf(x));
+}
+
 // steps 1-2 of the page for this lane's run: normalise, then add the row's bias (from shared memory)
 template <int VPL>
 __device__ __forceinline__ void normalise_and_bias(float (&v)[VPL], int norm_type, int nv, const float *bias)
@@ -198,11 +207,11 @@ __device__ __forceinline__ void normalise_and_bias(float (&v)[VPL], int norm_typ
     } else if (norm_type == 1) {
 #pragma unroll
         for (int u = 0; u < VPL; ++u)
-            v[u] = __frcp_rn(1.f + expf(-v[u]));
+            v[u] = sigmoid_score(v[u]);
     } else {
 #pragma unroll
         for (int u = 0; u < VPL; ++u)
-            v[u] = v[u] > 20.f ? v[u] + log1pf(expf(-v[u])) : log1pf(expf(v[u]));
+            v[u] = softplus_score(v[u]);
     }
     if (bias == nullptr)
         return;
@@ -280,8 +289,332 @@ __device__ __forceinline__ void rescan(LaneCands &c, const uint32_t (&kv)[VPL])
 // registers) was 7 % slower than 5.
 constexpr int min_ctas_per_sm(int vpl) { return vpl <= 12 ? 5 : (vpl <= 16 ? 4 : 3); }
 
-// VPL = experts per lane (the row's e <= 32 * VPL scores live in registers); DT = x's type.
+// Steps 1-3 of the page for row t with every score evaluated: normalise the lane's run, add the
+// bias, rank the groups, make the k picks (or look the experts up for hash routing).  Lane i
+// returns pick i in (y0, i0) and pick i + 32 in (y1, i1).
 template <int VPL, int DT>
+__device__ __forceinline__ void full_row(const Params &p, int t, int lane, int j0, int nv, float *smem,
+                                         float *s_row, uint32_t *s_gkey, uint32_t *s_kept, uint32_t &flags,
+                                         float &y0, uint32_t &i0, float &y1, uint32_t &i1)
+{
+    const int e = p.e, k = p.k;
+    // ---- steps 1-2
+    float v[VPL];
+    load_run<VPL, DT>(v, p, t, j0);
+    const bool extra = p.sm_extra >= 0 && p.extra_mask[t];
+    const float *bias = extra ? smem + p.sm_extra + j0 : (p.sm_bias >= 0 ? smem + p.sm_bias + j0 : nullptr);
+    normalise_and_bias<VPL>(v, p.norm_type, nv, bias);
+    if (p.norm_out) {
+        float *dst = p.norm_out + (long long)t * e + j0;
+        if (VPL % 4 == 0 && nv >= VPL && p.out_vec) {
+#pragma unroll
+            for (int c = 0; c < VPL / 4; ++c)
+                reinterpret_cast<float4 *>(dst)[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        } else {
+#pragma unroll
+            for (int u = 0; u < VPL; ++u)
+                if (u < nv)
+                    dst[u] = v[u];
+        }
+    }
+
+    // ---- step 3
+    y0 = y1 = 0.f;
+    i0 = i1 = 0u;
+    if (p.input_ids) {
+        // hash routing: the table row, scores looked up in the staged row
+#pragma unroll
+        for (int u = 0; u < VPL; ++u)
+            if (u < nv)
+                s_row[j0 + u] = v[u];
+        __syncwarp();
+        const long long id = p.input_ids[t];
+        const bool ok = id >= 0 && id < p.n_vocab;
+        for (int i = lane; i < k; i += 32) {
+            int j = ok ? p.tid2eid[id * k + i] : -1;
+            if (j < 0 || j >= e) {
+                flags |= kFlagBadIndex;
+                j = 0;
+            }
+            if (i < 32) {
+                y0 = s_row[j];
+                i0 = (uint32_t)j;
+            } else {
+                y1 = s_row[j];
+                i1 = (uint32_t)j;
+            }
+        }
+        __syncwarp();
+    } else {
+    uint32_t kv[VPL];
+#pragma unroll
+    for (int u = 0; u < VPL; ++u)
+        kv[u] = order_key(v[u]);
+    if (nv < VPL) {          // experts past e are no candidates
+#pragma unroll
+        for (int u = 0; u < VPL; ++u)
+            if (u >= nv)
+                kv[u] = 0u;
+    }
+
+    if (p.group_path == kLaneGroups) {
+        // each group is an aligned block of lanes_per_group lanes (a power of two)
+        const int lpg = p.lanes_per_group;
+        const int g = lane >> p.lpg_shift;
+        const bool member = g < p.group_count;
+        float m1 = v[0], m2 = -INFINITY;
+#pragma unroll
+        for (int u = 1; u < VPL; ++u) {
+            m2 = fmaxf(m2, fminf(m1, v[u]));
+            m1 = fmaxf(m1, v[u]);
+        }
+        for (int o = 1; o < lpg; o <<= 1) {
+            const float o1 = __shfl_xor_sync(kFull, m1, o), o2 = __shfl_xor_sync(kFull, m2, o);
+            m2 = fmaxf(fmaxf(m2, o2), fminf(m1, o1));
+            m1 = fmaxf(m1, o1);
+        }
+        const uint32_t gkey = order_key(p.select_mode == 0 ? m1 : m1 + m2);
+        const bool leader = member && (lane & (lpg - 1)) == 0;
+        bool kept = false;
+        for (int r = 0; r < p.k_group; ++r) {
+            const bool cand = leader && !kept;
+            const uint32_t top = __reduce_max_sync(kFull, cand ? gkey : 0u);
+            const uint32_t win = __reduce_min_sync(kFull, cand && gkey == top ? (uint32_t)g : kNoIndex);
+            kept = kept || (member && (uint32_t)g == win);
+        }
+        if (!kept) {
+#pragma unroll
+            for (int u = 0; u < VPL; ++u)
+                kv[u] = 0u;
+        }
+    } else if (p.group_path == kSmemGroups) {
+        const int G = p.group_count, gs = p.group_size;
+#pragma unroll
+        for (int u = 0; u < VPL; ++u)
+            if (u < nv)
+                s_row[j0 + u] = v[u];
+        s_kept[lane] = 0u;
+        __syncwarp();
+        for (int g = lane; g < G; g += 32) {
+            float m1 = -INFINITY, m2 = -INFINITY;
+            for (int j = g * gs; j < (g + 1) * gs; ++j) {
+                const float s = s_row[j];
+                m2 = fmaxf(m2, fminf(m1, s));
+                m1 = fmaxf(m1, s);
+            }
+            s_gkey[g] = order_key(p.select_mode == 0 ? m1 : m1 + m2);
+        }
+        __syncwarp();
+        for (int r = 0; r < p.k_group; ++r) {
+            uint32_t best = 0u, bg = kNoIndex;
+            for (int g = lane; g < G; g += 32) {   // g rises: the first of equal keys stays
+                const uint32_t key = ((s_kept[g >> 5] >> (g & 31)) & 1u) ? 0u : s_gkey[g];
+                if (key > best) {
+                    best = key;
+                    bg = (uint32_t)g;
+                }
+            }
+            const uint32_t top = __reduce_max_sync(kFull, best);
+            const uint32_t win = __reduce_min_sync(kFull, best == top ? bg : kNoIndex);
+            if (lane == 0 && win < (uint32_t)G)
+                s_kept[win >> 5] |= 1u << (win & 31);
+            __syncwarp();
+        }
+        // experts of dropped groups leave the candidates
+        int g = j0 / gs, r = j0 - g * gs;
+#pragma unroll
+        for (int u = 0; u < VPL; ++u) {
+            if (u < nv && !((s_kept[g >> 5] >> (g & 31)) & 1u))
+                kv[u] = 0u;
+            if (++r == gs) {
+                r = 0;
+                ++g;
+            }
+        }
+        __syncwarp();
+    }
+
+    // the k picks: the largest remaining key, ties to the lower expert index
+    LaneCands c;
+    first_scan<VPL>(c, kv);
+    uint32_t k0 = 0u, k1 = 0u;
+    for (int i = 0; i < k; ++i) {
+        const uint32_t top = __reduce_max_sync(kFull, c.b1);
+        const uint32_t mine = (uint32_t)(j0 + c.u1);
+        const bool has_top = c.b1 == top;
+        const uint32_t win = __reduce_min_sync(kFull, has_top ? mine : kNoIndex);
+        if (i < 32) {
+            k0 = lane == i ? top : k0;
+            i0 = lane == i ? win : i0;
+        } else {
+            k1 = lane == i - 32 ? top : k1;
+            i1 = lane == i - 32 ? win : i1;
+        }
+        bool need = false;
+        if (has_top && mine == win) {   // this lane gave the pick
+            c.last_key = c.b1;
+            c.last_u = c.u1;
+            c.b1 = c.b2;
+            c.u1 = c.u2;
+            c.b2 = 0u;
+            need = !c.complete && c.b1 == 0u;
+        }
+        if (__any_sync(kFull, need) && need)
+            rescan<VPL>(c, kv);
+    }
+    y0 = key_value(k0);
+    y1 = key_value(k1);
+    }
+}
+
+// the lane's two largest packed words below `below`
+template <int VPL>
+__device__ __forceinline__ void packed_top2(uint32_t &c1, uint32_t &c2, const uint32_t (&pk)[VPL], uint32_t below)
+{
+    c1 = c2 = 0u;
+#pragma unroll
+    for (int u = 0; u < VPL; ++u) {
+        const uint32_t w = pk[u] < below ? pk[u] : 0u;
+        c2 = max(c2, min(c1, w));
+        c1 = max(c1, w);
+    }
+}
+
+// the score of the 16-bit logit whose order key is `key`
+template <int DT>
+__device__ __forceinline__ float logit_score(uint32_t key, int norm_type)
+{
+    const uint32_t h = key >= 0x8000u ? key - 0x8000u : 0x8000u | (0x8000u - key);
+    const float x = bits16_to_float<DT>(h);
+    return norm_type == 1 ? sigmoid_score(x) : softplus_score(x);
+}
+
+// this lane's run of row `row` as 16-bit words, two experts per 32-bit word (experts past e: zero)
+template <int VPL>
+__device__ __forceinline__ void load_words(uint32_t (&w)[(VPL + 1) / 2], const Params &p, int row, int j0, int nv)
+{
+    constexpr int W = (VPL + 1) / 2;
+    const unsigned short *src = static_cast<const unsigned short *>(p.x) + (long long)row * p.e + j0;
+    if (VPL % 8 == 0 && nv >= VPL && p.vec_bytes >= 16) {
+#pragma unroll
+        for (int c = 0; c < VPL / 8; ++c) {
+            const uint4 q = __ldg(reinterpret_cast<const uint4 *>(src) + c);
+            w[4 * c] = q.x;
+            w[4 * c + 1] = q.y;
+            w[4 * c + 2] = q.z;
+            w[4 * c + 3] = q.w;
+        }
+    } else if (VPL % 4 == 0 && nv >= VPL && p.vec_bytes >= 8) {
+#pragma unroll
+        for (int c = 0; c < VPL / 4; ++c) {
+            const uint2 q = __ldg(reinterpret_cast<const uint2 *>(src) + c);
+            w[2 * c] = q.x;
+            w[2 * c + 1] = q.y;
+        }
+    } else if (VPL % 2 == 0 && nv >= VPL && p.vec_bytes >= 4) {
+#pragma unroll
+        for (int c = 0; c < W; ++c)
+            w[c] = __ldg(reinterpret_cast<const unsigned int *>(src) + c);
+    } else {
+#pragma unroll
+        for (int c = 0; c < W; ++c)
+            w[c] = 0u;
+#pragma unroll
+        for (int u = 0; u < VPL; ++u)
+            if (u < nv)
+                w[u >> 1] |= (uint32_t)__ldg(src + u) << (16 * (u & 1));
+    }
+}
+
+// Rank by logit.  Sigmoid and softplus are non-decreasing, so with no bias and no groups the
+// order of the scores is the order of the logits, and only the chosen experts need a score.  For
+// 16-bit x the lane packs each logit's 16-bit order key above (0xffff - expert): the packed words
+// are distinct, and one unsigned max over the row gives the largest logit and, among equal
+// logits, the lowest expert, so a pick is a single redux.sync.
+//
+// Float32 rounding can give different logits the same score (sigmoid saturates near 1), and the
+// ranking by score then puts the lower expert first.  The row checks the conditions below under
+// which the two rankings agree; where one fails it returns false and the caller evaluates the row
+// in full.  Otherwise lane i < k returns pick i in (y, idx), the same expert, order and score as the
+// full evaluation (for float32 functions that are monotone there).
+template <int VPL, int DT>
+__device__ __forceinline__ bool logit_ranked_row(const Params &p, int lane, int nv, const uint32_t (&w)[(VPL + 1) / 2],
+                                                 const uint32_t (&ip)[(VPL + 1) / 2], float &y, uint32_t &idx)
+{
+    constexpr int W = (VPL + 1) / 2;
+    const int k = p.k;
+    // 16-bit order keys, two at a time: positive h -> h ^ 0x8000, negative h -> (h ^ 0xffff) + 1,
+    // so -0 and +0 both map to 0x8000 and every key is >= 1; then packed with the expert
+    uint32_t pk[VPL];
+#pragma unroll
+    for (int c = 0; c < W; ++c) {
+        const uint32_t s = (w[c] >> 15) & 0x00010001u;
+        const uint32_t key2 = (w[c] ^ (s * 0x7fffu) ^ 0x80008000u) + s;
+        pk[2 * c] = __byte_perm(key2, ip[c], 0x1054);
+        if (2 * c + 1 < VPL)
+            pk[2 * c + 1] = __byte_perm(key2, ip[c], 0x3276);
+    }
+    if (nv < VPL) {          // experts past e are no candidates
+#pragma unroll
+        for (int u = 0; u < VPL; ++u)
+            if (u >= nv)
+                pk[u] = 0u;
+    }
+
+    // k picks; a lane keeps its two best remaining words and rescans below the last one it gave
+    // up when both are gone
+    uint32_t c1 = pk[0], c2 = 0u;
+#pragma unroll
+    for (int u = 1; u < VPL; ++u) {
+        c2 = max(c2, min(c1, pk[u]));
+        c1 = max(c1, pk[u]);
+    }
+    bool complete = c2 == 0u;
+    uint32_t pick = 0u;
+    for (int i = 0; i < k; ++i) {
+        const uint32_t top = __reduce_max_sync(kFull, c1);
+        pick = lane == i ? top : pick;
+        bool need = false;
+        uint32_t last = 0u;
+        if (c1 == top) {   // this lane gave the pick (never 0: the row has e >= k candidates)
+            last = c1;
+            c1 = c2;
+            c2 = 0u;
+            need = !complete && c1 == 0u;
+        }
+        if (__any_sync(kFull, need) && need) {
+            packed_top2<VPL>(c1, c2, pk, last);
+            complete = c2 == 0u;
+        }
+    }
+
+    // lane i: pick i's expert and score.  The picks rank exactly as their scores would when
+    //  * each pick i < k - 1 scores strictly above pick i + 1, or has the same logit (then the
+    //    lower expert is first either way), and
+    //  * pick k - 1 scores strictly above the next lower 16-bit logit, so no expert left out can
+    //    tie with it.
+    // Lane k (idle otherwise) scores that next lower logit; at k = 32, lane 31 does it as well.
+    const uint32_t key = pick >> 16;
+    const uint32_t key_prev = __shfl_up_sync(kFull, key, 1);
+    const float f = logit_score<DT>(lane == k ? key_prev - 1u : key, p.norm_type);
+    const float f_next = __shfl_down_sync(kFull, f, 1);
+    const uint32_t key_next = __shfl_down_sync(kFull, key, 1);
+    bool unsure;
+    if (lane == k - 1)
+        unsure = key > 1u && !((k < 32 ? f_next : logit_score<DT>(key - 1u, p.norm_type)) < f);
+    else
+        unsure = lane < k && key_next != key && !(f > f_next);
+    if (__any_sync(kFull, unsure))
+        return false;
+    y = lane < k ? f : 0.f;
+    idx = 0xffffu - (pick & 0xffffu);
+    return true;
+}
+
+// VPL = experts per lane (the row's e <= 32 * VPL scores live in registers); DT = x's type;
+// kByLogit: rank by logit (16-bit x, sigmoid or softplus, no bias, no groups, no hash routing, no
+// norm_out, k <= 32), with the full evaluation as the fallback.
+template <int VPL, int DT, bool kByLogit>
 __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(VPL)) gating_kernel(const Params p)
 {
     extern __shared__ __align__(16) float smem[];
@@ -306,176 +639,44 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(VPL)) gating_kernel(
                                       : nullptr;
     uint32_t *s_kept = p.sm_kept >= 0 ? reinterpret_cast<uint32_t *>(smem) + p.sm_kept + warp * 32 : nullptr;
 
-    uint32_t flags = 0u;
-    for (int t = blockIdx.x * kWarps + warp; t < p.T; t += gridDim.x * kWarps) {
-        // ---- steps 1-2
-        float v[VPL];
-        load_run<VPL, DT>(v, p, t, j0);
-        const bool extra = p.sm_extra >= 0 && p.extra_mask[t];
-        const float *bias = extra ? smem + p.sm_extra + j0 : (p.sm_bias >= 0 ? smem + p.sm_bias + j0 : nullptr);
-        normalise_and_bias<VPL>(v, p.norm_type, nv, bias);
-        if (p.norm_out) {
-            float *dst = p.norm_out + (long long)t * e + j0;
-            if (VPL % 4 == 0 && nv >= VPL && p.out_vec) {
+    // rank by logit: the inverted expert numbers of the lane's run, two per word
+    uint32_t ip[(VPL + 1) / 2];
+    if (kByLogit) {
+        const uint32_t base = 0xffffu - (uint32_t)(lane * VPL);
 #pragma unroll
-                for (int c = 0; c < VPL / 4; ++c)
-                    reinterpret_cast<float4 *>(dst)[c] =
-                        make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-            } else {
-#pragma unroll
-                for (int u = 0; u < VPL; ++u)
-                    if (u < nv)
-                        dst[u] = v[u];
-            }
-        }
+        for (int c = 0; c < (VPL + 1) / 2; ++c)
+            ip[c] = ((base - 2 * c - 1) << 16) | ((base - 2 * c) & 0xffffu);
+    }
 
-        // ---- step 3: lane i keeps pick i in (y0, i0) and pick i + 32 in (y1, i1)
+    // rank by logit: the warp's next row is loaded while it works on the current one (not at 32
+    // experts per lane, where the 16 words held across the full-evaluation fallback would spill)
+    constexpr int W = (VPL + 1) / 2;
+    constexpr bool kAhead = kByLogit && VPL < 32;
+    const int stride = gridDim.x * kWarps;
+    uint32_t w_next[W];
+    if (kAhead && blockIdx.x * kWarps + warp < p.T)
+        load_words<VPL>(w_next, p, blockIdx.x * kWarps + warp, j0, nv);
+
+    uint32_t flags = 0u;
+    for (int t = blockIdx.x * kWarps + warp; t < p.T; t += stride) {
         float y0 = 0.f, y1 = 0.f;
         uint32_t i0 = 0u, i1 = 0u;
-        if (p.input_ids) {
-            // hash routing: the table row, scores looked up in the staged row
+        bool done = false;
+        if (kByLogit) {
+            uint32_t w[W];
+            if (kAhead) {
 #pragma unroll
-            for (int u = 0; u < VPL; ++u)
-                if (u < nv)
-                    s_row[j0 + u] = v[u];
-            __syncwarp();
-            const long long id = p.input_ids[t];
-            const bool ok = id >= 0 && id < p.n_vocab;
-            for (int i = lane; i < k; i += 32) {
-                int j = ok ? p.tid2eid[id * k + i] : -1;
-                if (j < 0 || j >= e) {
-                    flags |= kFlagBadIndex;
-                    j = 0;
-                }
-                if (i < 32) {
-                    y0 = s_row[j];
-                    i0 = (uint32_t)j;
-                } else {
-                    y1 = s_row[j];
-                    i1 = (uint32_t)j;
-                }
+                for (int c = 0; c < W; ++c)
+                    w[c] = w_next[c];
+                if (t + stride < p.T)
+                    load_words<VPL>(w_next, p, t + stride, j0, nv);
+            } else {
+                load_words<VPL>(w, p, t, j0, nv);
             }
-            __syncwarp();
-        } else {
-            uint32_t kv[VPL];
-#pragma unroll
-            for (int u = 0; u < VPL; ++u)
-                kv[u] = order_key(v[u]);
-            if (nv < VPL) {          // experts past e are no candidates
-#pragma unroll
-                for (int u = 0; u < VPL; ++u)
-                    if (u >= nv)
-                        kv[u] = 0u;
-            }
-
-            if (p.group_path == kLaneGroups) {
-                // each group is an aligned block of lanes_per_group lanes (a power of two)
-                const int lpg = p.lanes_per_group;
-                const int g = lane >> p.lpg_shift;
-                const bool member = g < p.group_count;
-                float m1 = v[0], m2 = -INFINITY;
-#pragma unroll
-                for (int u = 1; u < VPL; ++u) {
-                    m2 = fmaxf(m2, fminf(m1, v[u]));
-                    m1 = fmaxf(m1, v[u]);
-                }
-                for (int o = 1; o < lpg; o <<= 1) {
-                    const float o1 = __shfl_xor_sync(kFull, m1, o), o2 = __shfl_xor_sync(kFull, m2, o);
-                    m2 = fmaxf(fmaxf(m2, o2), fminf(m1, o1));
-                    m1 = fmaxf(m1, o1);
-                }
-                const uint32_t gkey = order_key(p.select_mode == 0 ? m1 : m1 + m2);
-                const bool leader = member && (lane & (lpg - 1)) == 0;
-                bool kept = false;
-                for (int r = 0; r < p.k_group; ++r) {
-                    const bool cand = leader && !kept;
-                    const uint32_t top = __reduce_max_sync(kFull, cand ? gkey : 0u);
-                    const uint32_t win = __reduce_min_sync(kFull, cand && gkey == top ? (uint32_t)g : kNoIndex);
-                    kept = kept || (member && (uint32_t)g == win);
-                }
-                if (!kept) {
-#pragma unroll
-                    for (int u = 0; u < VPL; ++u)
-                        kv[u] = 0u;
-                }
-            } else if (p.group_path == kSmemGroups) {
-                const int G = p.group_count, gs = p.group_size;
-#pragma unroll
-                for (int u = 0; u < VPL; ++u)
-                    if (u < nv)
-                        s_row[j0 + u] = v[u];
-                s_kept[lane] = 0u;
-                __syncwarp();
-                for (int g = lane; g < G; g += 32) {
-                    float m1 = -INFINITY, m2 = -INFINITY;
-                    for (int j = g * gs; j < (g + 1) * gs; ++j) {
-                        const float s = s_row[j];
-                        m2 = fmaxf(m2, fminf(m1, s));
-                        m1 = fmaxf(m1, s);
-                    }
-                    s_gkey[g] = order_key(p.select_mode == 0 ? m1 : m1 + m2);
-                }
-                __syncwarp();
-                for (int r = 0; r < p.k_group; ++r) {
-                    uint32_t best = 0u, bg = kNoIndex;
-                    for (int g = lane; g < G; g += 32) {   // g rises: the first of equal keys stays
-                        const uint32_t key = ((s_kept[g >> 5] >> (g & 31)) & 1u) ? 0u : s_gkey[g];
-                        if (key > best) {
-                            best = key;
-                            bg = (uint32_t)g;
-                        }
-                    }
-                    const uint32_t top = __reduce_max_sync(kFull, best);
-                    const uint32_t win = __reduce_min_sync(kFull, best == top ? bg : kNoIndex);
-                    if (lane == 0 && win < (uint32_t)G)
-                        s_kept[win >> 5] |= 1u << (win & 31);
-                    __syncwarp();
-                }
-                // experts of dropped groups leave the candidates
-                int g = j0 / gs, r = j0 - g * gs;
-#pragma unroll
-                for (int u = 0; u < VPL; ++u) {
-                    if (u < nv && !((s_kept[g >> 5] >> (g & 31)) & 1u))
-                        kv[u] = 0u;
-                    if (++r == gs) {
-                        r = 0;
-                        ++g;
-                    }
-                }
-                __syncwarp();
-            }
-
-            // the k picks: the largest remaining key, ties to the lower expert index
-            LaneCands c;
-            first_scan<VPL>(c, kv);
-            uint32_t k0 = 0u, k1 = 0u;
-            for (int i = 0; i < k; ++i) {
-                const uint32_t top = __reduce_max_sync(kFull, c.b1);
-                const uint32_t mine = (uint32_t)(j0 + c.u1);
-                const bool has_top = c.b1 == top;
-                const uint32_t win = __reduce_min_sync(kFull, has_top ? mine : kNoIndex);
-                if (i < 32) {
-                    k0 = lane == i ? top : k0;
-                    i0 = lane == i ? win : i0;
-                } else {
-                    k1 = lane == i - 32 ? top : k1;
-                    i1 = lane == i - 32 ? win : i1;
-                }
-                bool need = false;
-                if (has_top && mine == win) {   // this lane gave the pick
-                    c.last_key = c.b1;
-                    c.last_u = c.u1;
-                    c.b1 = c.b2;
-                    c.u1 = c.u2;
-                    c.b2 = 0u;
-                    need = !c.complete && c.b1 == 0u;
-                }
-                if (__any_sync(kFull, need) && need)
-                    rescan<VPL>(c, kv);
-            }
-            y0 = key_value(k0);
-            y1 = key_value(k1);
+            done = logit_ranked_row<VPL, DT>(p, lane, nv, w, ip, y0, i0);
         }
+        if (!done)
+            full_row<VPL, DT>(p, t, lane, j0, nv, smem, s_row, s_gkey, s_kept, flags, y0, i0, y1, i1);
 
         // ---- step 4: scale and write
         const bool has0 = lane < k, has1 = lane + 32 < k;
@@ -525,17 +726,18 @@ int choose_vpl(int64_t e)
     return 32;
 }
 
-template <int VPL, int DT>
+template <int VPL, int DT, bool kByLogit>
 cudaError_t launch_gating_dt(const Params &p, size_t smem, int sms, cudaStream_t stream)
 {
+    const auto kernel = gating_kernel<VPL, DT, kByLogit>;
     if (smem > 48 * 1024) {
         const cudaError_t err =
-            cudaFuncSetAttribute(gating_kernel<VPL, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOptIn);
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOptIn);
         if (err != cudaSuccess)
             return err;
     }
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gating_kernel<VPL, DT>, kThreads, smem) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem) !=
             cudaSuccess ||
         per_sm < 1)
         per_sm = 1;
@@ -555,17 +757,19 @@ cudaError_t launch_gating_dt(const Params &p, size_t smem, int sms, cudaStream_t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gating_kernel<VPL, DT>, p);
+    return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 template <int VPL>
-cudaError_t launch_gating(const Params &p, size_t smem, int sms, cudaStream_t stream)
+cudaError_t launch_gating(const Params &p, bool by_logit, size_t smem, int sms, cudaStream_t stream)
 {
     if (p.dt == MRR_GATE_F32)
-        return launch_gating_dt<VPL, MRR_GATE_F32>(p, smem, sms, stream);
+        return launch_gating_dt<VPL, MRR_GATE_F32, false>(p, smem, sms, stream);
     if (p.dt == MRR_GATE_BF16)
-        return launch_gating_dt<VPL, MRR_GATE_BF16>(p, smem, sms, stream);
-    return launch_gating_dt<VPL, MRR_GATE_F16>(p, smem, sms, stream);
+        return by_logit ? launch_gating_dt<VPL, MRR_GATE_BF16, true>(p, smem, sms, stream)
+                        : launch_gating_dt<VPL, MRR_GATE_BF16, false>(p, smem, sms, stream);
+    return by_logit ? launch_gating_dt<VPL, MRR_GATE_F16, true>(p, smem, sms, stream)
+                    : launch_gating_dt<VPL, MRR_GATE_F16, false>(p, smem, sms, stream);
 }
 
 }  // namespace
@@ -671,17 +875,21 @@ extern "C" mrr_status mrr_gating_topk_run(const void *x, mrr_gate_dtype dt, int6
     p.sm_gkey = p.group_path == kSmemGroups ? take(kWarps * group_count) : -1;
     p.sm_kept = p.group_path == kSmemGroups ? take(kWarps * 32) : -1;
     const size_t smem = (size_t)words * 4;
+    // rank by logit where the scores keep the logits' order and nothing else decides: an
+    // element-wise normalisation, no bias rows, no groups, no hash table, no norm_out
+    const bool by_logit = dt != MRR_GATE_F32 && (norm_type == 1 || norm_type == 2) && !hashing &&
+                          p.group_path == kNoGroups && p.sm_bias < 0 && p.sm_extra < 0 && !norm_out && k <= 32;
     cudaError_t err;
     switch (vpl) {
-    case 1: err = launch_gating<1>(p, smem, sms, stream); break;
-    case 2: err = launch_gating<2>(p, smem, sms, stream); break;
-    case 4: err = launch_gating<4>(p, smem, sms, stream); break;
-    case 6: err = launch_gating<6>(p, smem, sms, stream); break;
-    case 8: err = launch_gating<8>(p, smem, sms, stream); break;
-    case 12: err = launch_gating<12>(p, smem, sms, stream); break;
-    case 16: err = launch_gating<16>(p, smem, sms, stream); break;
-    case 24: err = launch_gating<24>(p, smem, sms, stream); break;
-    default: err = launch_gating<32>(p, smem, sms, stream); break;
+    case 1: err = launch_gating<1>(p, by_logit, smem, sms, stream); break;
+    case 2: err = launch_gating<2>(p, by_logit, smem, sms, stream); break;
+    case 4: err = launch_gating<4>(p, by_logit, smem, sms, stream); break;
+    case 6: err = launch_gating<6>(p, by_logit, smem, sms, stream); break;
+    case 8: err = launch_gating<8>(p, by_logit, smem, sms, stream); break;
+    case 12: err = launch_gating<12>(p, by_logit, smem, sms, stream); break;
+    case 16: err = launch_gating<16>(p, by_logit, smem, sms, stream); break;
+    case 24: err = launch_gating<24>(p, by_logit, smem, sms, stream); break;
+    default: err = launch_gating<32>(p, by_logit, smem, sms, stream); break;
     }
     if (err != cudaSuccess) {
         (void)cudaGetLastError();

@@ -256,3 +256,44 @@ def test_grouped_additional_bias_and_norm_out():
         ref = gating.gating_topk(x, k, bias=bias, additional_bias=extra, additional_token_mask=mask, **kw)
         gpu = run_gpu_gating(x, "bfloat16", k, bias=bias, extra_bias=extra, mask=mask, **kw)
         check_against_oracle(gpu, ref, "bfloat16")
+
+
+def _logit_rows(rng, T_each, e, dt):
+    """Rows of several kinds: N(0,1), N(0,16), small integers (many equal logits), an ascending
+    ramp (every pick from the last lanes), +-0 only, and logits in [10, 20] where float32 sigmoid
+    saturates (different logits, equal scores)."""
+    kinds = [rng.standard_normal((T_each, e)),
+             rng.standard_normal((T_each, e)) * 4,
+             rng.integers(-2, 3, size=(T_each, e)).astype(np.float64),
+             np.tile(np.linspace(-3, 3, e), (T_each, 1)),
+             np.where(rng.random((T_each, e)) < 0.5, 0.0, -0.0),
+             rng.uniform(10, 20, size=(T_each, e))]
+    return as_dtype(np.concatenate(kinds), dt), len(kinds)
+
+
+@pytest.mark.parametrize("dt", ["float16", "bfloat16"])
+@pytest.mark.parametrize("norm_type", [1, 2])
+@pytest.mark.parametrize("e,k", [(384, 6), (256, 8), (1, 1), (7, 7), (33, 5), (64, 32), (100, 7), (160, 5),
+                                 (512, 20), (1000, 16), (1024, 32)])
+def test_rank_by_logit_matches_full_evaluation(dt, norm_type, e, k):
+    """With a 16-bit x, sigmoid or softplus, and no bias, groups, hash table or norm_out, the kernel
+    ranks by logit and scores only the chosen experts.  Asking for norm_out makes it evaluate every
+    score instead: the two runs must agree bit for bit, on rows that stress equal logits, saturated
+    scores and picks crowded into one lane, and match the oracle."""
+    rng = np.random.default_rng(e * 100 + k + 7 * norm_type)
+    T_each = 24
+    x, n_kinds = _logit_rows(rng, T_each, e, dt)
+    kw = dict(norm_type=norm_type, eps=1e-9, routed_scaling_factor=1.7)
+    fast = run_gpu_gating(x, dt, k, out_flag=False, **kw)
+    full = run_gpu_gating(x, dt, k, out_flag=True, **kw)
+    assert fast["status"] == m.MRR_OK and fast["guards"]
+    assert np.array_equal(fast["expert_idx"], full["expert_idx"])
+    assert np.array_equal(fast["y_out"].view(np.uint32), full["y_out"].view(np.uint32))
+    ref = gating.gating_topk(x, k, **kw)
+    plain = slice(0, 2 * T_each)           # random logits: near-ties are rare
+    check_against_oracle({**fast, "expert_idx": fast["expert_idx"][plain], "y_out": fast["y_out"][plain]},
+                         {key: v[plain] for key, v in ref.items()}, dt)
+    # constructed ties and saturated scores: every row must still be a valid top-k for the oracle
+    rest = slice(2 * T_each, n_kinds * T_each)
+    check_against_oracle({**fast, "expert_idx": fast["expert_idx"][rest], "y_out": fast["y_out"][rest]},
+                         {key: v[rest] for key, v in ref.items()}, dt, max_tie_rows=1.0)
