@@ -297,3 +297,36 @@ def test_rank_by_logit_matches_full_evaluation(dt, norm_type, e, k):
     rest = slice(2 * T_each, n_kinds * T_each)
     check_against_oracle({**fast, "expert_idx": fast["expert_idx"][rest], "y_out": fast["y_out"][rest]},
                          {key: v[rest] for key, v in ref.items()}, dt, max_tie_rows=1.0)
+
+
+@pytest.mark.parametrize("dt,T,e,k,norm_type", [("float16", 16384, 384, 6, 1), ("bfloat16", 20000, 256, 8, 2),
+                                                ("float16", 7001, 1000, 16, 1), ("bfloat16", 9000, 768, 32, 1)])
+def test_rank_by_logit_many_rows(dt, T, e, k, norm_type):
+    """Full-size batches: each warp ranks several rows, loading the next row while it works on the
+    current one.  Bit for bit against the full evaluation, and against the oracle."""
+    rng = np.random.default_rng(T + e + k)
+    x = as_dtype(rng.standard_normal((T, e)), dt)
+    kw = dict(norm_type=norm_type, eps=1e-6, routed_scaling_factor=2.5)
+    fast = run_gpu_gating(x, dt, k, out_flag=False, **kw)
+    full = run_gpu_gating(x, dt, k, out_flag=True, **kw)
+    assert np.array_equal(fast["expert_idx"], full["expert_idx"])
+    assert np.array_equal(fast["y_out"].view(np.uint32), full["y_out"].view(np.uint32))
+    ref = gating.gating_topk(x, k, **kw)
+    check_against_oracle(fast, ref, dt)
+
+
+@pytest.mark.parametrize("dt", ["float16", "bfloat16"])
+@pytest.mark.parametrize("e", [384, 100, 33, 1024])
+def test_rank_by_logit_misaligned_rows(dt, e):
+    """x at 2- and 4-byte offsets: the rank-by-logit loads fall back to 4-byte words or single
+    elements."""
+    rng = np.random.default_rng(70 + e)
+    x = as_dtype(rng.standard_normal((300, e)), dt)
+    kw = dict(norm_type=1, eps=1e-6)
+    ref = gating.gating_topk(x, 6, **kw)
+    for x_off in (2, 4, 8):
+        fast = run_gpu_gating(x, dt, 6, out_flag=False, x_offset=x_off, **kw)
+        full = run_gpu_gating(x, dt, 6, out_flag=True, x_offset=x_off, **kw)
+        assert np.array_equal(fast["expert_idx"], full["expert_idx"])
+        assert np.array_equal(fast["y_out"].view(np.uint32), full["y_out"].view(np.uint32))
+        check_against_oracle(fast, ref, dt)
