@@ -47,7 +47,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--op", choices=["route", "unroute", "gating"], default="route",
                     help="route: rank-major -> expert-major (the op); unroute: the inverse move; "
-                         "gating: the upstream gating top-k op (--config 1 or 2)")
+                         "gating: the upstream gating top-k op (--config 1, 2 or 3)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU oracle baseline budget (seconds of oracle work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -118,7 +118,9 @@ GATING_PROFILES = {1: "gating_kernel_T16384_e384_top6.md", 2: "gating_kernel_T16
 
 def gating_source_hash() -> str:
     h = hashlib.sha256()
-    for rel in ("moe_expert_token_gb300/csrc/gating.cu", "moe_expert_token_gb300/csrc/ptx.cuh"):
+    for rel in ("moe_expert_token_gb300/csrc/gating.cu", "moe_expert_token_gb300/csrc/gating_kernel.cuh",
+                "moe_expert_token_gb300/csrc/gating_f16.cu", "moe_expert_token_gb300/csrc/gating_bf16.cu",
+                "moe_expert_token_gb300/csrc/gating_f32.cu", "moe_expert_token_gb300/csrc/ptx.cuh"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

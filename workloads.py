@@ -235,11 +235,12 @@ def config(k: int, idx_type: Optional[int] = None) -> Problem:
 GATING_NAMES = {
     1: "gating: T=16384 tokens x 384 experts fp16, top-6, sigmoid, no groups",
     2: "gating: T=16384 tokens x 256 experts bf16, 8 groups keep 4, top-8, sigmoid + bias, top-2 group scores",
+    3: "gating: T=16384 tokens x 384 experts fp32, top-6, sigmoid, no groups",
 }
 
 
 def gating_config(k: int) -> dict:
-    """Gating workload k (1, 2), drawn with numpy default_rng(2000 + k).  x and bias are float32
+    """Gating workload k (1, 2, 3), drawn with numpy default_rng(2000 + k).  x and bias are float32
     arrays holding values already rounded to the workload's dtype."""
     import torch
 
@@ -259,4 +260,9 @@ def gating_config(k: int) -> dict:
         bias = rounded(rng.random(e) * 0.1, torch.bfloat16)
         return dict(name=GATING_NAMES[2], dtype="bfloat16", x=x, k=8, bias=bias, k_group=4, group_count=8,
                     group_select_mode=1, norm_type=1, routed_scaling_factor=2.5, eps=1e-20)
+    if k == 3:
+        T, e = 16384, 384
+        x = rng.standard_normal((T, e)).astype(np.float32)
+        return dict(name=GATING_NAMES[3], dtype="float32", x=x, k=6, bias=None, k_group=1, group_count=1,
+                    group_select_mode=0, norm_type=1, routed_scaling_factor=1.0, eps=1e-6)
     raise ValueError(f"no gating workload {k}")
