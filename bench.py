@@ -113,7 +113,8 @@ def profiled_traffic(config: int, op: str = "route"):
     return int(tr.group(1))
 
 
-GATING_PROFILES = {1: "gating_kernel_T16384_e384_top6.md", 2: "gating_kernel_T16384_e256_grouped_top8.md"}
+GATING_PROFILES = {1: "gating_kernel_T16384_e384_top6.md", 2: "gating_kernel_T16384_e256_grouped_top8.md",
+                   3: "gating_kernel_T16384_e384_fp32_top6.md"}
 
 
 def gating_source_hash() -> str:
