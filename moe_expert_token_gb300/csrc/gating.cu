@@ -126,9 +126,9 @@ extern "C" mrr_status mrr_gating_topk_run(const void *x, mrr_gate_dtype dt, int6
     p.sm_gkey = p.group_path == kSmemGroups ? take(kWarps * group_count) : -1;
     p.sm_kept = p.group_path == kSmemGroups ? take(kWarps * 32) : -1;
     const size_t smem = (size_t)words * 4;
-    // rank by logit where the scores keep the logits' order and nothing else decides: an
-    // element-wise normalisation, no bias rows, no groups, no hash table, no norm_out
-    const bool by_logit = (norm_type == 1 || norm_type == 2) && !hashing &&
+    // rank by logit where the scores keep the logits' order and nothing else decides: no bias
+    // rows, no groups, no hash table, no norm_out
+    const bool by_logit = !hashing &&
                           p.group_path == kNoGroups && p.sm_bias < 0 && p.sm_extra < 0 && !norm_out &&
                           k <= (dt == MRR_GATE_F32 ? 31 : 32);
     const cudaError_t err = dt == MRR_GATE_F32    ? launch_f32(p, vpl, by_logit, smem, sms, stream)

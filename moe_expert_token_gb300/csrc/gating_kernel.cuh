@@ -19,9 +19,9 @@
 //    used, so a pick costs a handful of instructions instead of a pass over the row;
 //  * group scores come from a shuffle butterfly when each group is an aligned block of lanes,
 //    else from the row staged in shared memory;
-//  * where sigmoid or softplus of a 16-bit x is all that ranks the experts, the row is ranked by
-//    logit: each logit's 16-bit order key is packed with its expert into one word, a pick is one
-//    redux.sync, and only the chosen experts are scored;
+//  * where the normalisation alone ranks the experts (no bias, no groups), the row is ranked by
+//    logit and only the chosen experts are scored; a 16-bit logit's order key is packed with its
+//    expert into one word, so a pick is one redux.sync;
 //  * 8 warps per CTA, shared memory sized to the call, as many CTAs as fit on the SMs.
 #pragma once
 
@@ -502,13 +502,38 @@ __device__ __forceinline__ void packed_top2(uint32_t &c1, uint32_t &c2, const ui
     }
 }
 
-// the score of the 16-bit logit whose order key is `key`
+// the 16-bit logit whose order key is `key`, as float
 template <int DT>
-__device__ __forceinline__ float logit_score(uint32_t key, int norm_type)
+__device__ __forceinline__ float logit_value(uint32_t key)
 {
     const uint32_t h = key >= 0x8000u ? key - 0x8000u : 0x8000u | (0x8000u - key);
-    const float x = bits16_to_float<DT>(h);
-    return norm_type == 1 ? sigmoid_score(x) : softplus_score(x);
+    return bits16_to_float<DT>(h);
+}
+
+// The score of one logit, computed as the full evaluation computes it.  Softmax needs the row's
+// largest logit mx and the reciprocal r of the row's exp-sum.
+struct LogitScorer {
+    int norm_type;
+    float mx, r;
+    __device__ __forceinline__ float operator()(float x) const
+    {
+        if (norm_type == 0)
+            return expf(x - mx) * r;
+        return norm_type == 1 ? sigmoid_score(x) : softplus_score(x);
+    }
+};
+
+// Softmax's mx and r for a row whose largest logit is mx: the lane adds exp(x - mx) over its run
+// in slot order, as the full evaluation does (experts past e add nothing), then the warp sums.
+template <int VPL>
+__device__ __forceinline__ float softmax_rcp(const float (&x)[VPL], int nv, float mx)
+{
+    float sum = 0.f;
+#pragma unroll
+    for (int u = 0; u < VPL; ++u)
+        if (u < nv)
+            sum += expf(x[u] - mx);
+    return __frcp_rn(warp_sum(sum));
 }
 
 // this lane's run of row `row` as 16-bit words, two experts per 32-bit word (experts past e: zero)
@@ -570,8 +595,9 @@ __device__ __forceinline__ bool logit_rank_holds(uint32_t key, int lane, int k, 
     return !__any_sync(kFull, unsure);
 }
 
-// Rank by logit.  Sigmoid and softplus are non-decreasing, so with no bias and no groups the
-// order of the scores is the order of the logits, and only the chosen experts need a score.  For
+// Rank by logit.  Softmax, sigmoid and softplus are non-decreasing in the logit, so with no bias
+// and no groups the order of the scores is the order of the logits, and only the chosen experts
+// need a score (softmax still sums exp over the row).  For
 // 16-bit x the lane packs each logit's 16-bit order key above (0xffff - expert): the packed words
 // are distinct, and one unsigned max over the row gives the largest logit and, among equal
 // logits, the lowest expert, so a pick is a single redux.sync.
@@ -582,7 +608,7 @@ __device__ __forceinline__ bool logit_rank_holds(uint32_t key, int lane, int k, 
 // caller evaluates the row in full.  Otherwise lane i < k returns pick i in (y, idx), the same
 // expert, order and score as the full evaluation (for float32 functions that are monotone there).
 template <int VPL, int DT>
-__device__ __forceinline__ bool logit_ranked_row(const Params &p, int lane, int nv, const uint32_t (&w)[(VPL + 1) / 2],
+__device__ __forceinline__ bool logit_ranked_row(const Params &p, int t, int lane, int nv, const uint32_t (&w)[(VPL + 1) / 2],
                                                  const uint32_t (&ip)[(VPL + 1) / 2], float &y, uint32_t &idx)
 {
     constexpr int W = (VPL + 1) / 2;
@@ -633,8 +659,19 @@ __device__ __forceinline__ bool logit_ranked_row(const Params &p, int lane, int 
     }
 
     // lane i: pick i's expert and score
+    LogitScorer score{p.norm_type, 0.f, 0.f};
+    if (p.norm_type == 0) {   // the run again (an L1 hit), rather than held across the picks
+        uint32_t w2[(VPL + 1) / 2];
+        load_words<VPL>(w2, p, t, lane * VPL, nv);
+        float x[VPL];
+#pragma unroll
+        for (int u = 0; u < VPL; ++u)
+            x[u] = bits16_to_float<DT>(w2[u >> 1] >> (16 * (u & 1)));
+        score.mx = logit_value<DT>(__shfl_sync(kFull, pick, 0) >> 16);
+        score.r = softmax_rcp<VPL>(x, nv, score.mx);
+    }
     float f;
-    if (!logit_rank_holds(pick >> 16, lane, k, [&](uint32_t key) { return logit_score<DT>(key, p.norm_type); }, f))
+    if (!logit_rank_holds(pick >> 16, lane, k, [&](uint32_t key) { return score(logit_value<DT>(key)); }, f))
         return false;
     y = lane < k ? f : 0.f;
     idx = 0xffffu - (pick & 0xffffu);
@@ -666,8 +703,13 @@ __device__ __forceinline__ bool logit_ranked_row_f32(const Params &p, int t, int
     }
     uint32_t key, k1, i1;
     pick_keys<VPL>(kv, j0, lane, k + 1, key, idx, k1, i1);   // lane k: the first expert left out
-    const float x = key_value(key);
-    const float f = p.norm_type == 1 ? sigmoid_score(x) : softplus_score(x);
+    LogitScorer score{p.norm_type, 0.f, 0.f};
+    if (p.norm_type == 0) {   // the run again (an L1 hit), rather than held across the picks
+        load_run<VPL, MRR_GATE_F32>(v, p, t, j0);
+        score.mx = key_value(__shfl_sync(kFull, key, 0));
+        score.r = softmax_rcp<VPL>(v, nv, score.mx);
+    }
+    const float f = score(key_value(key));
     const float f_next = __shfl_down_sync(kFull, f, 1);
     const uint32_t key_next = __shfl_down_sync(kFull, key, 1);
     bool unsure;
@@ -682,8 +724,8 @@ __device__ __forceinline__ bool logit_ranked_row_f32(const Params &p, int t, int
 }
 
 // VPL = experts per lane (the row's e <= 32 * VPL scores live in registers); DT = x's type;
-// kByLogit: rank by logit (sigmoid or softplus, no bias, no groups, no hash routing, no norm_out,
-// k <= 32, or k <= 31 for float32 x), with the full evaluation as the fallback.
+// kByLogit: rank by logit (no bias, no groups, no hash routing, no norm_out, k <= 32, or k <= 31
+// for float32 x), with the full evaluation as the fallback.
 template <int VPL, int DT, bool kByLogit>
 __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(VPL)) gating_kernel(const Params p)
 {
@@ -745,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(VPL)) gating_kernel(
             } else {
                 load_words<VPL>(w, p, t, j0, nv);
             }
-            done = logit_ranked_row<VPL, DT>(p, lane, nv, w, ip, y0, i0);
+            done = logit_ranked_row<VPL, DT>(p, t, lane, nv, w, ip, y0, i0);
         }
         if (!done)
             full_row<VPL, DT>(p, t, lane, j0, nv, smem, s_row, s_gkey, s_kept, flags, y0, i0, y1, i1);
