@@ -20,7 +20,12 @@
  * the page stores it in) and equal scores go to the lower group / expert index; y and the
  * normalised output include the bias; experts are listed in descending score order; y_out has
  * x's dtype; e must be a multiple of group_count and, for group_select_mode 1, groups hold at
- * least 2 experts.  This implementation handles e <= 1024.
+ * least 2 experts.  This implementation handles e <= 1024.  A row holding a NaN logit gets
+ * unspecified experts.
+ *
+ * Whether norm_out is asked for does not change y_out or expert_idx: without it, rows with no
+ * bias and no groups are ranked by logit and only the chosen experts are scored, which gives the
+ * same float32 scores, the same experts and the same order as scoring every expert.
  */
 #ifndef MRR_GATING_H
 #define MRR_GATING_H
