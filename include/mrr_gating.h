@@ -26,7 +26,8 @@
  * Whether norm_out is asked for does not change y_out or expert_idx: without it, rows with no
  * bias and no groups are ranked by logit and only the chosen experts are scored, which gives the
  * same float32 scores, the same experts and the same order as scoring every expert wherever the
- * float32 normalisation is monotone across the logits involved (always, for 16-bit x).
+ * float32 normalisation is monotone across the logits involved (where it is not, the ranking by
+ * logit is the one exact arithmetic gives).
  */
 #ifndef MRR_GATING_H
 #define MRR_GATING_H
