@@ -966,8 +966,53 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
             mbar_init(smem_addr(&bars[s]), 1u);
         mbar_init_fence();
     }
-    // Nothing above touches global memory.  When launched behind another kernel with
-    // programmatic stream serialization, wait for it here, then let the next launch be scheduled.
+    // Start streaming the token rows: their source addresses need no offsets.  Thread 0 fills the
+    // ring with this CTA's first chunks; warp 1 asks L2 for the next ones.
+    auto start_token_stream = [&]() {
+        if (kBulk && tid == 0) {
+            if (p.hints)
+                ring.policy = policy_evict_first();
+            while (ring.issued < p.stages && ring.next < ring.hi) {
+                const int64_t b0 = ring.next, b1 = min(ring.next + p.chunk_bytes, ring.hi);
+                ring.next = b1;
+                bulk_issue_load(p, ring, b0, b1);
+            }
+        }
+        if (kBulk && p.prefetch_chunks > 0 && tid >= 32 && tid < 64) {
+            // The ring holds only `stages` chunks, which land long before the offsets are ready.
+            // Keep HBM busy meanwhile: warp 1 asks L2 for the next chunks, one per lane -- first
+            // this CTA's own static chunks past the ring, then its share of the first chunks the
+            // counter hands out.
+            const int64_t C = p.chunk_bytes;
+            const int64_t st0 = ring.next + (int64_t)p.stages * C;  // ring.next: this CTA's first byte
+            const int64_t n_s =
+                st0 < ring.hi ? min((ring.hi - st0 + C - 1) / C, (int64_t)p.prefetch_chunks) : 0;
+            const int64_t n_d = ring.dyn_first >= 0 ? p.prefetch_chunks - n_s : 0;
+            const int64_t d_lo = ring.dyn_first + b * n_d;
+            for (int64_t i = tid - 32; i < n_s + n_d; i += 32) {
+                int64_t lo, hi;
+                if (i < n_s) {
+                    lo = st0 + i * C;
+                    hi = min(lo + C, ring.hi);
+                } else {
+                    const int64_t c = d_lo + (i - n_s);
+                    if (c >= ring.nch)
+                        break;
+                    lo = c * C;
+                    hi = min(lo + C, p.total_bytes);
+                }
+                bulk_prefetch_l2(p.tokens + lo, (uint32_t)(hi - lo));
+            }
+        }
+    };
+    // Behind the scan kernel (N*E > 4096) the tokens can stream before the wait below: that kernel
+    // runs its own wait before it lets this one start, so whatever wrote the tokens has finished,
+    // and it writes only the workspace tables, which are read after the wait.  The fused kernel may
+    // follow the tokens' producer directly, so it starts them after the wait.
+    if (!kFused)
+        start_token_stream();
+    // When launched behind another kernel with programmatic stream serialization, wait for it
+    // here, then let the next launch be scheduled.
     grid_dependency_wait();
     grid_launch_dependents();
     if (kFused) {
@@ -979,41 +1024,7 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
             issue_count_loads<long long>(p, 0, cb);
         else
             issue_count_loads<int>(p, 0, cb);
-    }
-
-    if (kBulk && tid == 0) {
-        if (p.hints)
-            ring.policy = policy_evict_first();
-        // source addresses need no offsets: start streaming the static chunks before the scan
-        while (ring.issued < p.stages && ring.next < ring.hi) {
-            const int64_t b0 = ring.next, b1 = min(ring.next + p.chunk_bytes, ring.hi);
-            ring.next = b1;
-            bulk_issue_load(p, ring, b0, b1);
-        }
-    }
-    if (kBulk && p.prefetch_chunks > 0 && tid >= 32 && tid < 64) {
-        // The ring holds only `stages` chunks, which land long before the offsets are ready.  Keep
-        // HBM busy meanwhile: warp 1 asks L2 for the next chunks, one per lane -- first this CTA's
-        // own static chunks past the ring, then its share of the first chunks the counter hands out.
-        const int64_t C = p.chunk_bytes;
-        const int64_t st0 = ring.next + (int64_t)p.stages * C;  // ring.next: this CTA's first byte
-        const int64_t n_s = st0 < ring.hi ? min((ring.hi - st0 + C - 1) / C, (int64_t)p.prefetch_chunks) : 0;
-        const int64_t n_d = ring.dyn_first >= 0 ? p.prefetch_chunks - n_s : 0;
-        const int64_t d_lo = ring.dyn_first + b * n_d;
-        for (int64_t i = tid - 32; i < n_s + n_d; i += 32) {
-            int64_t lo, hi;
-            if (i < n_s) {
-                lo = st0 + i * C;
-                hi = min(lo + C, ring.hi);
-            } else {
-                const int64_t c = d_lo + (i - n_s);
-                if (c >= ring.nch)
-                    break;
-                lo = c * C;
-                hi = min(lo + C, p.total_bytes);
-            }
-            bulk_prefetch_l2(p.tokens + lo, (uint32_t)(hi - lo));
-        }
+        start_token_stream();
     }
 
     uint32_t flags;
@@ -1537,7 +1548,8 @@ mrr_status make_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int64_
         // dynamic chunk scheduling unless the counter's 24-bit ticket space could run out
         p.static_chunks = p.stages + 1;
         // many segments: the in-CTA scan outlasts the ring's loads, so prefetch the next chunks
-        // into L2 meanwhile (measured: 4 chunks per CTA at 4096 segments, none below 1024)
+        // into L2 meanwhile (measured: 4 chunks per CTA at 4096 segments, none below 1024; behind
+        // the scan kernel, N*E > 4096, 4 to 12 chunks were 0-10 % slower than none)
         p.prefetch_chunks = (p.fuse_scan && NE > 1024) ? 4 : 0;
         const int64_t nch = (total + p.chunk_bytes - 1) / p.chunk_bytes;
         p.sched = (nch + 3 * kMaxGrid < (int64_t)kTicketMask) ? 1 : 0;
