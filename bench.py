@@ -54,6 +54,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-detail", action="store_true",
                     help="skip the batch spread, unrotated and CUDA-graph timings")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="time only the chosen workload (by default workload 2 is followed by 3, 4 and 5)")
     return ap.parse_args(argv)
 
 
@@ -314,8 +316,136 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------- GPU arm
 
+class RouteSetup:
+    """One workload on one GPU: its plan, rotating device buffer sets, and the C-ABI call of one
+    step (mrr_v2_run, or mrr_v2_unroute for the inverse move) with its arguments resolved."""
+
+    def __init__(self, p, op, dev, local_rank):
+        import numpy as np
+        import torch
+        import moe_expert_token_gb300.mrr_v2 as m
+
+        self.p, self.op, self.dev, self.m = p, op, dev, m
+        code = m.DTYPE_CODES[p.token_dtype]
+        sl = m.SCALE_CODES[p.scale_layout]
+        A, H, N, E = p.A, p.H, p.N, p.E
+        i64 = int(p.counts.dtype == np.int64)
+        if op == "route":
+            st, plan = m.mrr_v2_plan(A, H, code, N, E, i64, sl, p.scale_cols, p.topk is not None, 1,
+                                     p.idx_type, local_rank)
+        else:
+            st, plan = m.mrr_v2_unroute_plan(A, H, code, N, E, i64, sl, p.scale_cols, p.topk is not None,
+                                             local_rank)
+        if st != m.MRR_OK:
+            raise SystemExit(m.mrr_status_str(st))
+        self.plan = plan
+        self.launches_per_step = 1 if plan.fuse_scan else 2
+        self.bytes_step = op_bytes(p, op)
+
+        def dev_bytes(arr):
+            if arr is None:
+                return None
+            return torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8).reshape(-1).copy()).to(dev)
+
+        # buffer sets: enough that consecutive steps never hit in L2
+        self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.R = R = max(2, -(-4 * self.l2 // self.bytes_step))
+        host_in = {"tokens": p.tokens, "counts": p.counts, "scales": p.scales, "topk": p.topk}
+        inv = op == "unroute"   # the inverse move writes no index and no per-expert counts
+        self.sets = []
+        for _ in range(R):
+            s = {k: dev_bytes(v) for k, v in host_in.items()}
+            s["out_tokens"] = torch.empty(A * p.row_bytes, dtype=torch.uint8, device=dev)
+            s["out_scales"] = (None if p.scales is None
+                               else torch.empty(A * p.scale_row_bytes, dtype=torch.uint8, device=dev))
+            s["out_topk"] = None if p.topk is None else torch.empty(4 * A, dtype=torch.uint8, device=dev)
+            s["idx"] = None if inv else torch.empty(A, dtype=torch.int32, device=dev)
+            s["etn"] = None if inv else torch.empty(E * p.counts.dtype.itemsize, dtype=torch.uint8, device=dev)
+            s["ws"] = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+            self.sets.append(s)
+        lib = m.load_library()
+        P = lambda t: None if t is None else t.data_ptr()
+        if op == "route":
+            self.fn = lib.mrr_v2_run
+            self.args = [(P(s["tokens"]), code, A, H, P(s["counts"]), i64, N, E, P(s["scales"]), sl,
+                          p.scale_cols, P(s["topk"]), P(s["out_tokens"]), P(s["out_scales"]), P(s["idx"]),
+                          P(s["etn"]), P(s["out_topk"]), 1, p.idx_type, P(s["ws"]), s["ws"].numel())
+                         for s in self.sets]
+        else:  # the inverse move: the "tokens" buffers hold the expert-major rows
+            self.fn = lib.mrr_v2_unroute
+            self.args = [(P(s["tokens"]), code, A, H, P(s["counts"]), i64, N, E, P(s["scales"]), sl,
+                          p.scale_cols, P(s["topk"]), P(s["out_tokens"]), P(s["out_scales"]), P(s["out_topk"]),
+                          P(s["ws"]), s["ws"].numel())
+                         for s in self.sets]
+        self.set_index = {id(s): i for i, s in enumerate(self.sets)}
+
+    def launch(self, s, on_stream):
+        """One step on ``on_stream``: the C-ABI call on buffer set ``s``."""
+        st = self.fn(*self.args[self.set_index[id(s)]], on_stream.cuda_stream)
+        if st != self.m.MRR_OK:
+            raise RuntimeError(self.m.mrr_status_str(st))
+
+    def gate(self, stream):
+        """Untimed correctness gate on every buffer set: device status and a permutation check."""
+        import torch
+
+        m = self.m
+        for s in self.sets:
+            self.launch(s, stream)
+            st = m.mrr_v2_read_status(s["ws"].data_ptr(), s["ws"].numel(), stream.cuda_stream)
+            if st != m.MRR_OK:
+                raise RuntimeError(m.mrr_status_str(st))
+        if self.op == "route":
+            idx_sorted = torch.sort(self.sets[0]["idx"].to(torch.int64)).values
+            assert torch.equal(idx_sorted, torch.arange(self.p.A, device=self.dev)), "index is not a permutation"
+
+    def check_status(self, stream):
+        m = self.m
+        for s in self.sets:
+            st = m.mrr_v2_read_status(s["ws"].data_ptr(), s["ws"].numel(), stream.cuda_stream)
+            if st != m.MRR_OK:
+                raise RuntimeError(m.mrr_status_str(st))
+
+
+def timed_steps(setup, K, W, stream, dev, dist=None, clocks=None):
+    """W warm-up steps, then exactly K steps between two CUDA events on the launching stream,
+    bracketed by a barrier and a device synchronize on both sides.  The warm-up runs directly
+    before the timed region (nothing idles the GPU or the host in between).  An extra event after
+    the first timed step shows how long that step took from the start of the region.
+    Returns (region ms, first step us)."""
+    import torch
+
+    sets, R, fn, args = setup.sets, setup.R, setup.fn, setup.args
+    h = stream.cuda_stream
+    for k in range(W):
+        setup.launch(sets[k % R], stream)
+    t_begin, t_first, t_end = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    if clocks is not None:
+        clocks.t_start = time.time()
+    # only our launches run on this stream between the two events, back to back
+    t_begin.record(stream)
+    for k in range(K):
+        st = fn(*args[k % R], h)
+        if k == 0:
+            t_first.record(stream)
+        if st != 0:
+            raise RuntimeError(setup.m.mrr_status_str(st))
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    if clocks is not None:
+        clocks.t_end = time.time()
+    if dist is not None:
+        dist.barrier()
+    return t_begin.elapsed_time(t_end), t_begin.elapsed_time(t_first) * 1e3
+
+
+OTHER_CONFIGS = (3, 4, 5)
+
+
 def run_gpu(args):
-    import numpy as np
     import torch
     import workloads
     from moe_expert_token_gb300 import build as mbuild
@@ -338,98 +468,20 @@ def run_gpu(args):
     m.load_library()
 
     p = workloads.config(args.config)
-    code = m.DTYPE_CODES[p.token_dtype]
-    sl = m.SCALE_CODES[p.scale_layout]
-    A, H, N, E = p.A, p.H, p.N, p.E
-    i64 = p.counts.dtype == np.int64
-    if args.op == "route":
-        st, plan = m.mrr_v2_plan(A, H, code, N, E, i64, sl, p.scale_cols, p.topk is not None, 1,
-                                 p.idx_type, local_rank)
-    else:
-        st, plan = m.mrr_v2_unroute_plan(A, H, code, N, E, i64, sl, p.scale_cols, p.topk is not None,
-                                         local_rank)
-    if st != m.MRR_OK:
-        raise SystemExit(m.mrr_status_str(st))
-    launches_per_step = 1 if plan.fuse_scan else 2
-    bytes_step = op_bytes(p, args.op)
-
-    def dev_bytes(arr):
-        if arr is None:
-            return None
-        return torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8).reshape(-1).copy()).to(dev)
-
-    # buffer sets: enough that consecutive steps never hit in L2
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    footprint = bytes_step
-    R = max(2, -(-4 * l2 // footprint))
-    host_in = {"tokens": p.tokens, "counts": p.counts, "scales": p.scales, "topk": p.topk}
-    sets = []
-    for _ in range(R):
-        s = {k: dev_bytes(v) for k, v in host_in.items()}
-        s["out_tokens"] = torch.empty(A * p.row_bytes, dtype=torch.uint8, device=dev)
-        s["out_scales"] = (None if p.scales is None
-                           else torch.empty(A * p.scale_row_bytes, dtype=torch.uint8, device=dev))
-        s["out_topk"] = None if p.topk is None else torch.empty(4 * A, dtype=torch.uint8, device=dev)
-        inv = args.op == "unroute"   # the inverse move writes no index and no per-expert counts
-        s["idx"] = None if inv else torch.empty(A, dtype=torch.int32, device=dev)
-        s["etn"] = None if inv else torch.empty(E * p.counts.dtype.itemsize, dtype=torch.uint8, device=dev)
-        s["ws"] = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
-        sets.append(s)
+    A = p.A
+    setup = RouteSetup(p, args.op, dev, local_rank)
+    plan, sets, R = setup.plan, setup.sets, setup.R
+    bytes_step, launches_per_step = setup.bytes_step, setup.launches_per_step
     stream = torch.cuda.current_stream(dev)
-    sp = stream.cuda_stream
+    setup.gate(stream)
 
-    def P(t):
-        return None if t is None else t.data_ptr()
-
-    def launch(s, on_stream):
-        if args.op == "route":
-            st = m.mrr_v2_run(P(s["tokens"]), code, A, H, P(s["counts"]), i64, N, E, P(s["scales"]), sl,
-                              p.scale_cols, P(s["topk"]), P(s["out_tokens"]), P(s["out_scales"]),
-                              P(s["idx"]), P(s["etn"]), P(s["out_topk"]), 1, p.idx_type, P(s["ws"]),
-                              s["ws"].numel(), on_stream.cuda_stream)
-        else:  # the inverse move: the "tokens" buffers hold the expert-major rows
-            st = m.mrr_v2_unroute(P(s["tokens"]), code, A, H, P(s["counts"]), i64, N, E, P(s["scales"]),
-                                  sl, p.scale_cols, P(s["topk"]), P(s["out_tokens"]), P(s["out_scales"]),
-                                  P(s["out_topk"]), P(s["ws"]), s["ws"].numel(), on_stream.cuda_stream)
-        if st != m.MRR_OK:
-            raise RuntimeError(m.mrr_status_str(st))
-
-    def step(s):
-        launch(s, stream)
-
-    # untimed correctness gate on every buffer set: device status and a permutation check
-    for s in sets:
-        step(s)
-        st = m.mrr_v2_read_status(P(s["ws"]), s["ws"].numel(), sp)
-        if st != m.MRR_OK:
-            raise RuntimeError(m.mrr_status_str(st))
-    if args.op == "route":
-        idx_sorted = torch.sort(sets[0]["idx"].to(torch.int64)).values
-        assert torch.equal(idx_sorted, torch.arange(A, device=dev)), "index is not a permutation"
-
-    for k in range(args.warmup):
-        step(sets[k % R])
     clocks = ClockSampler(local_rank)
     clocks.start()
-    time.sleep(0.3)
+    time.sleep(0.3)          # the sampler's first samples; the warm-up follows right before timing
     K = args.steps
-    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    clocks.t_start = time.time()
-    # only our launches run on this stream between the two events, back to back
-    t_begin.record(stream)
-    for k in range(K):
-        step(sets[k % R])
-    t_end.record(stream)
-    torch.cuda.synchronize(dev)
-    clocks.t_end = time.time()
-    if dist is not None:
-        dist.barrier()
+    local_ms, first_us = timed_steps(setup, K, args.warmup, stream, dev, dist, clocks)
     time.sleep(0.2)
     clocks.stop()
-    local_ms = t_begin.elapsed_time(t_end)
     elapsed_ms = max_over_ranks(local_ms, dist, dev)
     value = throughput_gbs(world, bytes_step, K, elapsed_ms)
     ms_per_step = elapsed_ms / K
@@ -441,16 +493,15 @@ def run_gpu(args):
 
     detail = None
     if not args.no_detail:
-        detail = timing_detail(launch, sets, stream, launches_per_step)
-        for s in sets:   # the graph and unrotated runs left every set valid: check one status
-            st = m.mrr_v2_read_status(P(s["ws"]), s["ws"].numel(), sp)
-            if st != m.MRR_OK:
-                raise RuntimeError(m.mrr_status_str(st))
+        detail = timing_detail(setup.launch, sets, stream, launches_per_step)
+        detail["first_step_us"] = first_us
+        detail["first_step_excess_us"] = first_us - detail["batch_us"]["p50"]
+        setup.check_status(stream)   # the graph and unrotated runs left every set valid
 
     # end to end through the C ABI from pinned host buffers: H2D inputs, run, D2H outputs
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, p, sets, launch, dev, bytes_step, world, dist)
+        e2e = run_e2e(args, p, sets, setup.launch, dev, bytes_step, world, dist)
 
     cpu = cpu_par = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -460,6 +511,31 @@ def run_gpu(args):
         if args.op == "route":
             cpu_par = time_cpu_parallel(p, min(args.cpu_seconds, 10.0))
 
+    # the other large workloads, timed the same way in the same run (parity-tested elsewhere)
+    others = None
+    if args.op == "route" and args.config == 2 and not args.no_other_configs:
+        del setup, sets
+        torch.cuda.empty_cache()
+        others = {}
+        for k in OTHER_CONFIGS:
+            q = workloads.config(k)
+            su = RouteSetup(q, "route", dev, local_rank)
+            su.gate(stream)
+            ms_k, first_k = timed_steps(su, K, args.warmup, stream, dev, dist)
+            ms_k = max_over_ranks(ms_k, dist, dev)
+            gbs_k = throughput_gbs(world, su.bytes_step, K, ms_k)
+            others[f"C{k}"] = {
+                "workload": q.name, "value": gbs_k, "unit": "GB/s", "ms_per_step": ms_k / K,
+                "pct_of_peak": 100.0 * gbs_k / world / peak, "frac": gbs_k / world / peak,
+                "tokens_per_s": world * q.A * K / (ms_k * 1e-3), "bytes_per_step": su.bytes_step,
+                "gpu_launches": K * su.launches_per_step, "first_step_us": first_k,
+                "path": {1: "bulk", 2: "vector"}[su.plan.path], "grid": su.plan.grid,
+                "fused_scan": bool(su.plan.fuse_scan),
+                "traffic": profiled_traffic(k, "route"),
+                "l2": f"{su.R} rotating buffer sets, {su.R * su.bytes_step / 1e6:.0f} MB > 4x L2"}
+            del su
+            torch.cuda.empty_cache()
+
     if rank != 0:
         return 0
     line = {
@@ -468,7 +544,7 @@ def run_gpu(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded numpy draws shaped like the pages' workload)",
         "config": config_dict(p, args.config, op=args.op, extra={
-            "l2": f"{R} rotating buffer sets, {R * footprint / 1e6:.0f} MB > 4x L2 ({l2 / 1e6:.0f} MB)",
+            "l2": f"{R} rotating buffer sets, {R * bytes_step / 1e6:.0f} MB > 4x L2 ({setup_l2(dev) / 1e6:.0f} MB)",
             "path": {1: "bulk", 2: "vector"}[plan.path], "grid": plan.grid, "block": plan.block,
             "chunk_bytes": plan.chunk_bytes, "stages": plan.stages, "fused_scan": bool(plan.fuse_scan),
             "parallelism": f"replicas x{world}"}),
@@ -484,6 +560,7 @@ def run_gpu(args):
         "cpu_parallel": cpu_par,
         "timing_detail": detail,
         "e2e": e2e,
+        "other_configs": others,
         "gpu_launches": K * launches_per_step,
         "clocks": clocks.summary(),
     }
@@ -491,6 +568,12 @@ def run_gpu(args):
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def setup_l2(dev) -> int:
+    import torch
+
+    return torch.cuda.get_device_properties(dev).L2_cache_size
 
 
 def time_cpu_parallel(p, budget_s: float):
@@ -750,11 +833,11 @@ def run_gating(args):
         launch(s, stream)
     if m.mrr_v2_read_status(ws.data_ptr(), ws.numel(), stream.cuda_stream) != m.MRR_OK:
         raise RuntimeError("gating reported a device error")
-    for i in range(args.warmup):
-        launch(sets[i % R], stream)
     clocks = ClockSampler(local_rank)
     clocks.start()
-    time.sleep(0.3)
+    time.sleep(0.3)          # the sampler's first samples; the warm-up follows right before timing
+    for i in range(args.warmup):
+        launch(sets[i % R], stream)
     K = args.steps
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist is not None:

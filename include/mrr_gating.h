@@ -23,11 +23,14 @@
  * least 2 experts.  This implementation handles e <= 1024.  A row holding a NaN logit gets
  * unspecified experts.
  *
- * Whether norm_out is asked for does not change y_out or expert_idx: without it, rows with no
- * bias and no groups are ranked by logit and only the chosen experts are scored, which gives the
- * same float32 scores, the same experts and the same order as scoring every expert wherever the
- * float32 normalisation is monotone across the logits involved (where it is not, the ranking by
- * logit is the one exact arithmetic gives).
+ * Asking for norm_out can change which path scores a row, and so, in rare rows, the result.
+ * Without norm_out, rows with no bias, no groups and no hash table are ranked by their logits
+ * and only the chosen experts are scored; with norm_out every expert is scored and the scores
+ * are ranked.  The two agree (same experts, same order, same y_out bits) wherever CUDA's float32
+ * exp / log1p are monotone across the logits involved.  CUDA does not document them as
+ * monotone, so where two nearly equal logits round the other way round, the experts or their
+ * order may differ between the two modes; the ranking by logit is then the one exact arithmetic
+ * gives.
  */
 #ifndef MRR_GATING_H
 #define MRR_GATING_H

@@ -134,6 +134,12 @@ typedef struct mrr_v2_plan {
     int32_t prefetch_chunks;  /* bulk path: chunks each CTA asks L2 to prefetch while it scans
                                  the counts (its static chunks past the ring first, then its
                                  share of the first counter-served chunks); 0 = none, <= 64   */
+    int64_t epoch;            /* bulk path, sched 1: the tag this launch writes into the
+                                 workspace's chunk counter, 1 .. 2^40 - 1; 0 (what the plan
+                                 functions set) draws a fresh tag for every call.  A fixed tag
+                                 lets a caller (a test) plant a counter value the launch must
+                                 reject: a ticket beyond the launch's last one is reported as
+                                 MRR_ERR_TIMEOUT and the CTAs that drew it stop at once        */
 } mrr_v2_plan_t;
 
 /*

@@ -38,13 +38,15 @@
 
 #include "mrr_v2.h"
 #include "ptx.cuh"
+#include "ws_layout.h"
 
 namespace mrr {
 
-constexpr int kStatusBytes = 4096;                 // status region at the front of the workspace
-constexpr int kStatusWords = kStatusBytes / 4;     // [0] flags, [1] grid, [2 + b] CTA b's flags
-constexpr int kTicketOffset = kStatusBytes;        // 8-byte shared chunk counter (dynamic scheduling)
-constexpr int kHeaderBytes = kStatusBytes + 256;   // status region + counter; offset tables follow
+using mrr_ws::kHeaderBytes;   // status region + counter; offset tables follow
+using mrr_ws::kStatusBytes;   // status region at the front of the workspace
+using mrr_ws::kStatusWords;   // [0] flags, [1] grid, [2 + b] CTA b's flags
+using mrr_ws::kTicketOffset;  // 8-byte shared chunk counter (dynamic scheduling)
+using mrr_ws::padded_len;
 constexpr int kMaxGrid = kStatusWords - 2;
 constexpr int64_t kFusedMaxSegs = 4096;            // N*E scanned inside every CTA up to this
 constexpr int64_t kSmemScanMaxSegs = 16384;        // above kFusedMaxSegs: the scan kernel scans in
@@ -118,7 +120,6 @@ __device__ __forceinline__ int find_seg(const uint32_t *row_ex, int NE, uint32_t
 // Shared-memory index with one padding word per 32: walks with a stride that is a multiple of
 // 32 words (a column of the count matrix) then spread over the banks instead of hitting one.
 __device__ __forceinline__ int pad32(int k) { return k + (k >> 5); }
-__host__ __device__ constexpr int64_t padded_len(int64_t n) { return n + (n >> 5) + 1; }
 
 // The segments of one direction of the move, numbered in the order they sit in the SOURCE.
 //   forward (rank-major -> expert-major): g = q = i*E + j; starts = SrcOffset (row_ex, dense),
@@ -1112,6 +1113,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(const Params p)
         s_flags = 0u;
         s_sum = 0ull;
     }
+    // The wait must stay ahead of launch_dependents: the copy kernel behind this one loads token
+    // rows before its own wait, and only this order makes whatever wrote them finish first.
     grid_dependency_wait();
     grid_launch_dependents();
     if (p.scan_in_smem) {
@@ -1236,9 +1239,9 @@ int token_bits(int dt)
     }
 }
 
-int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+using mrr_ws::round_up;
+using mrr_ws::table_workspace_bytes;
 
-// workspace bytes of the two offset tables for N*E > 4096: SrcOffset dense, DstOffset padded
 // Shared memory of the two tables the copy kernel stages when N*E > 4096 (see reroute_kernel).
 int64_t staged_table_bytes(int64_t NE)
 {
@@ -1249,12 +1252,6 @@ int64_t staged_table_bytes(int64_t NE)
 int64_t scan_smem_bytes(int64_t NE)
 {
     return 4 * (NE + 1 + 2 * padded_len(NE));
-}
-
-int64_t table_workspace_bytes(int64_t NE, int inverse)
-{
-    return round_up(4 * (NE + 1), 256) + round_up(4 * padded_len(NE), 256) +
-           (inverse ? round_up(4 * padded_len(NE), 256) : 0);
 }
 
 int widest_width(uintptr_t a, uintptr_t b, int64_t bytes, int cap)
@@ -1365,7 +1362,9 @@ unsigned long long next_launch_epoch()
 }
 
 constexpr int kNumKernels = 9;
-bool g_smem_attr_set[64][kNumKernels];  // per device: max dynamic smem raised for each kernel
+// per device: the kernel's dynamic shared memory limit has been raised (any host thread may launch;
+// two first launches may both raise it, which is harmless, but the flag itself must not race)
+std::atomic<bool> g_smem_attr_set[64][kNumKernels];
 
 template <bool kBulk, bool kFused, bool kStage>
 int kernel_slot()
@@ -1395,7 +1394,8 @@ cudaError_t launch(K kern, const Params &p, int grid, int block, int smem, cudaS
 cudaError_t launch_scan(const Params &p, int smem, cudaStream_t stream, int device, bool pdl)
 {
     constexpr int slot = 8;
-    if (smem > 48 * 1024 && device >= 0 && device < 64 && !g_smem_attr_set[device][slot]) {
+    if (smem > 48 * 1024 && device >= 0 && device < 64 &&
+        !g_smem_attr_set[device][slot].load(std::memory_order_acquire)) {
         int optin = 0;
         cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
         if (e != cudaSuccess)
@@ -1403,7 +1403,7 @@ cudaError_t launch_scan(const Params &p, int smem, cudaStream_t stream, int devi
         e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - 1024);
         if (e != cudaSuccess)
             return e;
-        g_smem_attr_set[device][slot] = true;
+        g_smem_attr_set[device][slot].store(true, std::memory_order_release);
     }
     return launch(scan_kernel, p, 1, 1024, smem, stream, pdl);
 }
@@ -1413,7 +1413,7 @@ cudaError_t launch_copy(const Params &p, int grid, int block, int smem, cudaStre
 {
     auto kern = reroute_kernel<kBulk, kFused, kStage>;
     const int slot = kernel_slot<kBulk, kFused, kStage>();
-    if (device >= 0 && device < 64 && !g_smem_attr_set[device][slot]) {
+    if (device >= 0 && device < 64 && !g_smem_attr_set[device][slot].load(std::memory_order_acquire)) {
         int optin = 0;
         cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
         if (e != cudaSuccess)
@@ -1421,7 +1421,7 @@ cudaError_t launch_copy(const Params &p, int grid, int block, int smem, cudaStre
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - 1024);
         if (e != cudaSuccess)
             return e;
-        g_smem_attr_set[device][slot] = true;
+        g_smem_attr_set[device][slot].store(true, std::memory_order_release);
     }
     return launch(kern, p, grid, block, smem, stream, pdl);
 }
@@ -1640,6 +1640,8 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
         return MRR_ERR_PLAN;
     if (pl.pdl != 0 && pl.pdl != 1)
         return MRR_ERR_PLAN;
+    if (pl.epoch < 0 || pl.epoch >= (int64_t)(1ull << (64 - kTicketBits)))
+        return MRR_ERR_PLAN;
     int path = pl.path;
     const bool aligned16 = rb % 16 == 0 && ((uintptr_t)tokens % 16) == 0 && ((uintptr_t)permute_tokens % 16) == 0;
     if (path == MRR_PATH_AUTO)
@@ -1733,7 +1735,8 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
     p.prefetch_chunks = path == MRR_PATH_BULK ? pl.prefetch_chunks : 0;
     p.scan_in_smem = scan_in_smem ? 1 : 0;
     p.ticket = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(workspace) + kTicketOffset);
-    p.epoch = (path == MRR_PATH_BULK && pl.sched == 1) ? next_launch_epoch() : 0ull;
+    p.epoch = (path == MRR_PATH_BULK && pl.sched == 1)
+                  ? (pl.epoch ? (unsigned long long)pl.epoch : next_launch_epoch()) : 0ull;
     if (!pl.fuse_scan) {
         uint8_t *ws = static_cast<uint8_t *>(workspace) + kHeaderBytes;
         p.g_row_ex = reinterpret_cast<uint32_t *>(ws);

@@ -18,16 +18,14 @@
 #include <mutex>
 
 #include "mrr_v2.h"
+#include "ws_layout.h"
 
 namespace {
 
-constexpr int64_t kHeaderBytes = 4096 + 256;  // status region and chunk counter of any workspace
-// the two offset tables of mrr_v2_run's workspace: SrcOffset (N*E + 1 words) and DstOffset
-// (one padding word per 32: N*E + N*E/32 + 1 words), each rounded up to 256 bytes
-constexpr int64_t kMaxSegs = MRR_NOALLOC_MAX_SEGMENTS;
-constexpr int64_t kTableBytes = ((4 * (kMaxSegs + 1) + 255) / 256) * 256 +
-                                ((4 * (kMaxSegs + (kMaxSegs >> 5) + 1) + 255) / 256) * 256;
-static_assert(kHeaderBytes + kTableBytes <= MRR_NOALLOC_SCRATCH_BYTES,
+// mrr_v2_run's own workspace layout (status words, chunk counter, and the two forward-direction
+// offset tables above 4096 segments) at the largest N*E this entry point accepts
+static_assert(mrr_ws::kHeaderBytes + mrr_ws::table_workspace_bytes(MRR_NOALLOC_MAX_SEGMENTS, 0) <=
+                  MRR_NOALLOC_SCRATCH_BYTES,
               "the fixed scratch must hold the status words and both offset tables");
 
 // Shared by every call on a device; keeps the last call's contents.

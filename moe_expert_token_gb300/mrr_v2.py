@@ -34,6 +34,8 @@ MRR_ERR_COUNT_SUM = 17
 MRR_ERR_TIMEOUT = 18
 MRR_ERR_INDEX = 19
 MRR_GATE_F16, MRR_GATE_BF16, MRR_GATE_F32 = 0, 1, 2
+MRR_NOALLOC_MAX_SEGMENTS = 16384
+MRR_NOALLOC_SCRATCH_BYTES = 137984
 
 MRR_F16, MRR_BF16, MRR_I8, MRR_F8E5M2, MRR_F8E4M3FN, MRR_HIF8, MRR_F4E2M1, MRR_F4E1M2 = range(8)
 MRR_SCALE_NONE, MRR_SCALE_F32_A, MRR_SCALE_F32_AS, MRR_SCALE_E8M0_AK2 = range(4)
@@ -67,7 +69,7 @@ class mrr_v2_plan_t(ctypes.Structure):
         ("hints", ctypes.c_int32), ("sched", ctypes.c_int32), ("static_chunks", ctypes.c_int32),
         ("pdl", ctypes.c_int32), ("direction", ctypes.c_int32),
         ("smem_bytes", ctypes.c_int32), ("num_sms", ctypes.c_int32),
-        ("prefetch_chunks", ctypes.c_int32),
+        ("prefetch_chunks", ctypes.c_int32), ("epoch", ctypes.c_int64),
     ]
 
     def as_dict(self) -> dict:

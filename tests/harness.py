@@ -88,6 +88,9 @@ def run_gpu(p, *, path: Optional[int] = None, edit: Optional[dict] = None,
     assert st == m.MRR_OK, m.mrr_status_str(st)
     if workspace is None:
         workspace = DevBuf(plan.workspace_bytes, d, 0, fill=0x5A)
+    # device copies of the inputs, compared on the device after the call (any size)
+    in_bufs = [b for b in (tok, cnt, sc, tw) if b is not None]
+    in_copies = [b.t[b.off:b.off + b.n].clone() for b in in_bufs]
     stream = torch.cuda.current_stream(d).cuda_stream
     if path is None and not edit:
         st = m.mrr_v2_run(ptr(tok), code, A, H, ptr(cnt), c.dtype == np.int64, N, E, ptr(sc), sl,
@@ -116,8 +119,7 @@ def run_gpu(p, *, path: Optional[int] = None, edit: Optional[dict] = None,
     out["permute_topk_weight"] = None if out_tw is None else out_tw.host().view(np.float32)
     bufs = [out_tok, out_sc, idx, etn, out_tw]
     out["guards_intact"] = all(b.guards_intact() for b in bufs if b is not None)
-    out["inputs_intact"] = (np.array_equal(tok.host(), np.ascontiguousarray(p.tokens).reshape(-1))
-                            if A * p.row_bytes <= (64 << 20) else True)
+    out["inputs_intact"] = all(torch.equal(b.t[b.off:b.off + b.n], c) for b, c in zip(in_bufs, in_copies))
     return out
 
 

@@ -348,3 +348,52 @@ def test_many_segments(N, E, i64):
     assert_unroute_bit_exact(run_gpu_unroute(p, path=m.MRR_PATH_VECTOR), uref, p)
     # a smaller ring leaves room to stage the tables of 20000 segments on the bulk path too
     assert_bit_exact(run_gpu(p, path=m.MRR_PATH_BULK, edit=dict(chunk_bytes=16384, stages=2)), ref, p)
+
+
+# ------------------------------------------------------------------------------ ordering behind a producer
+
+@pytest.mark.parametrize("N,E", [(16, 16), (80, 64), (128, 128)],
+                         ids=["fused-scan", "scan-kernel-staged", "scan-kernel-16384"])
+def test_inputs_written_by_a_kernel_just_before_the_call(N, E):
+    """The kernels run with programmatic stream serialization.  Behind the scan kernel
+    (N*E > 4096) the copy kernel starts loading token rows before its own dependency wait: that
+    is safe only because the scan kernel waits for its predecessor before it lets the copy kernel
+    start.  Here a torch kernel on the same stream writes the tokens and the counts immediately
+    before the call, and every output must still match the oracle bit for bit."""
+    import torch
+
+    rng = np.random.default_rng(700 + N)
+    p = workloads.make_problem(rng, A=max(40000, 3 * N * E), H=1024, N=N, E=E, token_dtype="bfloat16",
+                               scale_layout="f32_a", scale_cols=1, has_topk=True)
+    ref = oracle.run_problem(p)
+    d = torch.device("cuda:0")
+    key = 0x5A
+    tok_x = torch.from_numpy(p.tokens.reshape(-1) ^ np.uint8(key)).to(d)         # tokens, masked
+    cnt_m1 = torch.from_numpy(p.counts.reshape(-1) - 1).to(d)                     # counts - 1
+    tok = DevBuf(p.A * p.row_bytes, d)
+    cnt = DevBuf(4 * N * E, d)
+    sc, tw = DevBuf.of(p.scales, d), DevBuf.of(p.topk, d)
+    out_tok, out_sc = DevBuf(p.A * p.row_bytes, d), DevBuf(4 * p.A, d)
+    idx, etn, out_tw = DevBuf(4 * p.A, d), DevBuf(4 * E, d), DevBuf(4 * p.A, d)
+    st, plan = m.mrr_v2_plan(p.A, p.H, m.MRR_BF16, N, E, 0, m.MRR_SCALE_F32_A, 1, 1, 1, 0, 0)
+    assert st == m.MRR_OK and plan.pdl == 1 and plan.fuse_scan == int(N * E <= 4096)
+    ws = DevBuf(plan.workspace_bytes, d, fill=0x5A)
+    s = torch.cuda.current_stream(d)
+    for rep in range(3):
+        for b in (tok, cnt, out_tok):                # stale contents the producer must replace
+            b.t.fill_(0xA5)
+        torch.cuda.synchronize(d)
+        # producer kernels, then the op, back to back on one stream with no host sync between
+        torch.bitwise_xor(tok_x, key, out=tok.t[tok.off:tok.off + tok.n])
+        torch.add(cnt_m1, 1, out=cnt.t[cnt.off:cnt.off + cnt.n].view(torch.int32))
+        st = m.mrr_v2_run(tok.ptr, m.MRR_BF16, p.A, p.H, cnt.ptr, 0, N, E, sc.ptr, m.MRR_SCALE_F32_A, 1,
+                          tw.ptr, out_tok.ptr, out_sc.ptr, idx.ptr, etn.ptr, out_tw.ptr, 1, 0, ws.ptr, ws.n,
+                          s.cuda_stream)
+        assert st == m.MRR_OK, m.mrr_status_str(st)
+        assert m.mrr_v2_read_status(ws.ptr, ws.n, s.cuda_stream) == m.MRR_OK
+        assert np.array_equal(out_tok.host().reshape(p.A, -1), ref["permute_tokens"]), rep
+        assert np.array_equal(out_sc.host().reshape(p.A, -1), ref["permute_scales"]), rep
+        assert np.array_equal(idx.host().view(np.int32), ref["permute_token_idx"]), rep
+        assert np.array_equal(etn.host().view(np.int32), ref["expert_token_num"]), rep
+        assert np.array_equal(out_tw.host().view(np.uint32), ref["permute_topk_weight"].view(np.uint32)), rep
+        assert all(b.guards_intact() for b in (out_tok, out_sc, idx, etn, out_tw))

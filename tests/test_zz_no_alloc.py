@@ -7,8 +7,10 @@ them, mrr_v2_run_noalloc uses a fixed array in the library's own device memory a
 
 This test calls it through the C ABI twice in a row, on two different problems.  Both problems
 have more than 4096 segments, so the shared scratch holds the offset tables.  It compares every
-output, bit for bit, with what mrr_v2_run produces from its own workspace.  It also checks the
-segment limit, and the optional wait-and-check status readback.
+output, bit for bit, with what mrr_v2_run produces from its own workspace, and with the CPU
+oracle.  Further cases run at the segment limit (N*E = 16384, both offset tables filling the
+array) and below 4096 segments (only the status words and the chunk counter live in the array);
+it also checks that larger problems are refused, and the optional wait-and-check readback.
 
 The file is named so that pytest collects it last.  It builds and loads everything it needs
 itself, so it also passes when run alone in a fresh process.
@@ -16,6 +18,7 @@ itself, so it also passes when run alone in a fresh process.
 import numpy as np
 import pytest
 
+import oracle
 import workloads
 import moe_expert_token_gb300.mrr_v2 as m
 
@@ -98,6 +101,32 @@ def _same(a, b):
         assert bool((a[k] == b[k]).all().item()), f"{k} differs from mrr_v2_run's output"
 
 
+def _matches_oracle(p, o):
+    """Every output of one call equal to the CPU oracle's, bit for bit."""
+    ref = oracle.run_problem(p)
+    assert np.array_equal(o["tok"].cpu().numpy().reshape(p.A, -1), ref["permute_tokens"])
+    assert np.array_equal(o["idx"].cpu().numpy(), ref["permute_token_idx"])
+    assert np.array_equal(o["etn"].cpu().numpy().view(p.counts.dtype), ref["expert_token_num"])
+    if p.scales is not None:
+        assert np.array_equal(o["sc"].cpu().numpy().reshape(p.A, -1), ref["permute_scales"])
+    if p.topk is not None:
+        assert np.array_equal(o["tw"].cpu().numpy().view(np.uint32),
+                              ref["permute_topk_weight"].view(np.uint32))
+
+
+def _compare_both(p, dev):
+    import torch
+
+    ins, outs = _buffers(p, dev)
+    ref, got = outs(), outs()
+    _run_existing(p, ins, ref, dev)
+    st = _run_noalloc(p, ins, got, dev)
+    assert st == m.MRR_OK, m.mrr_status_str(st)
+    torch.cuda.synchronize(dev)
+    _same(ref, got)
+    _matches_oracle(p, got)
+
+
 def test_noalloc_matches_mrr_v2_run_on_two_calls_in_a_row(dev):
     import torch
 
@@ -111,13 +140,22 @@ def test_noalloc_matches_mrr_v2_run_on_two_calls_in_a_row(dev):
     ]
     for p in problems:
         assert p.N * p.E > 4096      # the offset tables live in the shared scratch
-        ins, outs = _buffers(p, dev)
-        ref, got = outs(), outs()
-        _run_existing(p, ins, ref, dev)
-        st = _run_noalloc(p, ins, got, dev)
-        assert st == m.MRR_OK, m.mrr_status_str(st)
-        torch.cuda.synchronize(dev)
-        _same(ref, got)
+        _compare_both(p, dev)
+
+
+def test_noalloc_at_the_segment_limit_and_below_the_fused_limit(dev):
+    """N*E = 16384 exactly (the bulk path; both tables fill the array), then N*E = 256 (each CTA
+    scans the counts itself; only the status words and the chunk counter are in the array), then
+    the limit case once more on the array the small call left behind."""
+    limit = workloads.make_problem(np.random.default_rng(65), A=40000, H=256, N=128, E=128,
+                                   token_dtype="bfloat16", count_dtype=np.int32,
+                                   scale_layout="f32_a", scale_cols=1, has_topk=True, idx_type=0)
+    assert limit.N * limit.E == m.MRR_NOALLOC_MAX_SEGMENTS
+    small = workloads.make_problem(np.random.default_rng(66), A=50000, H=2048, N=16, E=16,
+                                   token_dtype="int8", count_dtype=np.int64,
+                                   scale_layout="f32_as", scale_cols=3, has_topk=True, idx_type=1)
+    for p in (limit, small, limit):
+        _compare_both(p, dev)
 
 
 def test_noalloc_rejects_too_many_segments(dev):
