@@ -67,7 +67,9 @@ typedef enum mrr_status {
     MRR_ERR_COUNT_NONPOS = 16, /* some counts[i,j] <= 0                                        */
     MRR_ERR_COUNT_SUM = 17,    /* Sum(counts) != A (or a single count > A)                     */
     MRR_ERR_TIMEOUT = 18,      /* a bounded wait inside the copy kernel gave up                */
-    MRR_ERR_INDEX = 19         /* gating top-k: an input_ids / tid2eid value out of range     */
+    MRR_ERR_INDEX = 19,        /* gating top-k: an input_ids / tid2eid value out of range     */
+    MRR_ERR_SOURCE = 20        /* multi-source form: a per-rank source pointer is NULL, or a
+                                  token source is not 16-byte aligned on the bulk path        */
 } mrr_status;
 
 /* Token element types (section 参数说明).  Only the width matters: rows move as bytes.
@@ -206,7 +208,7 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan,
 /*
  * mrr_v2_read_status -- synchronise `stream`, read the status words of the last run that used
  * `workspace`, and return MRR_OK or the device-detected error (MRR_ERR_COUNT_NONPOS,
- * MRR_ERR_COUNT_SUM, MRR_ERR_TIMEOUT), or MRR_ERR_CUDA if the copy back fails.
+ * MRR_ERR_COUNT_SUM, MRR_ERR_TIMEOUT, MRR_ERR_SOURCE), or MRR_ERR_CUDA if the copy back fails.
  * workspace_bytes must be >= 4096.
  */
 mrr_status mrr_v2_read_status(const void *workspace, size_t workspace_bytes, mrr_stream_t stream);
@@ -263,6 +265,60 @@ mrr_status mrr_v2_unroute(const void *permute_tokens, mrr_token_dtype dt, int64_
                           const void *permute_scales, mrr_scale_layout sl, int64_t scale_cols,
                           const float *permute_topk_w, void *tokens, void *scales, float *topk_w,
                           void *workspace, size_t workspace_bytes, mrr_stream_t stream);
+
+/*
+ * mrr_v2_run_multi -- the same move with the received rows still in one buffer per source rank:
+ * the receive side of the expert-parallel dispatch fused with the re-routing.  The dispatch
+ * ("torch_npu.npu_moe_distribute_dispatch" page: expand_x, ep_recv_counts) delivers each peer's
+ * rows, and the V2 article (section 数据流定位 / 在 MoE 网络中的角色) re-lays them out
+ * expert-major.  When the rows land in per-peer receive slots (for example fixed-capacity slots,
+ * or one buffer per peer), this call reads them there directly: rank i's segment (i, j) moves
+ * from its slot to DstOffset(i, j), so the rank-major concatenation is never written and read
+ * again.  The results equal mrr_v2_run on the concatenation of the N buffers in rank order.
+ *   src_tokens   DEVICE array of N device pointers; src_tokens[i] holds rank i's rows, that is
+ *                rows SrcOffset(i, 0) .. SrcOffset(i, 0) + sum_j counts[i, j] - 1 of the
+ *                rank-major order, as [rows_i, H] dt from the pointer on       (read)
+ *   src_scales   DEVICE array of N device pointers to rank i's scale rows in the layout `sl`
+ *                (same row order), or NULL with MRR_SCALE_NONE                 (read)
+ *   src_topk_w   DEVICE array of N device pointers to rank i's [rows_i] float32 top-k weights,
+ *                or NULL; NULL exactly when permute_topk_w is NULL            (read)
+ *   src_rows     DEVICE array [N] int64: the rows rank i's buffers hold (for example the
+ *                capacity of its receive slot), or NULL.  When given, a count matrix whose row
+ *                i sums to more than src_rows[i] is refused (MRR_ERR_SOURCE, nothing moved), so
+ *                counts that arrive over the network can never make the kernel read past a
+ *                buffer.  With NULL the counts are trusted for the buffers' extents.
+ *   every other argument as mrr_v2_run: counts [N, E] in device memory, the five outputs in
+ *   expert-major order, permute_token_idx numbering rows in the rank-major order, the workspace
+ *   of mrr_v2_plan for the same shapes.
+ * The pointer tables live in device memory, so the host cannot check them: the kernels do,
+ * before they read any source, and report MRR_ERR_SOURCE through mrr_v2_read_status (nothing is
+ * then moved) when a pointer is NULL, a rank's rows exceed src_rows, or, on the bulk path (row
+ * bytes a multiple of 16 and a 16-byte aligned permute_tokens), a token pointer is not 16-byte
+ * aligned.  Use
+ * mrr_v2_run_plan_multi with MRR_PATH_VECTOR for token buffers of any alignment.  Scale and
+ * top-k pointers may have any alignment.  The buffers must not overlap the outputs.
+ */
+mrr_status mrr_v2_run_multi(const void *const *src_tokens, const void *const *src_scales,
+                            const float *const *src_topk_w, const int64_t *src_rows,
+                            mrr_token_dtype dt, int64_t A, int64_t H,
+                            const void *counts, int count_is_i64, int64_t N, int64_t E,
+                            mrr_scale_layout sl, int64_t scale_cols,
+                            void *permute_tokens, void *permute_scales, int32_t *permute_token_idx,
+                            void *expert_token_num, float *permute_topk_w,
+                            int64_t expert_token_num_type, int64_t idx_type,
+                            void *workspace, size_t workspace_bytes, mrr_stream_t stream);
+
+/*
+ * mrr_v2_run_plan_multi -- mrr_v2_run_multi with the launch taken from *plan (mrr_v2_plan for
+ * the same shapes, tuning fields possibly edited; direction must be 0).  Same argument rules.
+ */
+mrr_status mrr_v2_run_plan_multi(const mrr_v2_plan_t *plan, const void *const *src_tokens,
+                                 const void *const *src_scales, const float *const *src_topk_w,
+                                 const int64_t *src_rows, mrr_token_dtype dt, const void *counts,
+                                 void *permute_tokens, void *permute_scales, int32_t *permute_token_idx,
+                                 void *expert_token_num, float *permute_topk_w,
+                                 int64_t expert_token_num_type,
+                                 void *workspace, size_t workspace_bytes, mrr_stream_t stream);
 
 /* mrr_status_str -- static, human-readable name of a status code (never NULL). */
 const char *mrr_status_str(mrr_status s);

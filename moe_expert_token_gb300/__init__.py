@@ -9,6 +9,7 @@ from .mrr_v2 import (  # noqa: F401
     load_library,
     moe_re_routing,
     moe_re_routing_inverse,
+    moe_re_routing_multi,
     moe_re_routing_v1,
     moe_gating_top_k,
     mrr_gating_topk_run,
@@ -17,7 +18,9 @@ from .mrr_v2 import (  # noqa: F401
     mrr_v2_plan,
     mrr_v2_read_status,
     mrr_v2_run,
+    mrr_v2_run_multi,
     mrr_v2_run_plan,
+    mrr_v2_run_plan_multi,
     mrr_v2_unroute,
     mrr_v2_unroute_plan,
 )

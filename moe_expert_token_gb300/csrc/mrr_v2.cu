@@ -53,6 +53,7 @@ constexpr int64_t kSmemScanMaxSegs = 16384;        // above kFusedMaxSegs: the s
                                                    // shared memory up to this (about 200 KB)
 constexpr uint32_t kFlagNonPos = 1u, kFlagSum = 2u, kFlagTimeout = 4u;
 constexpr uint32_t kFlagBadIndex = 8u;  // set by the gating kernel (gating.cu)
+constexpr uint32_t kFlagSource = 16u;   // multi-source form: a per-rank pointer is null or misaligned
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // bound on any single mbarrier wait: 2 s
 constexpr int kMaxStages = 8;
 
@@ -90,6 +91,14 @@ struct Params {
     int scan_in_smem;     // N*E > 4096: the scan kernel scans in smem (tables fit in one CTA)
     unsigned long long *ticket;  // sched 1: shared chunk counter in the workspace
     unsigned long long epoch;    // sched 1: this launch's tag for the counter (40 bits, nonzero)
+    // multi-source form (forward move only): rank i's rows sit in their own buffers; tokens,
+    // scales and topk above are then unused.  Each is a device array of N device pointers.
+    int multi;
+    int multi_bulk;                 // multi-source form on the bulk path (token sources 16-aligned)
+    const uint8_t *const *src_tok;  // [N] rank i's token rows (16-byte aligned on the bulk path)
+    const uint8_t *const *src_sc;   // [N] rank i's scale rows, or null without scales
+    const uint8_t *const *src_tk;   // [N] rank i's top-k weights (any alignment), or null
+    const long long *src_rows;      // [N] rows each rank's buffers hold, or null (not checked)
 };
 
 // ------------------------------------------------------------------------------------------------
@@ -159,6 +168,50 @@ __device__ __forceinline__ int64_t dst_row(const SegMap &m, int64_t s)
 {
     const int g = m.find((uint32_t)s);
     return (int64_t)m.dest(g) + (s - (int64_t)m.begin(g));
+}
+
+// Multi-source form (forward map only): the rows of rank i are rows [R(i), R(i+1)) of the
+// rank-major order, R(i) = SrcOffset(i, 0) = row_ex[i*E], R(N) = A; they sit in rank i's own
+// buffer from its start.  For source row s: its destination row, its rank and its row in that
+// rank's buffer.
+__device__ __forceinline__ int64_t dst_row_rank(const SegMap &m, int64_t s, int *rank, int64_t *local)
+{
+    const int g = m.find((uint32_t)s);
+    const int i = g / m.E;
+    *rank = i;
+    *local = s - (int64_t)m.row_ex[i * m.E];
+    return (int64_t)m.dest(g) + (s - (int64_t)m.begin(g));
+}
+
+// Every rank's pointers checked by threads t0, t0 + ts, ...: tokens present and, on the bulk path,
+// 16-byte aligned (the bulk copy engine's rule); scales and top-k weights present when they are
+// moved (any alignment: their copies fall back to narrower accesses).  Returns kFlagSource or 0
+// for this thread's share.
+__device__ __forceinline__ uint32_t check_sources(const Params &p, bool bulk, int t0, int ts)
+{
+    uint32_t f = 0u;
+    for (int i = t0; i < p.N; i += ts) {
+        const uintptr_t t = (uintptr_t)p.src_tok[i];
+        if (!t || (bulk && (t & 15u)))
+            f = kFlagSource;
+        if (p.src_sc && !p.src_sc[i])
+            f = kFlagSource;
+        if (p.src_tk && !p.src_tk[i])
+            f = kFlagSource;
+    }
+    return f;
+}
+
+// Multi-source form with capacities: rank i's rows, R(i+1) - R(i) from the scanned SrcOffset
+// table, must fit the rows its buffers hold.  Threads t0, t0 + ts, ...; kFlagSource or 0.
+__device__ __forceinline__ uint32_t check_capacity(const Params &p, const uint32_t *row_ex, int t0, int ts)
+{
+    uint32_t f = 0u;
+    if (p.src_rows)
+        for (int i = t0; i < p.N; i += ts)
+            if ((long long)(row_ex[(i + 1) * p.E] - row_ex[i * p.E]) > p.src_rows[i])
+                f = kFlagSource;
+    return f;
 }
 
 // Exclusive block-wide scan of one uint32 per thread (warp shuffles + one smem pass).
@@ -461,16 +514,43 @@ struct Vec<1> {
 
 constexpr int kSideBatch = 4;  // rows (or scale vectors) per thread with their loads in flight
 
-// Scale vectors of width W (16, 8 or 4 bytes, both pointers aligned to W) for source rows
-// [r_lo, r_hi): kSideBatch loads in flight per thread, then the stores.
+// W bytes from a source that may be less aligned than W (multi-source form: each rank's buffer has
+// its own alignment), assembled from byte loads.
 template <int W>
+__device__ __forceinline__ typename Vec<W>::T ld_any(const uint8_t *p)
+{
+    if (((uintptr_t)p & (W - 1)) == 0)
+        return Vec<W>::ld(p);
+    uint8_t b[W];
+#pragma unroll
+    for (int i = 0; i < W; ++i)
+        b[i] = __ldg(p + i);
+    typename Vec<W>::T v;
+    memcpy(&v, b, W);
+    return v;
+}
+
+// w bytes (a power of two up to 16) with the widest unit both addresses allow.
+__device__ __forceinline__ void copy_unit_any(uint8_t *d, const uint8_t *s, int w)
+{
+    int u = w;
+    while (u > 1 && (((uintptr_t)d | (uintptr_t)s) & (uintptr_t)(u - 1)))
+        u >>= 1;
+    for (int k = 0; k < w; k += u)
+        copy_unit(d + k, s + k, u);
+}
+
+// Scale vectors of width W (16, 8 or 4 bytes, both pointers aligned to W) for source rows
+// [r_lo, r_hi): kSideBatch loads in flight per thread, then the stores.  Multi-source form: the
+// source row is found in its rank's buffer, which may be less aligned than W.
+template <int W, bool kMulti>
 __device__ void move_scales(const Params &p, const SegMap &m, int64_t r_lo, int64_t r_hi, int t0, int ts)
 {
     const int64_t sb = p.scale_row_bytes, vpr = sb / W;
     const int64_t items = (r_hi - r_lo) * vpr;
     for (int64_t t = t0; t < items; t += (int64_t)ts * kSideBatch) {
         typename Vec<W>::T v[kSideBatch];
-        int64_t s[kSideBatch], off[kSideBatch];
+        int64_t s[kSideBatch], off[kSideBatch], d[kSideBatch];
 #pragma unroll
         for (int u = 0; u < kSideBatch; ++u) {
             const int64_t it = t + (int64_t)u * ts;
@@ -478,14 +558,22 @@ __device__ void move_scales(const Params &p, const SegMap &m, int64_t r_lo, int6
                 const int64_t r = it / vpr;
                 s[u] = r_lo + r;
                 off[u] = (it - r * vpr) * W;
-                v[u] = Vec<W>::ld(p.scales + s[u] * sb + off[u]);
+                if constexpr (kMulti) {
+                    int rk;
+                    int64_t loc;
+                    d[u] = dst_row_rank(m, s[u], &rk, &loc);
+                    v[u] = ld_any<W>(p.src_sc[rk] + loc * sb + off[u]);
+                } else {
+                    v[u] = Vec<W>::ld(p.scales + s[u] * sb + off[u]);
+                }
             }
         }
 #pragma unroll
         for (int u = 0; u < kSideBatch; ++u) {
             if (t + (int64_t)u * ts < items) {
-                const int64_t d = dst_row(m, s[u]);
-                Vec<W>::st(p.out_scales + d * sb + off[u], v[u]);
+                if constexpr (!kMulti)
+                    d[u] = dst_row(m, s[u]);
+                Vec<W>::st(p.out_scales + d[u] * sb + off[u], v[u]);
             }
         }
     }
@@ -493,25 +581,38 @@ __device__ void move_scales(const Params &p, const SegMap &m, int64_t r_lo, int6
 
 // Scale rows, top-k weights and the index for this CTA's share of the SOURCE rows,
 // processed by threads t0, t0 + ts, ... of the block.
+template <bool kMulti>
 __device__ void side_arrays(const Params &p, const SegMap &m, int t0, int ts)
 {
     const int64_t G = gridDim.x, b = blockIdx.x;
     const int64_t r_lo = b * p.A / G, r_hi = (b + 1) * p.A / G;
-    const bool topk4 = p.topk && p.topk_w == 4;
+    const bool topk4 = kMulti ? p.src_tk && p.topk_w == 4 : p.topk && p.topk_w == 4;
     for (int64_t base = r_lo + t0; base < r_hi; base += (int64_t)ts * kSideBatch) {
         uint32_t w[kSideBatch];
+        int64_t dd[kSideBatch], loc[kSideBatch];
+        int rk[kSideBatch];
 #pragma unroll
         for (int u = 0; u < kSideBatch; ++u) {
             const int64_t s = base + (int64_t)u * ts;
-            if (topk4 && s < r_hi)
-                w[u] = __ldg(reinterpret_cast<const uint32_t *>(p.topk) + s);
+            if constexpr (kMulti) {
+                if (s < r_hi) {
+                    dd[u] = dst_row_rank(m, s, &rk[u], &loc[u]);
+                    if (topk4) {
+                        const uint8_t *src = p.src_tk[rk[u]] + loc[u] * 4;
+                        w[u] = ((uintptr_t)src & 3u) ? ld_any<4>(src) : __ldg(reinterpret_cast<const uint32_t *>(src));
+                    }
+                }
+            } else {
+                if (topk4 && s < r_hi)
+                    w[u] = __ldg(reinterpret_cast<const uint32_t *>(p.topk) + s);
+            }
         }
 #pragma unroll
         for (int u = 0; u < kSideBatch; ++u) {
             const int64_t s = base + (int64_t)u * ts;
             if (s >= r_hi)
                 break;
-            const int64_t d = dst_row(m, s);
+            const int64_t d = kMulti ? dd[u] : dst_row(m, s);
             if (p.inverse) {
                 // the inverse move writes no index
             } else if (p.idx_type == 0) {
@@ -519,25 +620,28 @@ __device__ void side_arrays(const Params &p, const SegMap &m, int t0, int ts)
             } else {
                 p.idx[s] = (int32_t)d;  // scatter index: out[idx[s]] = in[s]
             }
-            if (topk4)
+            if (topk4) {
                 reinterpret_cast<uint32_t *>(p.out_topk)[d] = w[u];
-            else if (p.topk) {
+            } else if constexpr (kMulti) {
+                if (p.src_tk)
+                    copy_unit_any(p.out_topk + d * 4, p.src_tk[rk[u]] + loc[u] * 4, 4);
+            } else if (p.topk) {
                 for (int k = 0; k < 4; k += p.topk_w)
                     copy_unit(p.out_topk + d * 4 + k, p.topk + s * 4 + k, p.topk_w);
             }
         }
     }
-    if (!p.scales)
+    if (kMulti ? !p.src_sc : !p.scales)
         return;
     switch (p.scale_w) {
     case 16:
-        move_scales<16>(p, m, r_lo, r_hi, t0, ts);
+        move_scales<16, kMulti>(p, m, r_lo, r_hi, t0, ts);
         break;
     case 8:
-        move_scales<8>(p, m, r_lo, r_hi, t0, ts);
+        move_scales<8, kMulti>(p, m, r_lo, r_hi, t0, ts);
         break;
     case 4:
-        move_scales<4>(p, m, r_lo, r_hi, t0, ts);
+        move_scales<4, kMulti>(p, m, r_lo, r_hi, t0, ts);
         break;
     default: {  // 1- or 2-byte aligned scale rows
         const int w = p.scale_w;
@@ -547,8 +651,15 @@ __device__ void side_arrays(const Params &p, const SegMap &m, int t0, int ts)
             const int64_t r = t / vpr;
             const int64_t v = t - r * vpr;
             const int64_t s = r_lo + r;
-            const int64_t d = dst_row(m, s);
-            copy_unit(p.out_scales + d * sb + v * w, p.scales + s * sb + v * w, w);
+            if constexpr (kMulti) {
+                int rk1;
+                int64_t loc1;
+                const int64_t d = dst_row_rank(m, s, &rk1, &loc1);
+                copy_unit_any(p.out_scales + d * sb + v * w, p.src_sc[rk1] + loc1 * sb + v * w, w);
+            } else {
+                const int64_t d = dst_row(m, s);
+                copy_unit(p.out_scales + d * sb + v * w, p.scales + s * sb + v * w, w);
+            }
         }
     }
     }
@@ -689,7 +800,9 @@ __device__ __forceinline__ void copy_block(uint8_t *dst, const uint8_t *src, int
 // Walk the pieces of source byte range [lo, hi): each piece lies inside one segment, where the
 // destination is the source shifted by (DstOffset - SrcOffset) rows.  Every warp takes its own
 // contiguous sub-range (in 16-byte units), so a CTA has as many pieces in flight as it has warps:
-// a run of small segments is not copied one latency-bound piece at a time.
+// a run of small segments is not copied one latency-bound piece at a time.  Multi-source form:
+// the piece is read from its rank's buffer (segment q belongs to rank q / E).
+template <bool kMulti>
 __device__ void vector_copy(const Params &p, const SegMap &m, int64_t lo, int64_t hi, int tid, int nthr)
 {
     const int nwarps = nthr >> 5, warp = tid >> 5;
@@ -706,15 +819,32 @@ __device__ void vector_copy(const Params &p, const SegMap &m, int64_t lo, int64_
     int q = m.find((uint32_t)(lo / rb));
     int64_t seg_end = (int64_t)m.begin(q + 1) * rb;
     int64_t delta = ((int64_t)m.dest(q) - (int64_t)m.begin(q)) * rb;
+    // multi-source: rank of segment q, the rank's first byte in rank-major order, its buffer
+    int rank = kMulti ? q / m.E : 0;
+    int64_t rank_b0 = 0, rank_b1 = p.total_bytes;
+    const uint8_t *rank_buf = p.tokens;
+    if constexpr (kMulti) {
+        rank_b0 = (int64_t)m.row_ex[rank * m.E] * rb;
+        rank_b1 = (int64_t)m.row_ex[(rank + 1) * m.E] * rb;
+        rank_buf = p.src_tok[rank];
+    }
     for (int64_t pos = lo; pos < hi;) {
         while (pos >= seg_end) {
             ++q;
             seg_end = (int64_t)m.begin(q + 1) * rb;
             delta = ((int64_t)m.dest(q) - (int64_t)m.begin(q)) * rb;
+            if constexpr (kMulti) {
+                if (q == (rank + 1) * m.E) {
+                    ++rank;
+                    rank_b0 = rank_b1;
+                    rank_b1 = (int64_t)m.row_ex[(rank + 1) * m.E] * rb;
+                    rank_buf = p.src_tok[rank];
+                }
+            }
         }
         const int64_t pe = min(hi, seg_end);
-        copy_block(p.out_tokens + pos + delta, p.tokens + pos, pe - pos, p.tokens, p.tokens + p.total_bytes,
-                   tid, nthr);
+        copy_block(p.out_tokens + pos + delta, rank_buf + (pos - rank_b0), pe - pos, rank_buf,
+                   rank_buf + (rank_b1 - rank_b0), tid, nthr);
         pos = pe;
     }
 }
@@ -771,6 +901,10 @@ struct BulkRing {
     int64_t last_claim;            // the launch's last ticket value: tickets + 3 * grid - 1
     int64_t tk_next, tk_end;       // chunk ids of the current ticket not yet served
     int per_ticket;                // consecutive chunks per ticket (about 64 KiB per claim)
+    // multi-source form: the rank whose buffer the last load read, and its byte range in
+    // rank-major order (consecutive chunks mostly come from one rank: one lookup per change)
+    const uint8_t *src_base;
+    int64_t src_b0, src_b1;
 };
 
 // Next chunk of this CTA as the byte range [*b0, *b1); false when the CTA has no more work.
@@ -828,7 +962,12 @@ __device__ bool next_chunk(const Params &p, BulkRing &r, volatile uint32_t *s_fi
     return true;
 }
 
-__device__ __forceinline__ void bulk_issue_load(const Params &p, BulkRing &r, int64_t b0, int64_t b1)
+// Load source bytes [b0, b1) into the next ring stage.  Multi-source form: the range is split
+// where it crosses from one rank's buffer into the next (rank boundaries are whole rows, so every
+// piece stays 16-byte aligned); all pieces complete on the stage's one barrier.
+template <bool kMulti>
+__device__ __forceinline__ void bulk_issue_load(const Params &p, BulkRing &r, const SegMap &m, int64_t b0,
+                                                int64_t b1)
 {
     const int st = (int)(r.issued % p.stages);
     const uint32_t bytes = (uint32_t)(b1 - b0);
@@ -837,13 +976,33 @@ __device__ __forceinline__ void bulk_issue_load(const Params &p, BulkRing &r, in
     r.stage_b0[st] = b0;
     r.stage_b1[st] = b1;
     mbar_arrive_expect_tx(bar, bytes);
-    if (p.hints & MRR_HINT_LOAD_EVICT_FIRST)
-        bulk_g2s_hint(dst, p.tokens + b0, bytes, bar, r.policy);
-    else
-        bulk_g2s(dst, p.tokens + b0, bytes, bar);
+    if constexpr (kMulti) {
+        const int64_t rb = p.row_bytes;
+        for (int64_t x = b0; x < b1;) {
+            if (x < r.src_b0 || x >= r.src_b1) {
+                const int i = m.find((uint32_t)(x / rb)) / m.E;
+                r.src_b0 = (int64_t)m.row_ex[i * m.E] * rb;
+                r.src_b1 = (int64_t)m.row_ex[(i + 1) * m.E] * rb;
+                r.src_base = p.src_tok[i];
+            }
+            const int64_t y = min(b1, r.src_b1);
+            const uint32_t d = dst + (uint32_t)(x - b0), n = (uint32_t)(y - x);
+            if (p.hints & MRR_HINT_LOAD_EVICT_FIRST)
+                bulk_g2s_hint(d, r.src_base + (x - r.src_b0), n, bar, r.policy);
+            else
+                bulk_g2s(d, r.src_base + (x - r.src_b0), n, bar);
+            x = y;
+        }
+    } else {
+        if (p.hints & MRR_HINT_LOAD_EVICT_FIRST)
+            bulk_g2s_hint(dst, p.tokens + b0, bytes, bar, r.policy);
+        else
+            bulk_g2s(dst, p.tokens + b0, bytes, bar);
+    }
     ++r.issued;
 }
 
+template <bool kMulti>
 __device__ uint32_t bulk_driver(const Params &p, BulkRing &r, const SegMap &m, uint32_t flags,
                                 volatile uint32_t *s_first)
 {
@@ -858,7 +1017,7 @@ __device__ uint32_t bulk_driver(const Params &p, BulkRing &r, const SegMap &m, u
         while (more && r.issued < S) {
             more = next_chunk(p, r, s_first, &b0, &b1, &tflag);
             if (more)
-                bulk_issue_load(p, r, b0, b1);
+                bulk_issue_load<kMulti>(p, r, m, b0, b1);
         }
         for (int64_t n = 0; n < r.issued; ++n) {
             const int st = (int)(n % S);
@@ -893,7 +1052,7 @@ __device__ uint32_t bulk_driver(const Params &p, BulkRing &r, const SegMap &m, u
                     bulk_wait_read<1>();
                     waited = true;
                 }
-                bulk_issue_load(p, r, b0, b1);
+                bulk_issue_load<kMulti>(p, r, m, b0, b1);
             }
         }
     }
@@ -909,8 +1068,9 @@ __device__ uint32_t bulk_driver(const Params &p, BulkRing &r, const SegMap &m, u
 
 // kBulk: bulk-copy ring (rows a multiple of 16 bytes) or vector path; kFused: the counts are
 // scanned in every CTA (N*E <= 4096); kStage (N*E > 4096 only): the scan kernel's tables are
-// copied into shared memory first instead of being read from L2.
-template <bool kBulk, bool kFused, bool kStage>
+// copied into shared memory first instead of being read from L2; kMulti: the multi-source form
+// (rank i's rows in a buffer of their own, forward move only).
+template <bool kBulk, bool kFused, bool kStage, bool kMulti>
 __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -941,6 +1101,8 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
     ring.per_ticket = (int)max(1, min(64, 65536 / p.chunk_bytes));
     ring.started = false;
     ring.nch = (p.total_bytes + p.chunk_bytes - 1) / p.chunk_bytes;
+    ring.src_base = nullptr;
+    ring.src_b0 = ring.src_b1 = 0;
     const bool dynamic = kBulk && p.sched == 1;
     if (dynamic) {
         const int64_t span = (int64_t)p.static_chunks * p.chunk_bytes;
@@ -959,6 +1121,12 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
     }
     uint32_t *tab = reinterpret_cast<uint32_t *>(smem + (kBulk ? (size_t)p.stages * p.chunk_bytes : 0));
 
+    SegMap m;
+    m.NE = p.NE;
+    m.N = p.N;
+    m.E = p.E;
+    m.inv = p.inverse;
+
     CountBatch cb;
     if (tid == 0)
         s_first[1] = 0u;
@@ -967,8 +1135,10 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
             mbar_init(smem_addr(&bars[s]), 1u);
         mbar_init_fence();
     }
-    // Start streaming the token rows: their source addresses need no offsets.  Thread 0 fills the
-    // ring with this CTA's first chunks; warp 1 asks L2 for the next ones.
+    // Start streaming the token rows: their source addresses need no offsets (single source).
+    // Thread 0 fills the ring with this CTA's first chunks; warp 1 asks L2 for the next ones.
+    // The multi-source form needs the rank offsets to address its sources, so it starts only once
+    // the segment map is ready and the per-rank pointers have been checked.
     auto start_token_stream = [&]() {
         if (kBulk && tid == 0) {
             if (p.hints)
@@ -976,10 +1146,10 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
             while (ring.issued < p.stages && ring.next < ring.hi) {
                 const int64_t b0 = ring.next, b1 = min(ring.next + p.chunk_bytes, ring.hi);
                 ring.next = b1;
-                bulk_issue_load(p, ring, b0, b1);
+                bulk_issue_load<kMulti>(p, ring, m, b0, b1);
             }
         }
-        if (kBulk && p.prefetch_chunks > 0 && tid >= 32 && tid < 64) {
+        if (!kMulti && kBulk && p.prefetch_chunks > 0 && tid >= 32 && tid < 64) {
             // The ring holds only `stages` chunks, which land long before the offsets are ready.
             // Keep HBM busy meanwhile: warp 1 asks L2 for the next chunks, one per lane -- first
             // this CTA's own static chunks past the ring, then its share of the first chunks the
@@ -1010,7 +1180,7 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
     // runs its own wait before it lets this one start, so whatever wrote the tokens has finished,
     // and it writes only the workspace tables, which are read after the wait.  The fused kernel may
     // follow the tokens' producer directly, so it starts them after the wait.
-    if (!kFused)
+    if (!kFused && !kMulti)
         start_token_stream();
     // When launched behind another kernel with programmatic stream serialization, wait for it
     // here, then let the next launch be scheduled.
@@ -1025,21 +1195,23 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
             issue_count_loads<long long>(p, 0, cb);
         else
             issue_count_loads<int>(p, 0, cb);
-        start_token_stream();
+        if (!kMulti)
+            start_token_stream();
     }
 
     uint32_t flags;
-    SegMap m;
-    m.NE = p.NE;
-    m.N = p.N;
-    m.E = p.E;
-    m.inv = p.inverse;
     if (kFused) {
         uint32_t *rex = tab, *cnt_t = tab + p.NE + 1, *dof = cnt_t + padded_len(p.NE);
         flags = cta_scan(p, cb, rex, cnt_t, dof, s_warp, &s_flags, &s_sum);
         m.row_ex = rex;
         m.dst_off = dof;
         m.col_ex = cnt_t;
+        if constexpr (kMulti) {
+            // every rank's pointers and row count, before any source is read (uniform over the block)
+            const uint32_t f = flags ? 0u : check_sources(p, kBulk, tid, nthr) | check_capacity(p, rex, tid, nthr);
+            if (__syncthreads_or(f != 0u))
+                flags |= kFlagSource;
+        }
         if (b == 0) {
             if (!flags && !p.inverse)
                 write_expert_token_num(p, dof, tid, nthr);
@@ -1050,7 +1222,8 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
         }
     } else {
         __syncthreads();  // s_first[1] cleared before warp 1 may set it
-        flags = *reinterpret_cast<volatile uint32_t *>(p.status);  // written by the scan kernel
+        // written by the scan kernel (its count checks and, multi-source, its pointer checks)
+        flags = *reinterpret_cast<volatile uint32_t *>(p.status);
         m.row_ex = p.g_row_ex;
         m.dst_off = p.g_dst_off;
         m.col_ex = p.g_col_ex;
@@ -1078,22 +1251,24 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
         if (b == 0 && tid == 0)
             p.status[1] = (uint32_t)G;
     }
+    if (kMulti && !flags)
+        start_token_stream();
 
     uint32_t tflag = 0u;
     if (kBulk) {
         if (tid == 0) {
-            tflag = bulk_driver(p, ring, m, flags, s_first);
+            tflag = bulk_driver<kMulti>(p, ring, m, flags, s_first);
         } else if (tid >= 32 && !flags) {
             if (tid == 32 && dynamic && ring.dyn_first >= 0) {
                 s_first[0] = claim_first_ticket(p.ticket, p.epoch, ring.last_claim);
                 __threadfence_block();
                 s_first[1] = 1u;
             }
-            side_arrays(p, m, tid - 32, nthr - 32);
+            side_arrays<kMulti>(p, m, tid - 32, nthr - 32);
         }
     } else if (!flags) {
-        vector_copy(p, m, lo, hi, tid, nthr);
-        side_arrays(p, m, tid, nthr);
+        vector_copy<kMulti>(p, m, lo, hi, tid, nthr);
+        side_arrays<kMulti>(p, m, tid, nthr);
     }
     if (tid == 0)
         p.status[2 + b] = tflag;
@@ -1117,6 +1292,15 @@ __global__ void __launch_bounds__(1024) scan_kernel(const Params p)
     // rows before its own wait, and only this order makes whatever wrote them finish first.
     grid_dependency_wait();
     grid_launch_dependents();
+    if (p.multi) {
+        // the multi-source form's per-rank pointers, checked once here for the copy kernel, which
+        // reads this status word before it touches any source
+        if (__syncthreads_or(check_sources(p, p.multi_bulk != 0, tid, nthr) != 0u)) {
+            if (tid == 0)
+                p.status[0] = kFlagSource;
+            return;
+        }
+    }
     if (p.scan_in_smem) {
         // the same in-CTA scan the fused copy kernel runs, then the tables written out
         uint32_t *rex = sm_tab, *cnt_t = sm_tab + NE + 1, *dof = cnt_t + padded_len(NE);
@@ -1125,7 +1309,9 @@ __global__ void __launch_bounds__(1024) scan_kernel(const Params p)
             issue_count_loads<long long>(p, 0, cb);
         else
             issue_count_loads<int>(p, 0, cb);
-        const uint32_t flags = cta_scan(p, cb, rex, cnt_t, dof, s_warp, &s_flags, &s_sum);
+        uint32_t flags = cta_scan(p, cb, rex, cnt_t, dof, s_warp, &s_flags, &s_sum);
+        if (p.multi && !flags && __syncthreads_or(check_capacity(p, rex, tid, nthr) != 0u))
+            flags = kFlagSource;
         if (flags) {
             if (tid == 0)
                 p.status[0] = flags;
@@ -1188,6 +1374,11 @@ __global__ void __launch_bounds__(1024) scan_kernel(const Params p)
     if (tid == 0)
         p.g_row_ex[NE] = (uint32_t)p.A;
     __syncthreads();  // the row-major starts above, read by position below (inverse move)
+    if (p.multi && __syncthreads_or(check_capacity(p, p.g_row_ex, tid, nthr) != 0u)) {
+        if (tid == 0)
+            p.status[0] = kFlagSource;
+        return;
+    }
     carry = 0u;
     for (int base = 0; base < NE; base += nthr) {
         const int pos = base + tid;
@@ -1361,15 +1552,15 @@ unsigned long long next_launch_epoch()
     }
 }
 
-constexpr int kNumKernels = 9;
+constexpr int kNumKernels = 17;  // 16 copy-kernel variants, then the scan kernel
 // per device: the kernel's dynamic shared memory limit has been raised (any host thread may launch;
 // two first launches may both raise it, which is harmless, but the flag itself must not race)
 std::atomic<bool> g_smem_attr_set[64][kNumKernels];
 
-template <bool kBulk, bool kFused, bool kStage>
+template <bool kBulk, bool kFused, bool kStage, bool kMulti>
 int kernel_slot()
 {
-    return (kBulk ? 4 : 0) + (kFused ? 2 : 0) + (kStage ? 1 : 0);
+    return (kMulti ? 8 : 0) + (kBulk ? 4 : 0) + (kFused ? 2 : 0) + (kStage ? 1 : 0);
 }
 
 // Launch with or without programmatic stream serialization (the kernels wait for their
@@ -1393,7 +1584,7 @@ cudaError_t launch(K kern, const Params &p, int grid, int block, int smem, cudaS
 
 cudaError_t launch_scan(const Params &p, int smem, cudaStream_t stream, int device, bool pdl)
 {
-    constexpr int slot = 8;
+    constexpr int slot = 16;
     if (smem > 48 * 1024 && device >= 0 && device < 64 &&
         !g_smem_attr_set[device][slot].load(std::memory_order_acquire)) {
         int optin = 0;
@@ -1408,11 +1599,11 @@ cudaError_t launch_scan(const Params &p, int smem, cudaStream_t stream, int devi
     return launch(scan_kernel, p, 1, 1024, smem, stream, pdl);
 }
 
-template <bool kBulk, bool kFused, bool kStage>
+template <bool kBulk, bool kFused, bool kStage, bool kMulti>
 cudaError_t launch_copy(const Params &p, int grid, int block, int smem, cudaStream_t stream, int device, bool pdl)
 {
-    auto kern = reroute_kernel<kBulk, kFused, kStage>;
-    const int slot = kernel_slot<kBulk, kFused, kStage>();
+    auto kern = reroute_kernel<kBulk, kFused, kStage, kMulti>;
+    const int slot = kernel_slot<kBulk, kFused, kStage, kMulti>();
     if (device >= 0 && device < 64 && !g_smem_attr_set[device][slot].load(std::memory_order_acquire)) {
         int optin = 0;
         cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
@@ -1463,6 +1654,8 @@ const char *mrr_status_str(mrr_status s)
         return "MRR_ERR_TIMEOUT: a bounded wait in the copy kernel gave up";
     case MRR_ERR_INDEX:
         return "MRR_ERR_INDEX: an input_ids or tid2eid value is out of range";
+    case MRR_ERR_SOURCE:
+        return "MRR_ERR_SOURCE: a per-rank source pointer is NULL, or not 16-byte aligned on the bulk path";
     }
     return "unknown mrr_status";
 }
@@ -1572,30 +1765,35 @@ mrr_status make_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int64_
     return MRR_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-mrr_status mrr_v2_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int64_t E, int count_is_i64,
-                       mrr_scale_layout sl, int64_t scale_cols, int has_topk, int64_t expert_token_num_type,
-                       int64_t idx_type, int device, mrr_v2_plan_t *out)
+// The copy-kernel variant for a path, scan placement and table staging.
+template <bool kMulti>
+cudaError_t launch_variant(bool bulk, bool fused, bool stage, const Params &p, int grid, int block, int sm,
+                           cudaStream_t stream, int device, bool pdl)
 {
-    return make_plan(A, H, dt, N, E, count_is_i64, sl, scale_cols, has_topk, expert_token_num_type, idx_type,
-                     device, 0, out);
+    if (bulk)
+        return fused   ? launch_copy<true, true, false, kMulti>(p, grid, block, sm, stream, device, pdl)
+               : stage ? launch_copy<true, false, true, kMulti>(p, grid, block, sm, stream, device, pdl)
+                       : launch_copy<true, false, false, kMulti>(p, grid, block, sm, stream, device, pdl);
+    return fused   ? launch_copy<false, true, false, kMulti>(p, grid, block, sm, stream, device, pdl)
+           : stage ? launch_copy<false, false, true, kMulti>(p, grid, block, sm, stream, device, pdl)
+                   : launch_copy<false, false, false, kMulti>(p, grid, block, sm, stream, device, pdl);
 }
 
-mrr_status mrr_v2_unroute_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int64_t E, int count_is_i64,
-                               mrr_scale_layout sl, int64_t scale_cols, int has_topk, int device,
-                               mrr_v2_plan_t *out)
-{
-    return make_plan(A, H, dt, N, E, count_is_i64, sl, scale_cols, has_topk, 1, 0, device, 1, out);
-}
+// The per-rank source tables of the multi-source form (device arrays of N device pointers).
+struct MultiSrc {
+    const void *const *tokens;
+    const void *const *scales;
+    const float *const *topk;
+    const int64_t *rows;
+};
 
-mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_token_dtype dt, const void *counts,
-                           const void *scales, const float *topk_w, void *permute_tokens, void *permute_scales,
-                           int32_t *permute_token_idx, void *expert_token_num, float *permute_topk_w,
-                           int64_t expert_token_num_type, void *workspace, size_t workspace_bytes,
-                           mrr_stream_t stream_)
+// mrr_v2_run_plan, and with ms != NULL its multi-source form: tokens / scales / topk_w are then
+// unused and each rank's rows come from ms's tables.
+mrr_status run_plan_impl(const mrr_v2_plan_t *plan, const MultiSrc *ms, const void *tokens, mrr_token_dtype dt,
+                         const void *counts, const void *scales, const float *topk_w, void *permute_tokens,
+                         void *permute_scales, int32_t *permute_token_idx, void *expert_token_num,
+                         float *permute_topk_w, int64_t expert_token_num_type, void *workspace,
+                         size_t workspace_bytes, mrr_stream_t stream_)
 {
     if (!plan)
         return MRR_ERR_NULL;
@@ -1615,8 +1813,17 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
         return MRR_ERR_PLAN;
     const int inverse = pl.direction;
     if (inverse) {
+        if (ms)
+            return MRR_ERR_PLAN;  // the multi-source form is the forward move only
         permute_token_idx = nullptr;
         expert_token_num = nullptr;
+    }
+    if (ms) {
+        // the tables stand in for the buffers in the checks below; each rank's own pointers are
+        // checked on the device (they live in device memory)
+        tokens = ms->tokens;
+        scales = ms->scales;
+        topk_w = reinterpret_cast<const float *>(ms->topk);
     }
 
     st = check_buffers(NE, E, cb, pl.scale_layout, tokens, counts, scales, topk_w, permute_tokens, permute_scales,
@@ -1643,7 +1850,9 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
     if (pl.epoch < 0 || pl.epoch >= (int64_t)(1ull << (64 - kTicketBits)))
         return MRR_ERR_PLAN;
     int path = pl.path;
-    const bool aligned16 = rb % 16 == 0 && ((uintptr_t)tokens % 16) == 0 && ((uintptr_t)permute_tokens % 16) == 0;
+    // (multi-source: the sources' alignment is checked on the device, MRR_ERR_SOURCE)
+    const bool aligned16 = rb % 16 == 0 && (ms || ((uintptr_t)tokens % 16) == 0) &&
+                           ((uintptr_t)permute_tokens % 16) == 0;
     if (path == MRR_PATH_AUTO)
         path = aligned16 ? MRR_PATH_BULK : MRR_PATH_VECTOR;
     if (path == MRR_PATH_BULK && !aligned16)
@@ -1717,10 +1926,14 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
     p.scales = static_cast<const uint8_t *>(scales);
     p.out_scales = scales ? static_cast<uint8_t *>(permute_scales) : nullptr;
     p.scale_row_bytes = sb;
-    p.scale_w = scales ? widest_width((uintptr_t)scales, (uintptr_t)permute_scales, sb, 16) : 1;
+    // vector widths of the side arrays: both pointers aligned to them (multi-source: the output
+    // alone; a less aligned rank buffer is read with narrower loads)
+    const uintptr_t sc_src = ms ? (uintptr_t)permute_scales : (uintptr_t)scales;
+    const uintptr_t tk_src = ms ? (uintptr_t)permute_topk_w : (uintptr_t)topk_w;
+    p.scale_w = scales ? widest_width(sc_src, (uintptr_t)permute_scales, sb, 16) : 1;
     p.topk = reinterpret_cast<const uint8_t *>(topk_w);
     p.out_topk = reinterpret_cast<uint8_t *>(permute_topk_w);
-    p.topk_w = topk_w ? widest_width((uintptr_t)topk_w, (uintptr_t)permute_topk_w, 4, 4) : 4;
+    p.topk_w = topk_w ? widest_width(tk_src, (uintptr_t)permute_topk_w, 4, 4) : 4;
     p.idx = permute_token_idx;
     p.idx_type = pl.idx_type;
     p.etn = expert_token_num;
@@ -1734,6 +1947,18 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
     p.static_chunks = pl.static_chunks;
     p.prefetch_chunks = path == MRR_PATH_BULK ? pl.prefetch_chunks : 0;
     p.scan_in_smem = scan_in_smem ? 1 : 0;
+    if (ms) {
+        p.multi = 1;
+        p.multi_bulk = path == MRR_PATH_BULK ? 1 : 0;
+        p.src_tok = reinterpret_cast<const uint8_t *const *>(ms->tokens);
+        p.src_sc = reinterpret_cast<const uint8_t *const *>(ms->scales);
+        p.src_tk = reinterpret_cast<const uint8_t *const *>(ms->topk);
+        p.src_rows = reinterpret_cast<const long long *>(ms->rows);
+        p.tokens = nullptr;
+        p.scales = nullptr;
+        p.topk = nullptr;
+        p.prefetch_chunks = 0;
+    }
     p.ticket = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(workspace) + kTicketOffset);
     p.epoch = (path == MRR_PATH_BULK && pl.sched == 1)
                   ? (pl.epoch ? (unsigned long long)pl.epoch : next_launch_epoch()) : 0ull;
@@ -1752,20 +1977,104 @@ mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_to
         e = launch_scan(p, scan_in_smem ? (int)scan_smem_bytes(NE) : 0, stream, device, pdl);
     if (e == cudaSuccess) {
         const int grid = pl.grid, block = pl.block, sm = (int)smem;
-        if (path == MRR_PATH_BULK)
-            e = pl.fuse_scan      ? launch_copy<true, true, false>(p, grid, block, sm, stream, device, pdl)
-                : stage_tables    ? launch_copy<true, false, true>(p, grid, block, sm, stream, device, pdl)
-                                  : launch_copy<true, false, false>(p, grid, block, sm, stream, device, pdl);
+        if (ms)
+            e = launch_variant<true>(path == MRR_PATH_BULK, pl.fuse_scan != 0, stage_tables, p, grid, block, sm,
+                                     stream, device, pdl);
         else
-            e = pl.fuse_scan      ? launch_copy<false, true, false>(p, grid, block, sm, stream, device, pdl)
-                : stage_tables    ? launch_copy<false, false, true>(p, grid, block, sm, stream, device, pdl)
-                                  : launch_copy<false, false, false>(p, grid, block, sm, stream, device, pdl);
+            e = launch_variant<false>(path == MRR_PATH_BULK, pl.fuse_scan != 0, stage_tables, p, grid, block, sm,
+                                      stream, device, pdl);
     }
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return MRR_ERR_CUDA;
     }
     return MRR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mrr_status mrr_v2_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int64_t E, int count_is_i64,
+                       mrr_scale_layout sl, int64_t scale_cols, int has_topk, int64_t expert_token_num_type,
+                       int64_t idx_type, int device, mrr_v2_plan_t *out)
+{
+    return make_plan(A, H, dt, N, E, count_is_i64, sl, scale_cols, has_topk, expert_token_num_type, idx_type,
+                     device, 0, out);
+}
+
+mrr_status mrr_v2_unroute_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int64_t E, int count_is_i64,
+                               mrr_scale_layout sl, int64_t scale_cols, int has_topk, int device,
+                               mrr_v2_plan_t *out)
+{
+    return make_plan(A, H, dt, N, E, count_is_i64, sl, scale_cols, has_topk, 1, 0, device, 1, out);
+}
+
+mrr_status mrr_v2_run_plan(const mrr_v2_plan_t *plan, const void *tokens, mrr_token_dtype dt, const void *counts,
+                           const void *scales, const float *topk_w, void *permute_tokens, void *permute_scales,
+                           int32_t *permute_token_idx, void *expert_token_num, float *permute_topk_w,
+                           int64_t expert_token_num_type, void *workspace, size_t workspace_bytes,
+                           mrr_stream_t stream)
+{
+    return run_plan_impl(plan, nullptr, tokens, dt, counts, scales, topk_w, permute_tokens, permute_scales,
+                         permute_token_idx, expert_token_num, permute_topk_w, expert_token_num_type, workspace,
+                         workspace_bytes, stream);
+}
+
+mrr_status mrr_v2_run_plan_multi(const mrr_v2_plan_t *plan, const void *const *src_tokens,
+                                 const void *const *src_scales, const float *const *src_topk_w,
+                                 const int64_t *src_rows, mrr_token_dtype dt, const void *counts,
+                                 void *permute_tokens, void *permute_scales, int32_t *permute_token_idx,
+                                 void *expert_token_num, float *permute_topk_w, int64_t expert_token_num_type,
+                                 void *workspace, size_t workspace_bytes, mrr_stream_t stream)
+{
+    if (!src_tokens)
+        return MRR_ERR_NULL;
+    if ((uintptr_t)src_rows % 8)
+        return MRR_ERR_ALIGN;
+    const MultiSrc ms = {src_tokens, src_scales, src_topk_w, src_rows};
+    return run_plan_impl(plan, &ms, nullptr, dt, counts, nullptr, nullptr, permute_tokens, permute_scales,
+                         permute_token_idx, expert_token_num, permute_topk_w, expert_token_num_type, workspace,
+                         workspace_bytes, stream);
+}
+
+mrr_status mrr_v2_run_multi(const void *const *src_tokens, const void *const *src_scales,
+                            const float *const *src_topk_w, const int64_t *src_rows, mrr_token_dtype dt,
+                            int64_t A, int64_t H,
+                            const void *counts, int count_is_i64, int64_t N, int64_t E, mrr_scale_layout sl,
+                            int64_t scale_cols, void *permute_tokens, void *permute_scales,
+                            int32_t *permute_token_idx, void *expert_token_num, float *permute_topk_w,
+                            int64_t expert_token_num_type, int64_t idx_type, void *workspace,
+                            size_t workspace_bytes, mrr_stream_t stream)
+{
+    int64_t rb = 0, sb = 0;
+    mrr_status st = check_shape(A, H, (int)dt, N, E, count_is_i64, (int)sl, scale_cols, expert_token_num_type,
+                                idx_type, &rb, &sb);
+    if (st != MRR_OK)
+        return st;
+    if (!src_tokens)
+        return MRR_ERR_NULL;
+    if (sl == MRR_SCALE_NONE)
+        src_scales = nullptr;  // "meaningless" output: nothing is read or written
+    st = check_buffers(N * E, E, count_is_i64 ? 8 : 4, (int)sl, src_tokens, counts, src_scales, src_topk_w,
+                       permute_tokens, permute_scales, permute_token_idx, expert_token_num, permute_topk_w,
+                       workspace, workspace_bytes);
+    if (st != MRR_OK)
+        return st;
+    int device = -1;
+    if (cudaGetDevice(&device) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return MRR_ERR_CUDA;
+    }
+    mrr_v2_plan_t plan;
+    st = mrr_v2_plan(A, H, dt, N, E, count_is_i64, sl, scale_cols, src_topk_w != nullptr, expert_token_num_type,
+                     idx_type, device, &plan);
+    if (st != MRR_OK)
+        return st;
+    plan.path = MRR_PATH_AUTO;
+    return mrr_v2_run_plan_multi(&plan, src_tokens, src_scales, src_topk_w, src_rows, dt, counts, permute_tokens,
+                                 permute_scales, permute_token_idx, expert_token_num, permute_topk_w,
+                                 expert_token_num_type, workspace, workspace_bytes, stream);
 }
 
 mrr_status mrr_v2_run(const void *tokens, mrr_token_dtype dt, int64_t A, int64_t H, const void *counts,
@@ -1880,6 +2189,8 @@ mrr_status mrr_v2_read_status(const void *workspace, size_t workspace_bytes, mrr
         return MRR_ERR_TIMEOUT;
     if (flags & kFlagBadIndex)
         return MRR_ERR_INDEX;
+    if (flags & kFlagSource)
+        return MRR_ERR_SOURCE;
     return MRR_OK;
 }
 

@@ -33,6 +33,7 @@ MRR_ERR_COUNT_NONPOS = 16
 MRR_ERR_COUNT_SUM = 17
 MRR_ERR_TIMEOUT = 18
 MRR_ERR_INDEX = 19
+MRR_ERR_SOURCE = 20
 MRR_GATE_F16, MRR_GATE_BF16, MRR_GATE_F32 = 0, 1, 2
 MRR_NOALLOC_MAX_SEGMENTS = 16384
 MRR_NOALLOC_SCRATCH_BYTES = 137984
@@ -123,6 +124,12 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.mrr_gating_topk_run.argtypes = [P, I32, I64, I64, I64, P, P, P, I64, P, P, I64, I64,
                                         ctypes.c_float, ctypes.c_float, I64, I64, I64, P, P, P, P,
                                         ctypes.c_size_t, P]
+    lib.mrr_v2_run_multi.restype = I32
+    lib.mrr_v2_run_multi.argtypes = [P, P, P, P, I32, I64, I64, P, I32, I64, I64, I32, I64,
+                                     P, P, P, P, P, I64, I64, P, ctypes.c_size_t, P]
+    lib.mrr_v2_run_plan_multi.restype = I32
+    lib.mrr_v2_run_plan_multi.argtypes = [ctypes.POINTER(mrr_v2_plan_t), P, P, P, P, I32, P,
+                                          P, P, P, P, P, I64, P, ctypes.c_size_t, P]
     lib.mrr_v2_run_noalloc.restype = I32
     lib.mrr_v2_run_noalloc.argtypes = [P, I32, I64, I64, P, I32, I64, I64, P, I32, I64, P,
                                        P, P, P, P, P, I64, I64, I32, P]
@@ -202,6 +209,28 @@ def mrr_v2_unroute(permute_tokens, dt, A, H, counts, count_is_i64, N, E, permute
     return load_library().mrr_v2_unroute(
         permute_tokens, dt, A, H, counts, int(count_is_i64), N, E, permute_scales, sl, scale_cols,
         permute_topk_w, tokens, scales, topk_w, workspace, workspace_bytes, stream)
+
+
+def mrr_v2_run_multi(src_tokens, src_scales, src_topk_w, src_rows, dt, A, H, counts, count_is_i64,
+                     N, E, sl, scale_cols, permute_tokens, permute_scales, permute_token_idx,
+                     expert_token_num, permute_topk_w, expert_token_num_type, idx_type, workspace,
+                     workspace_bytes, stream) -> int:
+    """The multi-source form: src_tokens / src_scales / src_topk_w / src_rows are device
+    addresses of [N] tables (pointers, pointers, pointers, int64 rows), or None."""
+    return load_library().mrr_v2_run_multi(
+        src_tokens, src_scales, src_topk_w, src_rows, dt, A, H, counts, int(count_is_i64), N, E, sl,
+        scale_cols, permute_tokens, permute_scales, permute_token_idx, expert_token_num,
+        permute_topk_w, expert_token_num_type, idx_type, workspace, workspace_bytes, stream)
+
+
+def mrr_v2_run_plan_multi(plan: mrr_v2_plan_t, src_tokens, src_scales, src_topk_w, src_rows, dt,
+                          counts, permute_tokens, permute_scales, permute_token_idx,
+                          expert_token_num, permute_topk_w, expert_token_num_type, workspace,
+                          workspace_bytes, stream) -> int:
+    return load_library().mrr_v2_run_plan_multi(
+        ctypes.byref(plan), src_tokens, src_scales, src_topk_w, src_rows, dt, counts,
+        permute_tokens, permute_scales, permute_token_idx, expert_token_num, permute_topk_w,
+        expert_token_num_type, workspace, workspace_bytes, stream)
 
 
 def mrr_v2_read_status(workspace, workspace_bytes, stream) -> int:
@@ -324,6 +353,96 @@ def moe_re_routing(tokens, expert_token_num_per_rank, *, per_token_scales=None,
                         workspace.numel(), stream.cuda_stream)
         if st != MRR_OK:
             raise MrrError(st, "mrr_v2_run")
+        if check_status:
+            st = mrr_v2_read_status(workspace.data_ptr(), workspace.numel(), stream.cuda_stream)
+            if st != MRR_OK:
+                raise MrrError(st, "device")
+    return out_tok, out_sc, idx, etn, out_tw
+
+
+def moe_re_routing_multi(tokens_per_rank, expert_token_num_per_rank, *, per_token_scales=None,
+                         expert_topk_weight=None, expert_token_num_type: int = 1, idx_type: int = 0,
+                         tokens_dtype: Optional[str] = None, workspace=None, stream=None,
+                         check_status: bool = False):
+    """``moe_re_routing`` with the received rows still in one tensor per source rank.
+
+    ``tokens_per_rank[i]`` is a [rows_i, H] tensor holding rank i's rows (the rows row i of the
+    count matrix describes), and so are the optional per-rank lists ``per_token_scales`` and
+    ``expert_topk_weight`` ([rows_i, 1] float32).  The outputs equal ``moe_re_routing`` on the
+    concatenation of the lists; each rank's capacity (rows_i) is passed along, so counts that do
+    not fit a rank's tensor raise instead of reading past it (with ``check_status=True``)."""
+    import torch
+
+    ts, c = list(tokens_per_rank), expert_token_num_per_rank
+    if c.dim() != 2 or len(ts) != c.shape[0]:
+        raise ValueError("one tokens tensor per row of expert_token_num_per_rank")
+    if c.dtype not in (torch.int32, torch.int64):
+        raise TypeError("expert_token_num_per_rank must be int32 or int64")
+    dev = c.device
+    N, E = c.shape
+    code, H = _torch_token_code(ts[0], tokens_dtype)
+    lists = [ts, per_token_scales, expert_topk_weight]
+    if any(lst is not None and len(lst) != N for lst in lists):
+        raise ValueError("every per-rank list needs one tensor per rank")
+    for i, t in enumerate(ts):
+        if t.dim() != 2 or t.dtype != ts[0].dtype or _torch_token_code(t, tokens_dtype)[1] != H:
+            raise ValueError("per-rank token tensors must be [rows_i, H] of one dtype")
+        if not t.is_cuda or t.device != dev or not t.is_contiguous():
+            raise ValueError("per-rank tensors must be contiguous CUDA tensors on the counts' device")
+        for lst in lists[1:]:
+            if lst is not None and (lst[i].shape[0] != t.shape[0] or lst[i].device != dev
+                                    or not lst[i].is_contiguous()):
+                raise ValueError("rank %d: scales / top-k weights must match its token rows" % i)
+    A = sum(int(t.shape[0]) for t in ts)
+    sl, scale_cols = _scale_layout(None if per_token_scales is None else per_token_scales[0])
+    if per_token_scales is not None and any(_scale_layout(x) != (sl, scale_cols) for x in per_token_scales):
+        raise ValueError("per-rank scales must share one layout")
+    if expert_topk_weight is not None and any(x.dtype != torch.float32 or x.dim() != 2 or x.shape[1] != 1
+                                              for x in expert_topk_weight):
+        raise ValueError("expert_topk_weight entries must be float32 [rows_i, 1]")
+
+    st, plan = mrr_v2_plan(A, H, code, N, E, c.dtype == torch.int64, sl, scale_cols,
+                           expert_topk_weight is not None, expert_token_num_type, idx_type,
+                           dev.index if dev.index is not None else torch.cuda.current_device())
+    if st != MRR_OK:
+        raise MrrError(st, "mrr_v2_plan")
+
+    def table(lst):   # a device array of the tensors' addresses
+        if lst is None:
+            return None
+        return torch.tensor([x.data_ptr() for x in lst], dtype=torch.int64, device=dev)
+
+    t_tok, t_sc, t_tw = table(ts), table(per_token_scales), table(expert_topk_weight)
+    rows = torch.tensor([int(t.shape[0]) for t in ts], dtype=torch.int64, device=dev)
+    out_tok = torch.empty((A,) + tuple(ts[0].shape[1:]), dtype=ts[0].dtype, device=dev)
+    out_sc = (torch.empty((A,) + tuple(per_token_scales[0].shape[1:]), dtype=per_token_scales[0].dtype,
+                          device=dev)
+              if per_token_scales is not None else torch.empty(A, dtype=torch.float32, device=dev))
+    idx = torch.empty(A, dtype=torch.int32, device=dev)
+    etn = torch.empty(E, dtype=c.dtype, device=dev)
+    out_tw = (torch.empty(A, 1, dtype=torch.float32, device=dev) if expert_topk_weight is not None
+              else torch.empty(0, dtype=torch.float32, device=dev))
+    if workspace is None or workspace.numel() < plan.workspace_bytes:
+        workspace = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+
+    def ptr(x):
+        return None if x is None else x.data_ptr()
+
+    with torch.cuda.device(dev):
+        st = mrr_v2_run_multi(ptr(t_tok), ptr(t_sc), ptr(t_tw), ptr(rows), code, A, H, ptr(c),
+                              c.dtype == torch.int64, N, E, sl, scale_cols, ptr(out_tok),
+                              ptr(out_sc) if per_token_scales is not None else None, ptr(idx), ptr(etn),
+                              ptr(out_tw) if expert_topk_weight is not None else None,
+                              expert_token_num_type, idx_type, workspace.data_ptr(), workspace.numel(),
+                              stream.cuda_stream)
+        if st != MRR_OK:
+            raise MrrError(st, "mrr_v2_run_multi")
+        # the tables must outlive the enqueued work: keep them with the stream's pending work
+        for x in (t_tok, t_sc, t_tw, rows):
+            if x is not None:
+                x.record_stream(stream)
         if check_status:
             st = mrr_v2_read_status(workspace.data_ptr(), workspace.numel(), stream.cuda_stream)
             if st != MRR_OK:

@@ -26,7 +26,8 @@ def test_exports_every_header_function(lib):
     names = m.header_functions()
     assert set(names) == {"mrr_v2_plan", "mrr_v2_run", "mrr_v2_run_plan", "mrr_v2_read_status",
                           "mrr_status_str", "mrr_v2_run_noalloc", "mrr_v2_unroute_plan",
-                          "mrr_v2_unroute", "mrr_v1_run", "mrr_gating_topk_run"}
+                          "mrr_v2_unroute", "mrr_v1_run", "mrr_gating_topk_run", "mrr_v2_run_multi",
+                          "mrr_v2_run_plan_multi"}
     out = subprocess.run(["nm", "-D", "--defined-only", m.library_path()], capture_output=True,
                          text=True, check=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
@@ -43,7 +44,7 @@ def test_library_is_built_for_sm103a_only():
 
 
 def test_status_strings(lib):
-    for code in list(range(0, 11)) + [16, 17, 18, 19]:
+    for code in list(range(0, 11)) + [16, 17, 18, 19, 20]:
         s = m.mrr_status_str(code)
         assert s.startswith("MRR_"), (code, s)
     assert m.mrr_status_str(12345) == "unknown mrr_status"
