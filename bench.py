@@ -45,8 +45,9 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", type=int, default=2, help="workload 1..5 (2 is the headline)")
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--op", choices=["route", "unroute", "gating"], default="route",
+    ap.add_argument("--op", choices=["route", "unroute", "multi", "gating"], default="route",
                     help="route: rank-major -> expert-major (the op); unroute: the inverse move; "
+                         "multi: the op reading each source rank's rows from a buffer of its own; "
                          "gating: the upstream gating top-k op (--config 1, 2 or 3)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU oracle baseline budget (seconds of oracle work)")
@@ -102,7 +103,8 @@ def kernel_source_hash() -> str:
 
 def profiled_traffic(config: int, op: str = "route"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
-    name = f"reroute_kernel_C{config}.md" if op == "route" else f"reroute_kernel_inverse_C{config}.md"
+    name = {"route": f"reroute_kernel_C{config}.md", "unroute": f"reroute_kernel_inverse_C{config}.md",
+            "multi": f"reroute_kernel_multi_C{config}.md"}[op]
     path = os.path.join(ROOT, "profiles", name)
     try:
         text = open(path, encoding="utf-8").read()
@@ -233,8 +235,9 @@ def row_sample(p, frac: float):
 
 
 def op_bytes(p, op: str) -> int:
-    """Algorithmic bytes of one step.  The inverse move writes no index and no per-expert counts."""
-    if op == "route":
+    """Algorithmic bytes of one step.  The inverse move writes no index and no per-expert counts;
+    the multi-source form moves the same bytes as the op (plus N pointers per table, not counted)."""
+    if op in ("route", "multi"):
         return p.algorithmic_bytes()
     return p.algorithmic_bytes() - 4 * p.A - p.E * p.counts.dtype.itemsize
 
@@ -242,7 +245,7 @@ def op_bytes(p, op: str) -> int:
 def oracle_step(p, op: str, lib):
     import oracle
 
-    if op == "route":
+    if op in ("route", "multi"):   # multi: the oracle of the concatenation (the same rows)
         return oracle.run_problem(p, lib=lib)
     # the workload's payloads stand for the expert-major rows the inverse move reads
     return oracle.unroute(p.tokens, p.counts, permute_scales=p.scales, permute_topk=p.topk, lib=lib)
@@ -265,7 +268,9 @@ def time_oracle(p, budget_s: float, op: str = "route", max_reps: int = 1000):
 
 
 def config_dict(p, k, extra=None, op="route"):
-    d = {"workload": p.name if op == "route" else "inverse move of " + p.name, "op": op,
+    name = {"route": p.name, "unroute": "inverse move of " + p.name,
+            "multi": p.name + ", one source buffer per rank"}[op]
+    d = {"workload": name, "op": op,
          "A": p.A, "H": p.H, "N": p.N, "E": p.E, "token_dtype": p.token_dtype,
          "count_dtype": str(p.counts.dtype), "scales": p.scale_layout, "scale_cols": p.scale_cols,
          "topk": p.topk is not None, "idx_type": p.idx_type, "expert_token_num_type": 1,
@@ -330,7 +335,7 @@ class RouteSetup:
         sl = m.SCALE_CODES[p.scale_layout]
         A, H, N, E = p.A, p.H, p.N, p.E
         i64 = int(p.counts.dtype == np.int64)
-        if op == "route":
+        if op in ("route", "multi"):
             st, plan = m.mrr_v2_plan(A, H, code, N, E, i64, sl, p.scale_cols, p.topk is not None, 1,
                                      p.idx_type, local_rank)
         else:
@@ -352,9 +357,23 @@ class RouteSetup:
         self.R = R = max(2, -(-4 * self.l2 // self.bytes_step))
         host_in = {"tokens": p.tokens, "counts": p.counts, "scales": p.scales, "topk": p.topk}
         inv = op == "unroute"   # the inverse move writes no index and no per-expert counts
+        bounds = np.concatenate([[0], np.cumsum(p.counts.astype(np.int64).sum(axis=1))])
         self.sets = []
         for _ in range(R):
             s = {k: dev_bytes(v) for k, v in host_in.items()}
+            if op == "multi":
+                # one device buffer per source rank for each payload, and the tables of their
+                # addresses; the single buffers above are dropped
+                for key, rb in (("tokens", p.row_bytes), ("scales", p.scale_row_bytes), ("topk", 4)):
+                    if s[key] is None:
+                        s["tab_" + key] = None
+                        continue
+                    parts = [s[key][bounds[i] * rb:bounds[i + 1] * rb].clone() for i in range(N)]
+                    for i, t in enumerate(parts):
+                        s[f"{key}@{i}"] = t
+                    s["tab_" + key] = torch.tensor([t.data_ptr() for t in parts], dtype=torch.int64, device=dev)
+                    s[key] = None
+                s["rows"] = torch.tensor(np.diff(bounds), dtype=torch.int64, device=dev)
             s["out_tokens"] = torch.empty(A * p.row_bytes, dtype=torch.uint8, device=dev)
             s["out_scales"] = (None if p.scales is None
                                else torch.empty(A * p.scale_row_bytes, dtype=torch.uint8, device=dev))
@@ -370,6 +389,12 @@ class RouteSetup:
             self.args = [(P(s["tokens"]), code, A, H, P(s["counts"]), i64, N, E, P(s["scales"]), sl,
                           p.scale_cols, P(s["topk"]), P(s["out_tokens"]), P(s["out_scales"]), P(s["idx"]),
                           P(s["etn"]), P(s["out_topk"]), 1, p.idx_type, P(s["ws"]), s["ws"].numel())
+                         for s in self.sets]
+        elif op == "multi":
+            self.fn = lib.mrr_v2_run_multi
+            self.args = [(P(s["tab_tokens"]), P(s["tab_scales"]), P(s["tab_topk"]), P(s["rows"]), code, A, H,
+                          P(s["counts"]), i64, N, E, sl, p.scale_cols, P(s["out_tokens"]), P(s["out_scales"]),
+                          P(s["idx"]), P(s["etn"]), P(s["out_topk"]), 1, p.idx_type, P(s["ws"]), s["ws"].numel())
                          for s in self.sets]
         else:  # the inverse move: the "tokens" buffers hold the expert-major rows
             self.fn = lib.mrr_v2_unroute
@@ -395,7 +420,7 @@ class RouteSetup:
             st = m.mrr_v2_read_status(s["ws"].data_ptr(), s["ws"].numel(), stream.cuda_stream)
             if st != m.MRR_OK:
                 raise RuntimeError(m.mrr_status_str(st))
-        if self.op == "route":
+        if self.op in ("route", "multi"):
             idx_sorted = torch.sort(self.sets[0]["idx"].to(torch.int64)).values
             assert torch.equal(idx_sorted, torch.arange(self.p.A, device=self.dev)), "index is not a permutation"
 
@@ -646,6 +671,15 @@ def run_e2e(args, p, sets, launch, dev, bytes_step, world, dist):
 
     h_in = {"tokens": pinned(p.tokens), "counts": pinned(p.counts), "scales": pinned(p.scales),
             "topk": pinned(p.topk)}
+    if "tokens@0" in sets[0]:
+        # multi-source form: each rank's rows go up into that rank's own buffer
+        bounds = np.concatenate([[0], np.cumsum(p.counts.astype(np.int64).sum(axis=1))])
+        for key, arr, rb in (("tokens", p.tokens, p.row_bytes), ("scales", p.scales, p.scale_row_bytes),
+                             ("topk", p.topk, 4)):
+            h = h_in.pop(key)
+            if arr is not None:
+                for i in range(p.N):
+                    h_in[f"{key}@{i}"] = h[bounds[i] * rb:bounds[i + 1] * rb]
     outs = ["out_tokens", "out_scales", "out_topk", "idx", "etn"]
     return pipelined_e2e(args, h_in, outs, sets, launch, dev, bytes_step, world, dist)
 

@@ -320,6 +320,24 @@ mrr_status mrr_v2_run_plan_multi(const mrr_v2_plan_t *plan, const void *const *s
                                  int64_t expert_token_num_type,
                                  void *workspace, size_t workspace_bytes, mrr_stream_t stream);
 
+/*
+ * mrr_v2_offsets_host -- host only, enqueues nothing: the offsets of the move for a count matrix
+ * in HOST memory ("CANN ops-transformer MoeReRoutingV2" article, section 计算公式), for the
+ * push form of the fused receive.  There each sender writes its segments straight into the
+ * receiver's expert-major buffer, so it needs the receiver's DstOffset of its own row before any
+ * row moves (the receiver computes it from the counts it received and sends row i back to
+ * sender i; see moe_expert_token_gb300.ep).
+ *   counts            [N, E] int32 or int64 (count_is_i64), HOST memory          (read)
+ *   src_offset        [N, E] int64 or NULL: SrcOffset(i, j), rank-major prefix   (written)
+ *   dst_offset        [N, E] int64 or NULL: DstOffset(i, j), expert-major prefix (written)
+ *   expert_token_num  [E] int64 or NULL: tokens per expert                       (written)
+ * Returns MRR_ERR_COUNT_NONPOS / MRR_ERR_COUNT_SUM for counts the kernels would refuse (a count
+ * <= 0, Sum != A), writing nothing; MRR_ERR_SHAPE / MRR_ERR_DTYPE / MRR_ERR_NULL for bad
+ * arguments.  N*E = 0 with A = 0 is the empty problem.
+ */
+mrr_status mrr_v2_offsets_host(const void *counts, int count_is_i64, int64_t N, int64_t E, int64_t A,
+                               int64_t *src_offset, int64_t *dst_offset, int64_t *expert_token_num);
+
 /* mrr_status_str -- static, human-readable name of a status code (never NULL). */
 const char *mrr_status_str(mrr_status s);
 

@@ -2054,6 +2054,8 @@ mrr_status mrr_v2_run_multi(const void *const *src_tokens, const void *const *sr
         return st;
     if (!src_tokens)
         return MRR_ERR_NULL;
+    if ((uintptr_t)src_rows % 8)
+        return MRR_ERR_ALIGN;
     if (sl == MRR_SCALE_NONE)
         src_scales = nullptr;  // "meaningless" output: nothing is read or written
     st = check_buffers(N * E, E, count_is_i64 ? 8 : 4, (int)sl, src_tokens, counts, src_scales, src_topk_w,
@@ -2160,6 +2162,54 @@ mrr_status mrr_v2_unroute(const void *permute_tokens, mrr_token_dtype dt, int64_
     plan.path = MRR_PATH_AUTO;
     return mrr_v2_run_plan(&plan, permute_tokens, dt, counts, permute_scales, permute_topk_w, tokens, scales,
                            nullptr, nullptr, topk_w, 1, workspace, workspace_bytes, stream);
+}
+
+mrr_status mrr_v2_offsets_host(const void *counts, int count_is_i64, int64_t N, int64_t E, int64_t A,
+                               int64_t *src_offset, int64_t *dst_offset, int64_t *expert_token_num)
+{
+    if (!counts && N * E > 0)
+        return MRR_ERR_NULL;
+    if ((count_is_i64 != 0 && count_is_i64 != 1))
+        return MRR_ERR_DTYPE;
+    if (N < 0 || E < 0 || A < 0 || A > INT32_MAX || (N > 0 && E > INT32_MAX / N) || N > INT32_MAX)
+        return MRR_ERR_SHAPE;
+    auto count = [&](int64_t i, int64_t j) -> int64_t {
+        return count_is_i64 ? static_cast<const int64_t *>(counts)[i * E + j]
+                            : (int64_t) static_cast<const int32_t *>(counts)[i * E + j];
+    };
+    // the same checks the kernels make: every count > 0 and no larger than A, Sum = A
+    int64_t sum = 0;
+    for (int64_t q = 0; q < N * E; ++q) {
+        const int64_t c = count(q / E, q % E);
+        if (c <= 0)
+            return MRR_ERR_COUNT_NONPOS;
+        if (c > A)
+            return MRR_ERR_COUNT_SUM;
+        sum += c;
+        if (sum > A)
+            return MRR_ERR_COUNT_SUM;
+    }
+    if (sum != A)
+        return MRR_ERR_COUNT_SUM;
+    int64_t run = 0;  // SrcOffset: rank outer, expert inner
+    for (int64_t i = 0; i < N; ++i)
+        for (int64_t j = 0; j < E; ++j) {
+            if (src_offset)
+                src_offset[i * E + j] = run;
+            run += count(i, j);
+        }
+    run = 0;  // DstOffset: expert outer, rank inner; expert j's block is its count
+    for (int64_t j = 0; j < E; ++j) {
+        const int64_t start = run;
+        for (int64_t i = 0; i < N; ++i) {
+            if (dst_offset)
+                dst_offset[i * E + j] = run;
+            run += count(i, j);
+        }
+        if (expert_token_num)
+            expert_token_num[j] = run - start;
+    }
+    return MRR_OK;
 }
 
 mrr_status mrr_v2_read_status(const void *workspace, size_t workspace_bytes, mrr_stream_t stream_)

@@ -130,6 +130,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.mrr_v2_run_plan_multi.restype = I32
     lib.mrr_v2_run_plan_multi.argtypes = [ctypes.POINTER(mrr_v2_plan_t), P, P, P, P, I32, P,
                                           P, P, P, P, P, I64, P, ctypes.c_size_t, P]
+    lib.mrr_v2_offsets_host.restype = I32
+    lib.mrr_v2_offsets_host.argtypes = [P, I32, I64, I64, I64, P, P, P]
     lib.mrr_v2_run_noalloc.restype = I32
     lib.mrr_v2_run_noalloc.argtypes = [P, I32, I64, I64, P, I32, I64, I64, P, I32, I64, P,
                                        P, P, P, P, P, I64, I64, I32, P]
@@ -231,6 +233,12 @@ def mrr_v2_run_plan_multi(plan: mrr_v2_plan_t, src_tokens, src_scales, src_topk_
         ctypes.byref(plan), src_tokens, src_scales, src_topk_w, src_rows, dt, counts,
         permute_tokens, permute_scales, permute_token_idx, expert_token_num, permute_topk_w,
         expert_token_num_type, workspace, workspace_bytes, stream)
+
+
+def mrr_v2_offsets_host(counts, count_is_i64, N, E, A, src_offset, dst_offset, expert_token_num) -> int:
+    """Host addresses: counts [N, E] (int32 / int64), int64 outputs [N, E], [N, E], [E] or None."""
+    return load_library().mrr_v2_offsets_host(counts, int(count_is_i64), N, E, A, src_offset, dst_offset,
+                                              expert_token_num)
 
 
 def mrr_v2_read_status(workspace, workspace_bytes, stream) -> int:

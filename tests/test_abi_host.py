@@ -27,7 +27,7 @@ def test_exports_every_header_function(lib):
     assert set(names) == {"mrr_v2_plan", "mrr_v2_run", "mrr_v2_run_plan", "mrr_v2_read_status",
                           "mrr_status_str", "mrr_v2_run_noalloc", "mrr_v2_unroute_plan",
                           "mrr_v2_unroute", "mrr_v1_run", "mrr_gating_topk_run", "mrr_v2_run_multi",
-                          "mrr_v2_run_plan_multi"}
+                          "mrr_v2_run_plan_multi", "mrr_v2_offsets_host"}
     out = subprocess.run(["nm", "-D", "--defined-only", m.library_path()], capture_output=True,
                          text=True, check=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
@@ -231,3 +231,37 @@ def gate(**kw):
 ])
 def test_gating_rejects(lib, kw, code):
     assert gate(**kw) == code
+
+
+def run_multi(**kw):
+    a = dict(src_tokens=T, src_scales=S, src_topk_w=W, src_rows=None, dt=m.MRR_BF16, A=64, H=128, counts=C,
+             count_is_i64=0, N=4, E=4, sl=m.MRR_SCALE_F32_A, scale_cols=1, permute_tokens=O1,
+             permute_scales=O2, permute_token_idx=I, expert_token_num=X, permute_topk_w=OW,
+             expert_token_num_type=1, idx_type=0, workspace=WS, workspace_bytes=1 << 20, stream=None)
+    a.update(kw)
+    return m.mrr_v2_run_multi(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(src_tokens=None), m.MRR_ERR_NULL),
+    (dict(src_topk_w=None), m.MRR_ERR_TOPK_PAIR),                  # output given, input table not
+    (dict(permute_topk_w=None), m.MRR_ERR_TOPK_PAIR),
+    (dict(src_scales=None), m.MRR_ERR_NULL),                       # scales layout without a table
+    (dict(permute_scales=None), m.MRR_ERR_NULL),
+    (dict(H=16384), m.MRR_ERR_SHAPE),
+    (dict(A=10), m.MRR_ERR_SHAPE),                                 # N*E > A
+    (dict(idx_type=3), m.MRR_ERR_ATTR),
+    (dict(workspace=None), m.MRR_ERR_WORKSPACE),
+    (dict(src_rows=WS + 4), m.MRR_ERR_ALIGN),                      # int64 table misaligned
+])
+def test_run_multi_host_errors(lib, kw, code):
+    assert run_multi(**kw) == code
+
+
+def test_run_plan_multi_refuses_the_inverse_direction(lib):
+    plan = m.mrr_v2_plan_t()
+    plan.A, plan.H, plan.N, plan.E, plan.row_bytes = 64, 128, 4, 4, 256
+    plan.direction = 1
+    st = m.mrr_v2_run_plan_multi(plan, T, None, None, None, m.MRR_BF16, C, O1, None, I, X, None, 1, WS,
+                                 1 << 20, None)
+    assert st in (m.MRR_ERR_PLAN, m.MRR_ERR_CUDA)
