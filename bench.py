@@ -55,6 +55,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-detail", action="store_true",
                     help="skip the batch spread, unrotated and CUDA-graph timings")
+    ap.add_argument("--multi-layout", choices=["separate", "slots"], default="separate",
+                    help="--op multi: one allocation per source rank, or one receive buffer with a "
+                         "slot of the largest rank's rows per rank")
     ap.add_argument("--no-other-configs", action="store_true",
                     help="time only the chosen workload (by default workload 2 is followed by 3, 4 and 5)")
     return ap.parse_args(argv)
@@ -269,7 +272,7 @@ def time_oracle(p, budget_s: float, op: str = "route", max_reps: int = 1000):
 
 def config_dict(p, k, extra=None, op="route"):
     name = {"route": p.name, "unroute": "inverse move of " + p.name,
-            "multi": p.name + ", one source buffer per rank"}[op]
+            "multi": p.name + ", each source rank's rows in a buffer of their own"}[op]
     d = {"workload": name, "op": op,
          "A": p.A, "H": p.H, "N": p.N, "E": p.E, "token_dtype": p.token_dtype,
          "count_dtype": str(p.counts.dtype), "scales": p.scale_layout, "scale_cols": p.scale_cols,
@@ -325,7 +328,7 @@ class RouteSetup:
     """One workload on one GPU: its plan, rotating device buffer sets, and the C-ABI call of one
     step (mrr_v2_run, or mrr_v2_unroute for the inverse move) with its arguments resolved."""
 
-    def __init__(self, p, op, dev, local_rank):
+    def __init__(self, p, op, dev, local_rank, multi_layout="separate"):
         import numpy as np
         import torch
         import moe_expert_token_gb300.mrr_v2 as m
@@ -364,16 +367,26 @@ class RouteSetup:
             if op == "multi":
                 # one device buffer per source rank for each payload, and the tables of their
                 # addresses; the single buffers above are dropped
+                rows = np.diff(bounds)
+                cap = int(rows.max())
                 for key, rb in (("tokens", p.row_bytes), ("scales", p.scale_row_bytes), ("topk", 4)):
                     if s[key] is None:
                         s["tab_" + key] = None
                         continue
-                    parts = [s[key][bounds[i] * rb:bounds[i + 1] * rb].clone() for i in range(N)]
+                    if multi_layout == "slots":   # one receive buffer, rank i's slot at i * cap rows
+                        slab = torch.empty(N * cap * rb, dtype=torch.uint8, device=dev)
+                        parts = [slab[i * cap * rb:i * cap * rb + int(rows[i]) * rb] for i in range(N)]
+                        for i, t in enumerate(parts):
+                            t.copy_(s[key][bounds[i] * rb:bounds[i + 1] * rb])
+                        s["slab_" + key] = slab
+                    else:
+                        parts = [s[key][bounds[i] * rb:bounds[i + 1] * rb].clone() for i in range(N)]
                     for i, t in enumerate(parts):
                         s[f"{key}@{i}"] = t
                     s["tab_" + key] = torch.tensor([t.data_ptr() for t in parts], dtype=torch.int64, device=dev)
                     s[key] = None
-                s["rows"] = torch.tensor(np.diff(bounds), dtype=torch.int64, device=dev)
+                s["rows"] = torch.tensor(np.full(N, cap) if multi_layout == "slots" else rows, dtype=torch.int64,
+                                         device=dev)
             s["out_tokens"] = torch.empty(A * p.row_bytes, dtype=torch.uint8, device=dev)
             s["out_scales"] = (None if p.scales is None
                                else torch.empty(A * p.scale_row_bytes, dtype=torch.uint8, device=dev))
@@ -494,7 +507,7 @@ def run_gpu(args):
 
     p = workloads.config(args.config)
     A = p.A
-    setup = RouteSetup(p, args.op, dev, local_rank)
+    setup = RouteSetup(p, args.op, dev, local_rank, args.multi_layout)
     plan, sets, R = setup.plan, setup.sets, setup.R
     bytes_step, launches_per_step = setup.bytes_step, setup.launches_per_step
     stream = torch.cuda.current_stream(dev)
@@ -572,7 +585,8 @@ def run_gpu(args):
             "l2": f"{R} rotating buffer sets, {R * bytes_step / 1e6:.0f} MB > 4x L2 ({setup_l2(dev) / 1e6:.0f} MB)",
             "path": {1: "bulk", 2: "vector"}[plan.path], "grid": plan.grid, "block": plan.block,
             "chunk_bytes": plan.chunk_bytes, "stages": plan.stages, "fused_scan": bool(plan.fuse_scan),
-            "parallelism": f"replicas x{world}"}),
+            "parallelism": f"replicas x{world}",
+            **({"multi_layout": args.multi_layout} if args.op == "multi" else {})}),
         "pct_of_peak": 100.0 * value / world / peak,
         "tokens_per_s": world * A * K / (elapsed_ms * 1e-3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

@@ -35,6 +35,7 @@
 
 #include <atomic>
 #include <chrono>
+#include <type_traits>
 
 #include "mrr_v2.h"
 #include "ptx.cuh"
@@ -99,6 +100,17 @@ struct Params {
     const uint8_t *const *src_sc;   // [N] rank i's scale rows, or null without scales
     const uint8_t *const *src_tk;   // [N] rank i's top-k weights (any alignment), or null
     const long long *src_rows;      // [N] rows each rank's buffers hold, or null (not checked)
+    int ptr_off;                    // byte offset of the pointer tables' copy in dynamic shared
+                                    // memory (tokens, then scales, then top-k), or -1: read them
+                                    // from global memory
+};
+
+// The per-rank source tables the multi-source form reads: Params' global tables, or their copy in
+// shared memory (the bulk driver looks one up whenever a load crosses into another rank).
+struct Sources {
+    const uint8_t *const *tok;
+    const uint8_t *const *sc;
+    const uint8_t *const *tk;
 };
 
 // ------------------------------------------------------------------------------------------------
@@ -183,20 +195,35 @@ __device__ __forceinline__ int64_t dst_row_rank(const SegMap &m, int64_t s, int 
     return (int64_t)m.dest(g) + (s - (int64_t)m.begin(g));
 }
 
+// Multi-source form: the rank whose rows hold source byte x, the last i with R(i) * rb <= x
+// (a binary search over the N rank starts, with no division).
+__device__ __forceinline__ int rank_of_byte(const SegMap &m, int64_t x, int64_t rb)
+{
+    int lo = 0, hi = m.N;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if ((int64_t)m.row_ex[mid * m.E] * rb <= x)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
 // Every rank's pointers checked by threads t0, t0 + ts, ...: tokens present and, on the bulk path,
 // 16-byte aligned (the bulk copy engine's rule); scales and top-k weights present when they are
 // moved (any alignment: their copies fall back to narrower accesses).  Returns kFlagSource or 0
 // for this thread's share.
-__device__ __forceinline__ uint32_t check_sources(const Params &p, bool bulk, int t0, int ts)
+__device__ __forceinline__ uint32_t check_sources(const Params &p, const Sources &src, bool bulk, int t0, int ts)
 {
     uint32_t f = 0u;
     for (int i = t0; i < p.N; i += ts) {
-        const uintptr_t t = (uintptr_t)p.src_tok[i];
+        const uintptr_t t = (uintptr_t)src.tok[i];
         if (!t || (bulk && (t & 15u)))
             f = kFlagSource;
-        if (p.src_sc && !p.src_sc[i])
+        if (src.sc && !src.sc[i])
             f = kFlagSource;
-        if (p.src_tk && !p.src_tk[i])
+        if (src.tk && !src.tk[i])
             f = kFlagSource;
     }
     return f;
@@ -371,8 +398,16 @@ __device__ __forceinline__ uint32_t process_counts(const Params &p, int base, co
 //   dst_off[pad32(q)]  = DstOffset of segment q (column-major walk: expert outer, rank inner)
 // *s_flags and *s_sum must be zero before the call.  Returns the error flags (uniform over the
 // block); the tables are valid when it returns 0.
+struct NoMid {
+    __device__ void operator()() const {}
+};
+
+// `mid` (when given) is called by every thread once SrcOffset is complete and visible to the
+// block, before DstOffset is scanned: the multi-source form starts its token stream there.
+template <class Mid = NoMid>
 __device__ uint32_t cta_scan(const Params &p, CountBatch &cb, uint32_t *row_ex, uint32_t *cnt_t,
-                             uint32_t *dst_off, uint32_t *s_warp, uint32_t *s_flags, unsigned long long *s_sum)
+                             uint32_t *dst_off, uint32_t *s_warp, uint32_t *s_flags, unsigned long long *s_sum,
+                             Mid mid = Mid())
 {
     const int tid = threadIdx.x, lane = tid & 31, nthr = blockDim.x;
     const int NE = p.NE, N = p.N, E = p.E;
@@ -413,6 +448,10 @@ __device__ uint32_t cta_scan(const Params &p, CountBatch &cb, uint32_t *row_ex, 
         NE, s_warp, [&](int k) { return row_ex[k]; }, [&](int k, uint32_t v) { row_ex[k] = v; });
     if (tid == 0)
         row_ex[NE] = (uint32_t)p.A;
+    if constexpr (!std::is_same<Mid, NoMid>::value) {
+        __syncthreads();
+        mid();
+    }
     // DstOffset: exclusive prefix over the column-major copy, stored at pad32(q), q = i*E + j.
     // Each thread's positions come in increasing runs, so (i, j) of pos = j*N + i is stepped.
     int ci = -1, cj = 0, cpos = -2;
@@ -544,7 +583,8 @@ __device__ __forceinline__ void copy_unit_any(uint8_t *d, const uint8_t *s, int 
 // [r_lo, r_hi): kSideBatch loads in flight per thread, then the stores.  Multi-source form: the
 // source row is found in its rank's buffer, which may be less aligned than W.
 template <int W, bool kMulti>
-__device__ void move_scales(const Params &p, const SegMap &m, int64_t r_lo, int64_t r_hi, int t0, int ts)
+__device__ void move_scales(const Params &p, const SegMap &m, const Sources &src, int64_t r_lo, int64_t r_hi,
+                            int t0, int ts)
 {
     const int64_t sb = p.scale_row_bytes, vpr = sb / W;
     const int64_t items = (r_hi - r_lo) * vpr;
@@ -562,7 +602,7 @@ __device__ void move_scales(const Params &p, const SegMap &m, int64_t r_lo, int6
                     int rk;
                     int64_t loc;
                     d[u] = dst_row_rank(m, s[u], &rk, &loc);
-                    v[u] = ld_any<W>(p.src_sc[rk] + loc * sb + off[u]);
+                    v[u] = ld_any<W>(src.sc[rk] + loc * sb + off[u]);
                 } else {
                     v[u] = Vec<W>::ld(p.scales + s[u] * sb + off[u]);
                 }
@@ -582,11 +622,11 @@ __device__ void move_scales(const Params &p, const SegMap &m, int64_t r_lo, int6
 // Scale rows, top-k weights and the index for this CTA's share of the SOURCE rows,
 // processed by threads t0, t0 + ts, ... of the block.
 template <bool kMulti>
-__device__ void side_arrays(const Params &p, const SegMap &m, int t0, int ts)
+__device__ void side_arrays(const Params &p, const SegMap &m, const Sources &src, int t0, int ts)
 {
     const int64_t G = gridDim.x, b = blockIdx.x;
     const int64_t r_lo = b * p.A / G, r_hi = (b + 1) * p.A / G;
-    const bool topk4 = kMulti ? p.src_tk && p.topk_w == 4 : p.topk && p.topk_w == 4;
+    const bool topk4 = kMulti ? src.tk && p.topk_w == 4 : p.topk && p.topk_w == 4;
     for (int64_t base = r_lo + t0; base < r_hi; base += (int64_t)ts * kSideBatch) {
         uint32_t w[kSideBatch];
         int64_t dd[kSideBatch], loc[kSideBatch];
@@ -598,8 +638,8 @@ __device__ void side_arrays(const Params &p, const SegMap &m, int t0, int ts)
                 if (s < r_hi) {
                     dd[u] = dst_row_rank(m, s, &rk[u], &loc[u]);
                     if (topk4) {
-                        const uint8_t *src = p.src_tk[rk[u]] + loc[u] * 4;
-                        w[u] = ((uintptr_t)src & 3u) ? ld_any<4>(src) : __ldg(reinterpret_cast<const uint32_t *>(src));
+                        const uint8_t *a = src.tk[rk[u]] + loc[u] * 4;
+                        w[u] = ((uintptr_t)a & 3u) ? ld_any<4>(a) : __ldg(reinterpret_cast<const uint32_t *>(a));
                     }
                 }
             } else {
@@ -623,25 +663,25 @@ __device__ void side_arrays(const Params &p, const SegMap &m, int t0, int ts)
             if (topk4) {
                 reinterpret_cast<uint32_t *>(p.out_topk)[d] = w[u];
             } else if constexpr (kMulti) {
-                if (p.src_tk)
-                    copy_unit_any(p.out_topk + d * 4, p.src_tk[rk[u]] + loc[u] * 4, 4);
+                if (src.tk)
+                    copy_unit_any(p.out_topk + d * 4, src.tk[rk[u]] + loc[u] * 4, 4);
             } else if (p.topk) {
                 for (int k = 0; k < 4; k += p.topk_w)
                     copy_unit(p.out_topk + d * 4 + k, p.topk + s * 4 + k, p.topk_w);
             }
         }
     }
-    if (kMulti ? !p.src_sc : !p.scales)
+    if (kMulti ? !src.sc : !p.scales)
         return;
     switch (p.scale_w) {
     case 16:
-        move_scales<16, kMulti>(p, m, r_lo, r_hi, t0, ts);
+        move_scales<16, kMulti>(p, m, src, r_lo, r_hi, t0, ts);
         break;
     case 8:
-        move_scales<8, kMulti>(p, m, r_lo, r_hi, t0, ts);
+        move_scales<8, kMulti>(p, m, src, r_lo, r_hi, t0, ts);
         break;
     case 4:
-        move_scales<4, kMulti>(p, m, r_lo, r_hi, t0, ts);
+        move_scales<4, kMulti>(p, m, src, r_lo, r_hi, t0, ts);
         break;
     default: {  // 1- or 2-byte aligned scale rows
         const int w = p.scale_w;
@@ -655,7 +695,7 @@ __device__ void side_arrays(const Params &p, const SegMap &m, int t0, int ts)
                 int rk1;
                 int64_t loc1;
                 const int64_t d = dst_row_rank(m, s, &rk1, &loc1);
-                copy_unit_any(p.out_scales + d * sb + v * w, p.src_sc[rk1] + loc1 * sb + v * w, w);
+                copy_unit_any(p.out_scales + d * sb + v * w, src.sc[rk1] + loc1 * sb + v * w, w);
             } else {
                 const int64_t d = dst_row(m, s);
                 copy_unit(p.out_scales + d * sb + v * w, p.scales + s * sb + v * w, w);
@@ -803,7 +843,8 @@ __device__ __forceinline__ void copy_block(uint8_t *dst, const uint8_t *src, int
 // a run of small segments is not copied one latency-bound piece at a time.  Multi-source form:
 // the piece is read from its rank's buffer (segment q belongs to rank q / E).
 template <bool kMulti>
-__device__ void vector_copy(const Params &p, const SegMap &m, int64_t lo, int64_t hi, int tid, int nthr)
+__device__ void vector_copy(const Params &p, const SegMap &m, const Sources &src, int64_t lo, int64_t hi, int tid,
+                            int nthr)
 {
     const int nwarps = nthr >> 5, warp = tid >> 5;
     const int64_t units = (hi - lo + 15) >> 4;
@@ -826,7 +867,7 @@ __device__ void vector_copy(const Params &p, const SegMap &m, int64_t lo, int64_
     if constexpr (kMulti) {
         rank_b0 = (int64_t)m.row_ex[rank * m.E] * rb;
         rank_b1 = (int64_t)m.row_ex[(rank + 1) * m.E] * rb;
-        rank_buf = p.src_tok[rank];
+        rank_buf = src.tok[rank];
     }
     for (int64_t pos = lo; pos < hi;) {
         while (pos >= seg_end) {
@@ -838,7 +879,7 @@ __device__ void vector_copy(const Params &p, const SegMap &m, int64_t lo, int64_
                     ++rank;
                     rank_b0 = rank_b1;
                     rank_b1 = (int64_t)m.row_ex[(rank + 1) * m.E] * rb;
-                    rank_buf = p.src_tok[rank];
+                    rank_buf = src.tok[rank];
                 }
             }
         }
@@ -905,6 +946,7 @@ struct BulkRing {
     // rank-major order (consecutive chunks mostly come from one rank: one lookup per change)
     const uint8_t *src_base;
     int64_t src_b0, src_b1;
+    const uint8_t *const *src_tab;  // the token pointer table (shared memory when staged)
 };
 
 // Next chunk of this CTA as the byte range [*b0, *b1); false when the CTA has no more work.
@@ -980,10 +1022,10 @@ __device__ __forceinline__ void bulk_issue_load(const Params &p, BulkRing &r, co
         const int64_t rb = p.row_bytes;
         for (int64_t x = b0; x < b1;) {
             if (x < r.src_b0 || x >= r.src_b1) {
-                const int i = m.find((uint32_t)(x / rb)) / m.E;
+                const int i = rank_of_byte(m, x, rb);
                 r.src_b0 = (int64_t)m.row_ex[i * m.E] * rb;
                 r.src_b1 = (int64_t)m.row_ex[(i + 1) * m.E] * rb;
-                r.src_base = p.src_tok[i];
+                r.src_base = r.src_tab[i];
             }
             const int64_t y = min(b1, r.src_b1);
             const uint32_t d = dst + (uint32_t)(x - b0), n = (uint32_t)(y - x);
@@ -1000,6 +1042,26 @@ __device__ __forceinline__ void bulk_issue_load(const Params &p, BulkRing &r, co
             bulk_g2s(dst, p.tokens + b0, bytes, bar);
     }
     ++r.issued;
+}
+
+// Ask L2 for source bytes [lo, hi) (16-byte aligned, a multiple of 16 long); the multi-source
+// form splits the range where it crosses into the next rank's buffer.
+template <bool kMulti>
+__device__ __forceinline__ void prefetch_src(const Params &p, const SegMap &m, const Sources &src, int64_t lo,
+                                             int64_t hi)
+{
+    if constexpr (!kMulti) {
+        bulk_prefetch_l2(p.tokens + lo, (uint32_t)(hi - lo));
+    } else {
+        const int64_t rb = p.row_bytes;
+        int i = rank_of_byte(m, lo, rb);
+        for (int64_t x = lo; x < hi; ++i) {
+            const int64_t b0 = (int64_t)m.row_ex[i * m.E] * rb, b1 = (int64_t)m.row_ex[(i + 1) * m.E] * rb;
+            const int64_t y = min(hi, b1);
+            bulk_prefetch_l2(src.tok[i] + (x - b0), (uint32_t)(y - x));
+            x = y;
+        }
+    }
 }
 
 template <bool kMulti>
@@ -1126,6 +1188,28 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
     m.N = p.N;
     m.E = p.E;
     m.inv = p.inverse;
+    Sources src{p.src_tok, p.src_sc, p.src_tk};
+    ring.src_tab = p.src_tok;
+    // Multi-source form: copy the per-rank pointer tables into shared memory (their loads overlap
+    // the count loads); the bulk driver then finds a rank's buffer without a global round trip.
+    // The block synchronises before anything reads the copy.
+    auto stage_pointers = [&]() {
+        if (kMulti && p.ptr_off >= 0) {
+            const uint8_t **t = reinterpret_cast<const uint8_t **>(smem + p.ptr_off);
+            const uint8_t **tok = t, **sc = t + p.N, **tk = t + (p.src_sc ? 2 : 1) * p.N;
+            for (int i = tid; i < p.N; i += nthr) {
+                tok[i] = p.src_tok[i];
+                if (p.src_sc)
+                    sc[i] = p.src_sc[i];
+                if (p.src_tk)
+                    tk[i] = p.src_tk[i];
+            }
+            src.tok = tok;
+            src.sc = p.src_sc ? sc : nullptr;
+            src.tk = p.src_tk ? tk : nullptr;
+            ring.src_tab = tok;
+        }
+    };
 
     CountBatch cb;
     if (tid == 0)
@@ -1149,7 +1233,7 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
                 bulk_issue_load<kMulti>(p, ring, m, b0, b1);
             }
         }
-        if (!kMulti && kBulk && p.prefetch_chunks > 0 && tid >= 32 && tid < 64) {
+        if (kBulk && p.prefetch_chunks > 0 && tid >= 32 && tid < 64) {
             // The ring holds only `stages` chunks, which land long before the offsets are ready.
             // Keep HBM busy meanwhile: warp 1 asks L2 for the next chunks, one per lane -- first
             // this CTA's own static chunks past the ring, then its share of the first chunks the
@@ -1172,7 +1256,7 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
                     lo = c * C;
                     hi = min(lo + C, p.total_bytes);
                 }
-                bulk_prefetch_l2(p.tokens + lo, (uint32_t)(hi - lo));
+                prefetch_src<kMulti>(p, m, src, lo, hi);
             }
         }
     };
@@ -1197,20 +1281,30 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
             issue_count_loads<int>(p, 0, cb);
         if (!kMulti)
             start_token_stream();
+        stage_pointers();
     }
 
     uint32_t flags;
     if (kFused) {
         uint32_t *rex = tab, *cnt_t = tab + p.NE + 1, *dof = cnt_t + padded_len(p.NE);
-        flags = cta_scan(p, cb, rex, cnt_t, dof, s_warp, &s_flags, &s_sum);
         m.row_ex = rex;
         m.dst_off = dof;
         m.col_ex = cnt_t;
         if constexpr (kMulti) {
-            // every rank's pointers and row count, before any source is read (uniform over the block)
-            const uint32_t f = flags ? 0u : check_sources(p, kBulk, tid, nthr) | check_capacity(p, rex, tid, nthr);
-            if (__syncthreads_or(f != 0u))
-                flags |= kFlagSource;
+            // Once SrcOffset is scanned (rank i's rows start at SrcOffset(i, 0)), check every
+            // rank's pointers and row count (uniform over the block), then start the token stream
+            // while DstOffset is scanned.  Counts that fail validation return before this point.
+            uint32_t src_flag = 0u;
+            auto mid = [&]() {
+                const uint32_t f = check_sources(p, src, kBulk, tid, nthr) | check_capacity(p, rex, tid, nthr);
+                if (__syncthreads_or(f != 0u))
+                    src_flag = kFlagSource;
+                else
+                    start_token_stream();
+            };
+            flags = cta_scan(p, cb, rex, cnt_t, dof, s_warp, &s_flags, &s_sum, mid) | src_flag;
+        } else {
+            flags = cta_scan(p, cb, rex, cnt_t, dof, s_warp, &s_flags, &s_sum);
         }
         if (b == 0) {
             if (!flags && !p.inverse)
@@ -1221,7 +1315,8 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
             }
         }
     } else {
-        __syncthreads();  // s_first[1] cleared before warp 1 may set it
+        stage_pointers();
+        __syncthreads();  // s_first[1] cleared before warp 1 may set it; pointer tables staged
         // written by the scan kernel (its count checks and, multi-source, its pointer checks)
         flags = *reinterpret_cast<volatile uint32_t *>(p.status);
         m.row_ex = p.g_row_ex;
@@ -1251,7 +1346,7 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
         if (b == 0 && tid == 0)
             p.status[1] = (uint32_t)G;
     }
-    if (kMulti && !flags)
+    if (kMulti && !kFused && !flags)
         start_token_stream();
 
     uint32_t tflag = 0u;
@@ -1264,11 +1359,11 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
                 __threadfence_block();
                 s_first[1] = 1u;
             }
-            side_arrays<kMulti>(p, m, tid - 32, nthr - 32);
+            side_arrays<kMulti>(p, m, src, tid - 32, nthr - 32);
         }
     } else if (!flags) {
-        vector_copy<kMulti>(p, m, lo, hi, tid, nthr);
-        side_arrays<kMulti>(p, m, tid, nthr);
+        vector_copy<kMulti>(p, m, src, lo, hi, tid, nthr);
+        side_arrays<kMulti>(p, m, src, tid, nthr);
     }
     if (tid == 0)
         p.status[2 + b] = tflag;
@@ -1295,7 +1390,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(const Params p)
     if (p.multi) {
         // the multi-source form's per-rank pointers, checked once here for the copy kernel, which
         // reads this status word before it touches any source
-        if (__syncthreads_or(check_sources(p, p.multi_bulk != 0, tid, nthr) != 0u)) {
+        const Sources src{p.src_tok, p.src_sc, p.src_tk};
+        if (__syncthreads_or(check_sources(p, src, p.multi_bulk != 0, tid, nthr) != 0u)) {
             if (tid == 0)
                 p.status[0] = kFlagSource;
             return;
@@ -1947,7 +2043,14 @@ mrr_status run_plan_impl(const mrr_v2_plan_t *plan, const MultiSrc *ms, const vo
     p.static_chunks = pl.static_chunks;
     p.prefetch_chunks = path == MRR_PATH_BULK ? pl.prefetch_chunks : 0;
     p.scan_in_smem = scan_in_smem ? 1 : 0;
+    p.ptr_off = -1;
     if (ms) {
+        // the pointer tables' copy in shared memory, behind everything else, when it fits
+        const int64_t pb = 8 * N * (1 + (ms->scales ? 1 : 0) + (ms->topk ? 1 : 0));
+        if (round_up(smem, 16) + pb <= optin - 1024) {
+            p.ptr_off = (int)round_up(smem, 16);
+            smem = p.ptr_off + pb;
+        }
         p.multi = 1;
         p.multi_bulk = path == MRR_PATH_BULK ? 1 : 0;
         p.src_tok = reinterpret_cast<const uint8_t *const *>(ms->tokens);
@@ -1957,7 +2060,6 @@ mrr_status run_plan_impl(const mrr_v2_plan_t *plan, const MultiSrc *ms, const vo
         p.tokens = nullptr;
         p.scales = nullptr;
         p.topk = nullptr;
-        p.prefetch_chunks = 0;
     }
     p.ticket = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(workspace) + kTicketOffset);
     p.epoch = (path == MRR_PATH_BULK && pl.sched == 1)

@@ -165,7 +165,7 @@ for _c in range(28):
     dt = _dtypes[_c % len(_dtypes)]
     H = int(_H[_rng.integers(len(_H))])
     if dt.startswith("float4") and H % 2:
-        H += 1
+        H -= 1 if H > 1 else -1
     N, E = _NE[_c % len(_NE)]
     FUZZ.append(dict(case=_c, dt=dt, H=H, N=N, E=E, i64=bool(_c % 3 == 0),
                      sl=["none", "f32_a", "f32_as", "e8m0"][_c % 4], topk=bool(_c % 2),
