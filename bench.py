@@ -98,7 +98,8 @@ def measured_peak():
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for rel in ("moe_expert_token_gb300/csrc/mrr_v2.cu", "moe_expert_token_gb300/csrc/ptx.cuh"):
+    for rel in ("moe_expert_token_gb300/csrc/mrr_v2.cu", "moe_expert_token_gb300/csrc/ptx.cuh",
+                "moe_expert_token_gb300/csrc/ws_layout.h"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
