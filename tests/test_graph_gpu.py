@@ -151,3 +151,69 @@ def test_concurrent_streams_with_their_own_workspaces():
         for b, ws in zip(sets, wss):
             assert m.mrr_v2_read_status(ws.ptr, ws.n, torch.cuda.current_stream().cuda_stream) == m.MRR_OK
             assert_bit_exact(_result(b, p), ref, p)
+
+
+@pytest.mark.parametrize("N,E", [(8, 16), (70, 64)], ids=["fused-scan", "scan-kernel"])
+def test_graph_replays_multi_source(N, E):
+    """The multi-source form captured in a CUDA graph: its pointer tables live in device memory, so
+    a replay reads whatever rows the per-rank buffers hold at that moment.  The buffers are
+    rewritten with new rows between replays, and every replay must match the oracle on them."""
+    import torch
+
+    d = torch.device("cuda:0")
+    A, H = 3 * N * E + 500, 1024
+    base = workloads.make_problem(np.random.default_rng(300 + N), A=A, H=H, N=N, E=E, token_dtype="bfloat16",
+                                  scale_layout="f32_as", scale_cols=2, has_topk=True)
+    bounds = np.concatenate([[0], np.cumsum(base.counts.astype(np.int64).sum(axis=1))])
+    rb, sb = base.row_bytes, base.scale_row_bytes
+    tok = [DevBuf(int(bounds[i + 1] - bounds[i]) * rb, d) for i in range(N)]
+    sc = [DevBuf(int(bounds[i + 1] - bounds[i]) * sb, d) for i in range(N)]
+    tw = [DevBuf(int(bounds[i + 1] - bounds[i]) * 4, d) for i in range(N)]
+    tab = {k: torch.tensor([b.ptr for b in v], dtype=torch.int64, device=d) for k, v in
+           (("tok", tok), ("sc", sc), ("tw", tw))}
+    rows = torch.tensor(np.diff(bounds), dtype=torch.int64, device=d)
+    cnt = DevBuf.of(base.counts, d)
+    outs = dict(out_tok=DevBuf(A * rb, d), out_sc=DevBuf(A * sb, d), idx=DevBuf(4 * A, d),
+                etn=DevBuf(E * 4, d), out_tw=DevBuf(4 * A, d))
+    st, plan = m.mrr_v2_plan(A, H, m.MRR_BF16, N, E, 0, m.MRR_SCALE_F32_AS, 2, 1, 1, 0, 0)
+    assert st == m.MRR_OK
+    ws = DevBuf(plan.workspace_bytes, d, fill=0x5A)
+
+    def fill(p):   # the problem's rows into the per-rank buffers
+        for i in range(N):
+            for bl, arr, w in ((tok, p.tokens, rb), (sc, p.scales, sb), (tw, p.topk.view(np.uint8).reshape(A, 4), 4)):
+                part = np.ascontiguousarray(arr).reshape(A, w)[bounds[i]:bounds[i + 1]].reshape(-1)
+                bl[i].t[bl[i].off:bl[i].off + bl[i].n].copy_(torch.from_numpy(part.copy()).to(d))
+
+    def launch(stream):
+        st = m.mrr_v2_run_multi(tab["tok"].data_ptr(), tab["sc"].data_ptr(), tab["tw"].data_ptr(), rows.data_ptr(),
+                                m.MRR_BF16, A, H, cnt.ptr, 0, N, E, m.MRR_SCALE_F32_AS, 2, outs["out_tok"].ptr,
+                                outs["out_sc"].ptr, outs["idx"].ptr, outs["etn"].ptr, outs["out_tw"].ptr, 1, 0,
+                                ws.ptr, ws.n, stream)
+        assert st == m.MRR_OK, m.mrr_status_str(st)
+
+    fill(base)
+    launch(torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    with torch.cuda.graph(g, stream=cap):
+        launch(cap.cuda_stream)
+    for rep in range(3):
+        p = workloads.make_problem(np.random.default_rng(400 + rep), A=A, H=H, N=N, E=E, token_dtype="bfloat16",
+                                   counts=base.counts, scale_layout="f32_as", scale_cols=2, has_topk=True)
+        fill(p)
+        _poison(outs)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert m.mrr_v2_read_status(ws.ptr, ws.n, torch.cuda.current_stream().cuda_stream) == m.MRR_OK
+        ref = oracle.run_problem(p)
+        got = {"status": m.MRR_OK,
+               "permute_tokens": outs["out_tok"].host().reshape(A, rb),
+               "permute_scales": outs["out_sc"].host().reshape(A, sb),
+               "permute_token_idx": outs["idx"].host().view(np.int32),
+               "expert_token_num": outs["etn"].host().view(np.int32),
+               "permute_topk_weight": outs["out_tw"].host().view(np.float32),
+               "guards_intact": all(b.guards_intact() for b in outs.values()), "inputs_intact": True}
+        assert_bit_exact(got, ref, p)
