@@ -1831,12 +1831,18 @@ mrr_status make_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int64_
         // Up to 1024 segments a deeper ring of smaller chunks (5 x 44 KiB, else 5 x 40 KiB) keeps
         // more loads in flight per SM: measured on GB300 against 3 x 64 KiB, C2 36.99 -> 35.96 us,
         // C3 70.49 -> 69.58, C4 72.91 -> 71.75.  At 4096 segments (C5) five stages lost (51 us).
+        // Above 1024 segments (the in-CTA tables take 13-50 KB) four stages of 44 KiB still fit:
+        // measured on GB300 against 3 x 48 KiB / 3 x 64 KiB, 4096 segments (C5) 44.22 -> 42.99 us
+        // and 2048 segments 44.90 -> 42.7 us, with 2 prefetched chunks and 8 static chunks (below).
         if (NE <= 1024 && 5 * 45056 + table_bytes <= optin - 1024) {
             p.chunk_bytes = 45056;
             p.stages = 5;
         } else if (NE <= 1024 && 5 * 40960 + table_bytes <= optin - 1024) {
             p.chunk_bytes = 40960;
             p.stages = 5;
+        } else if (p.fuse_scan && 4 * 45056 + table_bytes <= optin - 1024) {
+            p.chunk_bytes = 45056;
+            p.stages = 4;
         }
         if ((int64_t)p.stages * p.chunk_bytes + table_bytes > optin - 1024)
             p.chunk_bytes = 49152;
@@ -1848,12 +1854,17 @@ mrr_status make_plan(int64_t A, int64_t H, mrr_token_dtype dt, int64_t N, int64_
             --p.stages;
         while (p.chunk_bytes > 4096 && (int64_t)p.stages * p.chunk_bytes + table_bytes > optin - 1024)
             p.chunk_bytes /= 2;
-        // dynamic chunk scheduling unless the counter's 24-bit ticket space could run out
-        p.static_chunks = p.stages + 1;
+        // dynamic chunk scheduling unless the counter's 24-bit ticket space could run out; with
+        // the four-stage ring above 1024 segments, 8 static chunks per CTA (measured at 4096
+        // segments: 6 or 8 best, 42.99 us; the default 5: 43.69; 12: 43.39; 16: 44.00)
+        const bool ring4 = p.fuse_scan && NE > 1024 && p.stages == 4;
+        p.static_chunks = ring4 ? 8 : p.stages + 1;
         // many segments: the in-CTA scan outlasts the ring's loads, so prefetch the next chunks
-        // into L2 meanwhile (measured: 4 chunks per CTA at 4096 segments, none below 1024; behind
-        // the scan kernel, N*E > 4096, 4 to 12 chunks were 0-10 % slower than none)
-        p.prefetch_chunks = (p.fuse_scan && NE > 1024) ? 4 : 0;
+        // into L2 meanwhile (measured at 4096 segments: 4 chunks per CTA with a 3-stage ring, 2
+        // with the 4-stage ring (0: 44.93 us, 1: 43.95, 2: 43.69, 3: 44.04, 6: 45.10); none
+        // below 1024 segments; behind the scan kernel, N*E > 4096, 4 to 12 chunks were 0-10 %
+        // slower than none)
+        p.prefetch_chunks = (p.fuse_scan && NE > 1024) ? (ring4 ? 2 : 4) : 0;
         const int64_t nch = (total + p.chunk_bytes - 1) / p.chunk_bytes;
         p.sched = (nch + 3 * kMaxGrid < (int64_t)kTicketMask) ? 1 : 0;
         p.smem_bytes = (int32_t)((int64_t)p.stages * p.chunk_bytes + table_bytes);
