@@ -16,7 +16,7 @@ Source: the article "CANN 自定义算子详解：npu_moe_gating_top_k 实现 Mo
      groups, and take the k largest normOut values inside them;
   4. y = normOut at the chosen experts; yOut = y / (sum(y) + eps) * routed_scaling_factor.
 
-Readings where the page is silent (each listed in the design notes):
+Readings where the page is silent:
   * the top-k decisions are taken on the float32 normOut the page stores (both the oracle and the
     GPU decide in float32); equal scores go to the lower group / expert index;
   * y and the optional normOut output include the bias (the page assigns normOut += bias before
