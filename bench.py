@@ -409,7 +409,7 @@ class RouteSetup:
             # may start before the counts are scanned; slots pass their capacity
             import ctypes
 
-            self.mplan = plan
+            self.mplan = m.mrr_v2_plan_t.from_buffer_copy(plan)   # the reported plan stays as made
             self.mplan.path = m.MRR_PATH_AUTO
             self.mplan.multi_rows_exact = 1 if multi_layout == "separate" else 0
             self.fn = lib.mrr_v2_run_plan_multi
