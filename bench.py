@@ -405,17 +405,10 @@ class RouteSetup:
                           P(s["etn"]), P(s["out_topk"]), 1, p.idx_type, P(s["ws"]), s["ws"].numel())
                          for s in self.sets]
         elif op == "multi":
-            # separate buffers hold exactly each rank's rows: the plan says so, and the token stream
-            # may start before the counts are scanned; slots pass their capacity
-            import ctypes
-
-            self.mplan = m.mrr_v2_plan_t.from_buffer_copy(plan)   # the reported plan stays as made
-            self.mplan.path = m.MRR_PATH_AUTO
-            self.mplan.multi_rows_exact = 1 if multi_layout == "separate" else 0
-            self.fn = lib.mrr_v2_run_plan_multi
-            self.args = [(ctypes.byref(self.mplan), P(s["tab_tokens"]), P(s["tab_scales"]), P(s["tab_topk"]),
-                          P(s["rows"]), code, P(s["counts"]), P(s["out_tokens"]), P(s["out_scales"]), P(s["idx"]),
-                          P(s["etn"]), P(s["out_topk"]), 1, P(s["ws"]), s["ws"].numel())
+            self.fn = lib.mrr_v2_run_multi
+            self.args = [(P(s["tab_tokens"]), P(s["tab_scales"]), P(s["tab_topk"]), P(s["rows"]), code, A, H,
+                          P(s["counts"]), i64, N, E, sl, p.scale_cols, P(s["out_tokens"]), P(s["out_scales"]),
+                          P(s["idx"]), P(s["etn"]), P(s["out_topk"]), 1, p.idx_type, P(s["ws"]), s["ws"].numel())
                          for s in self.sets]
         else:  # the inverse move: the "tokens" buffers hold the expert-major rows
             self.fn = lib.mrr_v2_unroute

@@ -142,12 +142,6 @@ typedef struct mrr_v2_plan {
                                  lets a caller (a test) plant a counter value the launch must
                                  reject: a ticket beyond the launch's last one is reported as
                                  MRR_ERR_TIMEOUT and the CTAs that drew it stop at once        */
-    int32_t multi_rows_exact; /* mrr_v2_run_plan_multi only: 1 = src_rows holds each rank's
-                                 exact row count (not a capacity); a rank whose counts sum to
-                                 anything else is refused (MRR_ERR_SOURCE), and the token
-                                 stream can start before the counts are scanned; 0 (what the
-                                 plan functions set) = src_rows are capacities             */
-    int32_t reserved;         /* 0                                                          */
 } mrr_v2_plan_t;
 
 /*

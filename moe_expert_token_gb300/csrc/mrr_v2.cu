@@ -103,12 +103,6 @@ struct Params {
     int ptr_off;                    // byte offset of the pointer tables' copy in dynamic shared
                                     // memory (tokens, then scales, then top-k), or -1: read them
                                     // from global memory
-    int rows_exact;                 // src_rows are each rank's exact row counts (not capacities):
-                                    // a rank whose counts sum to anything else is refused
-    int rs_off;                     // fused bulk kernel, rows_exact: byte offset in dynamic shared
-                                    // memory of the rank starts (prefix of src_rows, N + 1 words),
-                                    // so the token stream starts before the counts are scanned;
-                                    // -1: it starts once SrcOffset is scanned
 };
 
 // The per-rank source tables the multi-source form reads: Params' global tables, or their copy in
@@ -158,11 +152,8 @@ struct SegMap {
     const uint32_t *row_ex;
     const uint32_t *dst_off;
     const uint32_t *col_ex;
-    const uint32_t *rank_start;  // multi-source form: rank i's first row, when known before the scan
     int NE, N, E;
     int inv;
-    // multi-source form: the first row of rank i (i <= N), SrcOffset(i, 0)
-    __device__ __forceinline__ uint32_t rank_row(int i) const { return rank_start ? rank_start[i] : row_ex[i * E]; }
     __device__ __forceinline__ uint32_t begin(int g) const { return inv ? col_ex[pad32(g)] : row_ex[g]; }
     // forward: DstOffset of segment g; inverse: SrcOffset of the segment at position g (the scan
     // stores it by position, so neither direction divides here)
@@ -225,7 +216,7 @@ __device__ __forceinline__ int rank_of_byte(const SegMap &m, int64_t x, int64_t 
     int lo = 0, hi = m.N;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if ((int64_t)m.rank_row(mid) * rb <= x)
+        if ((int64_t)m.row_ex[mid * m.E] * rb <= x)
             lo = mid;
         else
             hi = mid;
@@ -258,11 +249,9 @@ __device__ __forceinline__ uint32_t check_capacity(const Params &p, const uint32
 {
     uint32_t f = 0u;
     if (p.src_rows)
-        for (int i = t0; i < p.N; i += ts) {
-            const long long rows = (long long)(row_ex[(i + 1) * p.E] - row_ex[i * p.E]);
-            if (p.rows_exact ? rows != p.src_rows[i] : rows > p.src_rows[i])
+        for (int i = t0; i < p.N; i += ts)
+            if ((long long)(row_ex[(i + 1) * p.E] - row_ex[i * p.E]) > p.src_rows[i])
                 f = kFlagSource;
-        }
     return f;
 }
 
@@ -1048,8 +1037,8 @@ __device__ __forceinline__ void bulk_issue_load(const Params &p, BulkRing &r, co
         for (int64_t x = b0; x < b1;) {
             if (x < r.src_b0 || x >= r.src_b1) {
                 const int i = rank_of_byte(m, x, rb);
-                r.src_b0 = (int64_t)m.rank_row(i) * rb;
-                r.src_b1 = (int64_t)m.rank_row(i + 1) * rb;
+                r.src_b0 = (int64_t)m.row_ex[i * m.E] * rb;
+                r.src_b1 = (int64_t)m.row_ex[(i + 1) * m.E] * rb;
                 r.src_base = r.src_tab[i];
             }
             const int64_t y = min(b1, r.src_b1);
@@ -1081,7 +1070,7 @@ __device__ __forceinline__ void prefetch_src(const Params &p, const SegMap &m, c
         const int64_t rb = p.row_bytes;
         int i = rank_of_byte(m, lo, rb);
         for (int64_t x = lo; x < hi; ++i) {
-            const int64_t b0 = (int64_t)m.rank_row(i) * rb, b1 = (int64_t)m.rank_row(i + 1) * rb;
+            const int64_t b0 = (int64_t)m.row_ex[i * m.E] * rb, b1 = (int64_t)m.row_ex[(i + 1) * m.E] * rb;
             const int64_t y = min(hi, b1);
             bulk_prefetch_l2(src.tok[i] + (x - b0), (uint32_t)(y - x));
             x = y;
@@ -1226,7 +1215,6 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
     m.N = p.N;
     m.E = p.E;
     m.inv = p.inverse;
-    m.rank_start = nullptr;
     Sources src{p.src_tok, p.src_sc, p.src_tk};
     ring.src_tab = p.src_tok;
     // Multi-source form: copy the per-rank pointer tables into shared memory (their loads overlap
@@ -1323,42 +1311,6 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
         stage_pointers();
     }
 
-    // Multi-source form with each rank's exact row count given: the rank starts are the prefix of
-    // those counts, known before any count of the matrix arrives, so the token stream starts now
-    // (the pointers checked first).  The scan below still checks every rank's rows against them;
-    // a mismatch is refused before any store, and the loads stayed inside each rank's rows.
-    bool early = false;
-    if constexpr (kMulti && kBulk && kFused) {
-        if (p.rs_off >= 0) {
-            uint32_t *rs = reinterpret_cast<uint32_t *>(smem + p.rs_off);
-            uint32_t bad = 0u;
-            block_scan_runs(
-                p.N, s_warp,
-                [&](int i) {
-                    const long long r = p.src_rows[i];
-                    return (r >= 1 && r <= p.A) ? (uint32_t)r : 0u;
-                },
-                [&](int i, uint32_t v) { rs[i] = v; });
-            for (int i = tid; i < p.N; i += nthr)
-                if (p.src_rows[i] < 1 || p.src_rows[i] > p.A)
-                    bad = 1u;
-            __syncthreads();   // every exclusive prefix written
-            if (tid == 0) {
-                const long long last = p.src_rows[p.N - 1];
-                rs[p.N] = rs[p.N - 1] + (uint32_t)((last >= 1 && last <= p.A) ? last : 0);
-            }
-            __syncthreads();
-            if (rs[p.N] != (uint32_t)p.A)
-                bad = 1u;
-            bad |= check_sources(p, src, true, tid, nthr);
-            if (!__syncthreads_or(bad != 0u)) {
-                m.rank_start = rs;
-                early = true;
-                start_token_stream();
-            }
-        }
-    }
-
     uint32_t flags;
     if (kFused) {
         uint32_t *rex = tab, *cnt_t = tab + p.NE + 1, *dof = cnt_t + padded_len(p.NE);
@@ -1368,14 +1320,13 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
         if constexpr (kMulti) {
             // Once SrcOffset is scanned (rank i's rows start at SrcOffset(i, 0)), check every
             // rank's pointers and row count (uniform over the block), then start the token stream
-            // while DstOffset is scanned, unless it started early above.  Counts that fail
-            // validation return before this point.
+            // while DstOffset is scanned.  Counts that fail validation return before this point.
             uint32_t src_flag = 0u;
             auto mid = [&]() {
                 const uint32_t f = check_sources(p, src, kBulk, tid, nthr) | check_capacity(p, rex, tid, nthr);
                 if (__syncthreads_or(f != 0u))
                     src_flag = kFlagSource;
-                else if (!early)
+                else
                     start_token_stream();
             };
             flags = cta_scan(p, cb, rex, cnt_t, dof, s_warp, &s_flags, &s_sum, mid) | src_flag;
@@ -2043,10 +1994,6 @@ mrr_status run_plan_impl(const mrr_v2_plan_t *plan, const MultiSrc *ms, const vo
         return MRR_ERR_PLAN;
     if (pl.epoch < 0 || pl.epoch >= (int64_t)(1ull << (64 - kTicketBits)))
         return MRR_ERR_PLAN;
-    if (pl.multi_rows_exact != 0 && pl.multi_rows_exact != 1)
-        return MRR_ERR_PLAN;
-    if (pl.multi_rows_exact && (!ms || !ms->rows))
-        return MRR_ERR_PLAN;   // exact row counts only make sense with the multi-source tables
     int path = pl.path;
     // (multi-source: the sources' alignment is checked on the device, MRR_ERR_SOURCE)
     const bool aligned16 = rb % 16 == 0 && (ms || ((uintptr_t)tokens % 16) == 0) &&
@@ -2146,22 +2093,13 @@ mrr_status run_plan_impl(const mrr_v2_plan_t *plan, const MultiSrc *ms, const vo
     p.prefetch_chunks = path == MRR_PATH_BULK ? pl.prefetch_chunks : 0;
     p.scan_in_smem = scan_in_smem ? 1 : 0;
     p.ptr_off = -1;
-    p.rs_off = -1;
     if (ms) {
-        // the pointer tables' copy in shared memory, behind everything else, when it fits; then,
-        // with exact row counts on the fused bulk path, the rank starts
+        // the pointer tables' copy in shared memory, behind everything else, when it fits
         const int64_t pb = 8 * N * (1 + (ms->scales ? 1 : 0) + (ms->topk ? 1 : 0));
         if (round_up(smem, 16) + pb <= optin - 1024) {
             p.ptr_off = (int)round_up(smem, 16);
             smem = p.ptr_off + pb;
-            const int64_t rsb = 4 * (N + 1);
-            if (pl.multi_rows_exact && pl.fuse_scan && path == MRR_PATH_BULK &&
-                round_up(smem, 16) + rsb <= optin - 1024) {
-                p.rs_off = (int)round_up(smem, 16);
-                smem = p.rs_off + rsb;
-            }
         }
-        p.rows_exact = pl.multi_rows_exact ? 1 : 0;
         p.multi = 1;
         p.multi_bulk = path == MRR_PATH_BULK ? 1 : 0;
         p.src_tok = reinterpret_cast<const uint8_t *const *>(ms->tokens);

@@ -71,7 +71,6 @@ class mrr_v2_plan_t(ctypes.Structure):
         ("pdl", ctypes.c_int32), ("direction", ctypes.c_int32),
         ("smem_bytes", ctypes.c_int32), ("num_sms", ctypes.c_int32),
         ("prefetch_chunks", ctypes.c_int32), ("epoch", ctypes.c_int64),
-        ("multi_rows_exact", ctypes.c_int32), ("reserved", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:
@@ -378,9 +377,8 @@ def moe_re_routing_multi(tokens_per_rank, expert_token_num_per_rank, *, per_toke
     ``tokens_per_rank[i]`` is a [rows_i, H] tensor holding rank i's rows (the rows row i of the
     count matrix describes), and so are the optional per-rank lists ``per_token_scales`` and
     ``expert_topk_weight`` ([rows_i, 1] float32).  The outputs equal ``moe_re_routing`` on the
-    concatenation of the lists.  Each rank's row count (rows_i) is passed along as exact, so the
-    token stream can start before the counts are scanned, and counts whose row i does not sum to
-    rows_i are refused on the device (raised with ``check_status=True``)."""
+    concatenation of the lists; each rank's capacity (rows_i) is passed along, so counts that do
+    not fit a rank's tensor raise instead of reading past it (with ``check_status=True``)."""
     import torch
 
     ts, c = list(tokens_per_rank), expert_token_num_per_rank
@@ -440,18 +438,15 @@ def moe_re_routing_multi(tokens_per_rank, expert_token_num_per_rank, *, per_toke
     def ptr(x):
         return None if x is None else x.data_ptr()
 
-    # the tensors' row counts are exact: the kernel may start the token stream before the counts
-    # are scanned, and refuses counts whose rank sums differ from them
-    plan.path = MRR_PATH_AUTO
-    plan.multi_rows_exact = 1
     with torch.cuda.device(dev):
-        st = mrr_v2_run_plan_multi(plan, ptr(t_tok), ptr(t_sc), ptr(t_tw), ptr(rows), code, ptr(c),
-                                   ptr(out_tok), ptr(out_sc) if per_token_scales is not None else None,
-                                   ptr(idx), ptr(etn), ptr(out_tw) if expert_topk_weight is not None else None,
-                                   expert_token_num_type, workspace.data_ptr(), workspace.numel(),
-                                   stream.cuda_stream)
+        st = mrr_v2_run_multi(ptr(t_tok), ptr(t_sc), ptr(t_tw), ptr(rows), code, A, H, ptr(c),
+                              c.dtype == torch.int64, N, E, sl, scale_cols, ptr(out_tok),
+                              ptr(out_sc) if per_token_scales is not None else None, ptr(idx), ptr(etn),
+                              ptr(out_tw) if expert_topk_weight is not None else None,
+                              expert_token_num_type, idx_type, workspace.data_ptr(), workspace.numel(),
+                              stream.cuda_stream)
         if st != MRR_OK:
-            raise MrrError(st, "mrr_v2_run_plan_multi")
+            raise MrrError(st, "mrr_v2_run_multi")
         # the tables must outlive the enqueued work: keep them with the stream's pending work
         for x in (t_tok, t_sc, t_tw, rows):
             if x is not None:

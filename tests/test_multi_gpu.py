@@ -45,15 +45,14 @@ def rank_rows(counts: np.ndarray) -> np.ndarray:
 
 def run_gpu_multi(p, *, layout="separate", path=None, edit=None, src_offset=0, sc_offset=0, tk_offset=0,
                   spare_rows=0, rows_given=True, rows_override=None, null_rank=None, counts=None,
-                  workspace=None, device="cuda:0", expect_host_status=m.MRR_OK, exact=False):
+                  workspace=None, device="cuda:0", expect_host_status=m.MRR_OK):
     """Run the multi-source form on problem ``p``: rank i's token / scale / top-k rows are cut
     out of the problem's rank-major arrays and placed in per-rank buffers.
 
     layout "separate": one guard-banded buffer per rank and array, starting ``*_offset`` bytes
     past an aligned address; "slots": one buffer per array holding N slots of
     (rows_i + spare_rows) rows each (the capacity passed in src_rows).  ``null_rank`` puts NULL
-    in the token table for that rank.  ``exact``: src_rows holds each rank's exact row count
-    (plan.multi_rows_exact); every buffer still holds at least that many rows."""
+    in the token table for that rank."""
     import torch
 
     d = torch.device(device)
@@ -88,10 +87,7 @@ def run_gpu_multi(p, *, layout="separate", path=None, edit=None, src_offset=0, s
         cap = np.full(N, int(cap.max()))
     src_rows = None
     if rows_given:
-        given = rows if exact else cap
-        src_rows = torch.tensor(given if rows_override is None else rows_override, dtype=torch.int64, device=d)
-    if exact:
-        edit = dict(edit or {}, multi_rows_exact=1)
+        src_rows = torch.tensor(cap if rows_override is None else rows_override, dtype=torch.int64, device=d)
     cnt = DevBuf.of(c, d)
     out_tok = DevBuf(p.A * p.row_bytes, d)
     out_sc = None if p.scales is None else DevBuf(p.A * p.scale_row_bytes, d)
@@ -268,62 +264,3 @@ def test_torch_level_call_matches_single_source():
     with pytest.raises(m.MrrError) as err:
         m.moe_re_routing_multi(moved, cnt, check_status=True)
     assert err.value.code == m.MRR_ERR_SOURCE
-
-
-# ------------------------------------------------------------------------------ exact row counts
-
-@pytest.mark.parametrize("k", [2, 3, 4, 5])
-def test_workload_full_size_exact_rows(k):
-    """plan.multi_rows_exact: src_rows holds each rank's exact row count, so the kernel starts the
-    token stream from their prefix before the count matrix is scanned.  Bit-exact at full size,
-    in separate buffers and in receive slots with spare rows."""
-    p, ref = workload(k)
-    assert_bit_exact(run_gpu_multi(p, exact=True), ref, p)
-    if k in (4, 5):
-        assert_bit_exact(run_gpu_multi(p, layout="slots", spare_rows=5, exact=True), ref, p)
-
-
-@pytest.mark.parametrize("c", [c for c in FUZZ if c["off"] == 0 and c["N"] * c["E"] > 1],
-                         ids=lambda c: f"case{c['case']}-{c['dt']}-H{c['H']}-{c['N']}x{c['E']}")
-def test_fuzz_exact_rows(c):
-    rng = np.random.default_rng(5000 + c["case"])
-    NE = c["N"] * c["E"]
-    row_bytes = c["H"] * (4 if c["dt"].startswith("float4") else 8 if "8" in c["dt"] or c["dt"] == "int8"
-                          else 16) // 8
-    A = int(max(NE, min(3 * NE + int(rng.integers(0, 5000)), (64 << 20) // max(1, row_bytes))))
-    scale_cols = {"none": 0, "f32_a": 1, "f32_as": 3, "e8m0": 2 * int(rng.integers(1, 60))}[c["sl"]]
-    p = workloads.make_problem(rng, A=A, H=c["H"], N=c["N"], E=c["E"], token_dtype=c["dt"],
-                               count_dtype=np.int64 if c["i64"] else np.int32, scale_layout=c["sl"],
-                               scale_cols=scale_cols, has_topk=c["topk"], idx_type=c["idx"])
-    assert_bit_exact(run_gpu_multi(p, layout=c["layout"], spare_rows=c["case"] % 7, exact=True),
-                     oracle.run_problem(p), p)
-
-
-@pytest.mark.parametrize("N,E", [(8, 8), (16, 16), (90, 60)], ids=["fused-64", "fused-256", "scan-kernel"])
-@pytest.mark.parametrize("shift", ["moved", "added"])
-def test_exact_rows_that_disagree_with_the_counts_are_refused(N, E, shift):
-    """With exact rows the counts must sum, rank by rank, to src_rows.  A row moved from one rank
-    to another (the total still A, so the early token stream starts) or added to one rank (the
-    total off) is refused with MRR_ERR_SOURCE and nothing is stored.  Every buffer is a receive
-    slot with spare rows, so even the misstated counts stay inside the buffers."""
-    rng = np.random.default_rng(31 * N + E)
-    p = workloads.make_problem(rng, A=3 * N * E + 100, H=512, N=N, E=E, token_dtype="bfloat16",
-                               scale_layout="f32_a", scale_cols=1, has_topk=True)
-    rows = np.diff(rank_rows(p.counts))
-    wrong = rows.copy()
-    wrong[N // 3] += 1
-    if shift == "moved":
-        wrong[N - 1] -= 1
-    ws = DevBuf(1 << 20, "cuda:0")
-    bad = run_gpu_multi(p, layout="slots", spare_rows=3, exact=True, rows_override=wrong, workspace=ws)
-    assert bad["status"] == m.MRR_ERR_SOURCE, m.mrr_status_str(bad["status"])
-    assert bad["guards_intact"] and bad["inputs_intact"]
-    assert (bad["permute_tokens"] == 0xA5).all()
-    assert_bit_exact(run_gpu_multi(p, layout="slots", spare_rows=3, exact=True, workspace=ws),
-                     oracle.run_problem(p), p)
-
-
-def test_exact_rows_need_the_row_table():
-    p = workloads.config(1)
-    out = run_gpu_multi(p, exact=True, rows_given=False, expect_host_status=m.MRR_ERR_PLAN)
-    assert out["host_status"] == m.MRR_ERR_PLAN
