@@ -482,6 +482,7 @@ def timed_steps(setup, K, W, stream, dev, dist=None, clocks=None):
 
 
 OTHER_CONFIGS = (3, 4, 5)
+STEADY_K = 500
 
 
 def run_gpu(args):
@@ -563,11 +564,18 @@ def run_gpu(args):
             ms_k, first_k = timed_steps(su, K, args.warmup, stream, dev, dist)
             ms_k = max_over_ranks(ms_k, dist, dev)
             gbs_k = throughput_gbs(world, su.bytes_step, K, ms_k)
+            # the same launches over a longer region, where the first launch's start-up after
+            # the synchronize weighs 1/STEADY_K instead of 1/K
+            ms_s, _ = timed_steps(su, STEADY_K, args.warmup, stream, dev, dist)
+            ms_s = max_over_ranks(ms_s, dist, dev)
+            gbs_s = throughput_gbs(world, su.bytes_step, STEADY_K, ms_s)
             others[f"C{k}"] = {
                 "workload": q.name, "value": gbs_k, "unit": "GB/s", "ms_per_step": ms_k / K,
                 "pct_of_peak": 100.0 * gbs_k / world / peak, "frac": gbs_k / world / peak,
                 "tokens_per_s": world * q.A * K / (ms_k * 1e-3), "bytes_per_step": su.bytes_step,
                 "gpu_launches": K * su.launches_per_step, "first_step_us": first_k,
+                "steady_state": {"steps": STEADY_K, "ms_per_step": ms_s / STEADY_K,
+                                 "frac": gbs_s / world / peak},
                 "path": {1: "bulk", 2: "vector"}[su.plan.path], "grid": su.plan.grid,
                 "fused_scan": bool(su.plan.fuse_scan),
                 "traffic": profiled_traffic(k, "route"),

@@ -415,13 +415,17 @@ def moe_re_routing_multi(tokens_per_rank, expert_token_num_per_rank, *, per_toke
     if st != MRR_OK:
         raise MrrError(st, "mrr_v2_plan")
 
-    def table(lst):   # a device array of the tensors' addresses
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+
+    def table(lst):   # a device array of the tensors' addresses, uploaded on the op's stream
         if lst is None:
             return None
         return torch.tensor([x.data_ptr() for x in lst], dtype=torch.int64, device=dev)
 
-    t_tok, t_sc, t_tw = table(ts), table(per_token_scales), table(expert_topk_weight)
-    rows = torch.tensor([int(t.shape[0]) for t in ts], dtype=torch.int64, device=dev)
+    with torch.cuda.device(dev), torch.cuda.stream(stream):
+        t_tok, t_sc, t_tw = table(ts), table(per_token_scales), table(expert_topk_weight)
+        rows = torch.tensor([int(t.shape[0]) for t in ts], dtype=torch.int64, device=dev)
     out_tok = torch.empty((A,) + tuple(ts[0].shape[1:]), dtype=ts[0].dtype, device=dev)
     out_sc = (torch.empty((A,) + tuple(per_token_scales[0].shape[1:]), dtype=per_token_scales[0].dtype,
                           device=dev)
@@ -432,8 +436,6 @@ def moe_re_routing_multi(tokens_per_rank, expert_token_num_per_rank, *, per_toke
               else torch.empty(0, dtype=torch.float32, device=dev))
     if workspace is None or workspace.numel() < plan.workspace_bytes:
         workspace = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
-    if stream is None:
-        stream = torch.cuda.current_stream(dev)
 
     def ptr(x):
         return None if x is None else x.data_ptr()
