@@ -184,7 +184,43 @@ __device__ __forceinline__ void load_run(float (&v)[VPL], const Params &p, long 
 
 // The two element-wise normalisations.  Both rank-by-logit rows and fully evaluated rows call
 // these, so a score is the same float whichever path computed it.
-__device__ __forceinline__ float sigmoid_score(float x) { return __frcp_rn(1.f + expf(-x)); }
+//
+// Sigmoid: 1 / (1 + e^-x) with e^-x = 2^(-x log2 e).  The product -x log2 e is carried in two
+// floats, hi + lo (Cody and Waite's split of the constant, "Software Manual for the Elementary
+// Functions", 1980: log2 e = kHi + kLo with kHi a float, and an fma recovers the rounding error of
+// -x kHi exactly).  The hardware base-2 exponential (ex2.approx) takes hi, the first-order factor
+// 2^lo = 1 + lo ln 2 corrects for lo, and rcp.approx gives the reciprocal.  Rounding -x log2 e to
+// one float instead would cost up to |x| 2^-24 ln 2 of relative error, about 17 ulp at |x| = 25.
+// lo is tiny wherever 2^hi is a normal float; where 2^hi is 0 or inf (|x| above about 88, or
+// x = +-inf, where lo is huge, infinite or NaN) the clamp to [-1, 1] keeps the factor finite and
+// positive, so 0 and inf pass through (sigmoid 1 or 0), and a NaN logit stays NaN.
+// Subnormals flush: 2^hi below 2^-126 leaves 1 + 2^hi = 1, and a sigmoid below 2^-126
+// (x < -87.3) comes out 0.  Over every float16 and bfloat16 logit the result is within a few
+// float32 ulps of the exact sigmoid (tests/test_gating_gpu.py measures it).
+__device__ __forceinline__ float ex2_approx_ftz(float t)
+{
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
+    return r;
+}
+
+__device__ __forceinline__ float rcp_approx_ftz(float t)
+{
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
+    return r;
+}
+
+__device__ __forceinline__ float sigmoid_score(float x)
+{
+    constexpr float kHi = 1.44269502162933349609375f;   // log2 e rounded to float
+    constexpr float kLo = 1.9259629911266175e-8f;        // log2 e - kHi
+    constexpr float kLn2 = 0.693147180559945309f;
+    const float hi = -x * kHi;
+    const float lo = fminf(fmaxf(fmaf(-x, kLo, fmaf(-x, kHi, -hi)), -1.f), 1.f);
+    const float e = ex2_approx_ftz(hi) * fmaf(lo, kLn2, 1.f);
+    return rcp_approx_ftz(1.f + e);
+}
 
 __device__ __forceinline__ float softplus_score(float x)
 {
@@ -239,20 +275,21 @@ __device__ __forceinline__ void normalise_and_bias(float (&v)[VPL], int norm_typ
     }
 }
 
-// A lane's view of its run during the picks: the three best remaining keys (b1 >= b2 >= b3, with
-// their slots), whether those three are all that remain, and the last key the lane gave up.  Keys
-// leave a lane in (key descending, slot ascending) order, so "remaining" means: below the last key
-// given up, or equal to it at a later slot.  Three rather than two: on the grouped 256-expert case
-// the eight picks crowd into the kept groups' 16 lanes, and a two-key cache rescanned about 1.3
-// times per row (a top-3 cache 0.13 times); measured 6.7 % faster on GB300.
+// A lane's view of its run during the picks: its three best remaining keys (b1 >= b2 >= b3) with
+// their experts, and what moves in behind b3 when one is given up: 0 when those three were all the
+// lane had, else kRefill.  A lane whose b1 reads kRefill has given up its three and must look at
+// its run again before the next pick.  Three rather than two: on the grouped 256-expert case the
+// eight picks crowd into the kept groups' 16 lanes, and a two-key cache rescanned about 1.3 times
+// per row (a top-3 cache 0.13 times).
+constexpr uint32_t kRefill = 0xffffffffu;   // above every key but a NaN score's
+
 struct LaneCands {
-    uint32_t b1, b2, b3, last_key;
-    int u1, u2, u3, last_u;
-    bool complete;
+    uint32_t b1, b2, b3, fill;
+    uint32_t u1, u2, u3;
 };
 
-// insert key (slot u) into the lane's three best; equal keys keep the earlier slot first
-__device__ __forceinline__ void insert3(LaneCands &c, uint32_t key, int u)
+// insert key (expert u) into the lane's three best; equal keys keep the earlier expert first
+__device__ __forceinline__ void insert3(LaneCands &c, uint32_t key, uint32_t u)
 {
     const bool over1 = key > c.b1, over2 = key > c.b2, over3 = key > c.b3;
     c.b3 = over2 ? c.b2 : (over3 ? key : c.b3);
@@ -263,87 +300,106 @@ __device__ __forceinline__ void insert3(LaneCands &c, uint32_t key, int u)
     c.u1 = over1 ? u : c.u1;
 }
 
-// the lane's three best keys before any pick
-template <int VPL>
-__device__ __forceinline__ void first_scan(LaneCands &c, const uint32_t (&kv)[VPL])
-{
-    c.b1 = kv[0];
-    c.u1 = 0;
-    c.b2 = c.b3 = 0u;
-    c.u2 = c.u3 = 0;
-#pragma unroll
-    for (int u = 1; u < VPL; ++u)
-        insert3(c, kv[u], u);
-    c.complete = c.b3 == 0u;
-    c.last_key = 0xffffffffu;
-    c.last_u = -1;
-}
-
-// the lane's three best remaining keys after some picks
-template <int VPL>
-__device__ __forceinline__ void rescan(LaneCands &c, const uint32_t (&kv)[VPL])
+// the lane's three best keys among those `live` admits (the run starts at expert j0)
+template <int VPL, typename Live>
+__device__ __forceinline__ void scan3(LaneCands &c, const uint32_t (&kv)[VPL], uint32_t j0, Live live)
 {
     c.b1 = c.b2 = c.b3 = 0u;
-    c.u1 = c.u2 = c.u3 = 0;
+    c.u1 = c.u2 = c.u3 = j0;
 #pragma unroll
-    for (int u = 0; u < VPL; ++u) {
-        const uint32_t key = kv[u];
-        const bool live = key < c.last_key || (key == c.last_key && u > c.last_u);
-        insert3(c, live ? key : 0u, u);
-    }
-    c.complete = c.b3 == 0u;
+    for (int u = 0; u < VPL; ++u)
+        insert3(c, live(kv[u], j0 + u) ? kv[u] : 0u, j0 + u);
+    c.fill = c.b3 == 0u ? 0u : kRefill;
 }
 
-// The k picks over 32-bit keys: the largest remaining key, ties to the lower expert index (two
-// redux.sync per pick).  Lane i returns pick i's key and expert in (k0, i0), pick i + 32's in
-// (k1, i1); keys 0 are no candidates.
 template <int VPL>
-__device__ __forceinline__ void pick_keys(const uint32_t (&kv)[VPL], int j0, int lane, int k, uint32_t &k0,
-                                          uint32_t &i0, uint32_t &k1, uint32_t &i1)
+__device__ __forceinline__ void first_scan(LaneCands &c, const uint32_t (&kv)[VPL], uint32_t j0)
 {
-    LaneCands c;
-    first_scan<VPL>(c, kv);
-    k0 = k1 = 0u;
-    for (int i = 0; i < k; ++i) {
-        const uint32_t top = __reduce_max_sync(kFull, c.b1);
-        const uint32_t mine = (uint32_t)(j0 + c.u1);
-        const bool has_top = c.b1 == top;
-        const uint32_t win = __reduce_min_sync(kFull, has_top ? mine : kNoIndex);
-        if (i < 32) {
-            k0 = lane == i ? top : k0;
-            i0 = lane == i ? win : i0;
-        } else {
-            k1 = lane == i - 32 ? top : k1;
-            i1 = lane == i - 32 ? win : i1;
+    scan3<VPL>(c, kv, j0, [](uint32_t, uint32_t) { return true; });
+}
+
+// A lane that has given up its three cached keys looks at its run again: the keys still there are
+// those below the last key it gave up, or equal to it at a later expert (keys leave a lane in
+// that order).  The last key it gave up is found among the n picks so far.  Rarely taken, so it is
+// a call of its own: the run is passed by value and the pick loop keeps its registers.
+template <int VPL>
+struct KeyRun {
+    uint32_t k[VPL];
+};
+
+template <int VPL>
+__device__ __noinline__ LaneCands refill(const KeyRun<VPL> run, uint32_t j0, const uint2 *s_pick, int n)
+{
+    bool gave = false;
+    uint32_t last_key = 0u, last_u = 0u;
+    for (int p = 0; p < n; ++p) {
+        const uint2 q = s_pick[p];
+        if (q.y - j0 < (uint32_t)VPL) {
+            gave = true;
+            last_key = q.x;
+            last_u = q.y;
         }
-        bool need = false;
-        if (has_top && mine == win) {   // this lane gave the pick
-            c.last_key = c.b1;
-            c.last_u = c.u1;
+    }
+    LaneCands c;
+    scan3<VPL>(c, run.k, j0, [&](uint32_t key, uint32_t u) {
+        return !gave || key < last_key || (key == last_key && u > last_u);
+    });
+    return c;
+}
+
+// The k picks: each is the largest remaining key over the warp, ties to the lower expert (two
+// redux.sync).  Expert numbers are distinct across lanes, so the lane whose b1 is the winning
+// expert is the one that gave the pick; it records the pick in s_pick[i] (64 entries per warp).
+// Lane i returns pick i's key and expert in (k0, i0), pick i + 32's in (k1, i1).
+template <int VPL>
+__device__ __forceinline__ void pick_keys(LaneCands &c, const uint32_t (&kv)[VPL], int j0, int lane, int k,
+                                          uint2 *s_pick, uint32_t &k0, uint32_t &i0, uint32_t &k1, uint32_t &i1)
+{
+    for (int i = 0; i < k; ++i) {
+        uint32_t top = __reduce_max_sync(kFull, c.b1);
+        if (top == kRefill) {   // some lane has used up its cache (or the row holds a NaN score)
+            __syncwarp();
+            if (c.b1 == kRefill) {
+                KeyRun<VPL> run;
+#pragma unroll
+                for (int u = 0; u < VPL; ++u)
+                    run.k[u] = kv[u];
+                c = refill<VPL>(run, (uint32_t)j0, s_pick, i);
+            }
+            top = __reduce_max_sync(kFull, c.b1);
+        }
+        const uint32_t win = __reduce_min_sync(kFull, c.b1 == top ? c.u1 : kNoIndex);
+        if (c.u1 == win) {
+            s_pick[i] = make_uint2(top, win);
             c.b1 = c.b2;
             c.u1 = c.u2;
             c.b2 = c.b3;
             c.u2 = c.u3;
-            c.b3 = 0u;
-            need = !c.complete && c.b1 == 0u;
+            c.b3 = c.fill;
         }
-        if (__any_sync(kFull, need) && need)
-            rescan<VPL>(c, kv);
     }
+    __syncwarp();
+    const uint2 p0 = lane < k ? s_pick[lane] : make_uint2(0u, 0u);
+    const uint2 p1 = lane + 32 < k ? s_pick[lane + 32] : make_uint2(0u, 0u);
+    __syncwarp();   // the next row's picks overwrite s_pick
+    k0 = p0.x;
+    i0 = p0.y;
+    k1 = p1.x;
+    i1 = p1.y;
 }
 
-// CTAs per SM each width is compiled for (its register budget: 48, 48, 64 or 80 per thread).
+// CTAs per SM each width is compiled for (its register budget: 40, 48, 64 or 80 per thread).
 // Measured on GB300: 5 CTAs for 12 experts per lane beat 4 by 3.6 %; 6 CTAs for 8 per lane (40
-// registers) was 7 % slower than 5.
-constexpr int min_ctas_per_sm(int vpl) { return vpl <= 12 ? 5 : (vpl <= 16 ? 4 : 3); }
+// registers) beat 5 by 2 % on the grouped 256-expert case once the picks kept no last-key state.
+constexpr int min_ctas_per_sm(int vpl) { return vpl <= 8 ? 6 : (vpl <= 12 ? 5 : (vpl <= 16 ? 4 : 3)); }
 
 // Steps 1-3 of the page for row t with every score evaluated: normalise the lane's run, add the
 // bias, rank the groups, make the k picks (or look the experts up for hash routing).  Lane i
 // returns pick i in (y0, i0) and pick i + 32 in (y1, i1).
 template <int VPL, int DT>
 __device__ __forceinline__ void full_row(const Params &p, int t, int lane, int j0, int nv, float *smem,
-                                         float *s_row, uint32_t *s_gkey, uint32_t *s_kept, uint32_t &flags,
-                                         float &y0, uint32_t &i0, float &y1, uint32_t &i1)
+                                         float *s_row, uint32_t *s_gkey, uint32_t *s_kept, uint2 *s_pick,
+                                         uint32_t &flags, float &y0, uint32_t &i0, float &y1, uint32_t &i1)
 {
     const int e = p.e, k = p.k;
     // ---- steps 1-2
@@ -405,23 +461,21 @@ __device__ __forceinline__ void full_row(const Params &p, int t, int lane, int j
                 kv[u] = 0u;
     }
 
+    LaneCands c;
     if (p.group_path == kLaneGroups) {
-        // each group is an aligned block of lanes_per_group lanes (a power of two)
+        // each group is an aligned block of lanes_per_group lanes (a power of two); the group's
+        // two best keys come from the lanes' caches
+        first_scan<VPL>(c, kv, (uint32_t)j0);
         const int lpg = p.lanes_per_group;
         const int g = lane >> p.lpg_shift;
         const bool member = g < p.group_count;
-        float m1 = v[0], m2 = -INFINITY;
-#pragma unroll
-        for (int u = 1; u < VPL; ++u) {
-            m2 = fmaxf(m2, fminf(m1, v[u]));
-            m1 = fmaxf(m1, v[u]);
-        }
+        uint32_t g1 = c.b1, g2 = c.b2;
         for (int o = 1; o < lpg; o <<= 1) {
-            const float o1 = __shfl_xor_sync(kFull, m1, o), o2 = __shfl_xor_sync(kFull, m2, o);
-            m2 = fmaxf(fmaxf(m2, o2), fminf(m1, o1));
-            m1 = fmaxf(m1, o1);
+            const uint32_t o1 = __shfl_xor_sync(kFull, g1, o), o2 = __shfl_xor_sync(kFull, g2, o);
+            g2 = max(max(g2, o2), min(g1, o1));
+            g1 = max(g1, o1);
         }
-        const uint32_t gkey = order_key(p.select_mode == 0 ? m1 : m1 + m2);
+        const uint32_t gkey = p.select_mode == 0 ? g1 : order_key(key_value(g1) + key_value(g2));
         const bool leader = member && (lane & (lpg - 1)) == 0;
         bool kept = false;
         for (int r = 0; r < p.k_group; ++r) {
@@ -430,12 +484,12 @@ __device__ __forceinline__ void full_row(const Params &p, int t, int lane, int j
             const uint32_t win = __reduce_min_sync(kFull, cand && gkey == top ? (uint32_t)g : kNoIndex);
             kept = kept || (member && (uint32_t)g == win);
         }
-        if (!kept) {
-#pragma unroll
-            for (int u = 0; u < VPL; ++u)
-                kv[u] = 0u;
+        if (!kept) {   // a dropped group's experts leave the candidates
+            c.b1 = c.b2 = c.b3 = 0u;
+            c.fill = 0u;
         }
-    } else if (p.group_path == kSmemGroups) {
+    } else {
+    if (p.group_path == kSmemGroups) {
         const int G = p.group_count, gs = p.group_size;
 #pragma unroll
         for (int u = 0; u < VPL; ++u)
@@ -481,9 +535,11 @@ __device__ __forceinline__ void full_row(const Params &p, int t, int lane, int j
         }
         __syncwarp();
     }
+    first_scan<VPL>(c, kv, (uint32_t)j0);
+    }
 
     uint32_t k0, k1;
-    pick_keys<VPL>(kv, j0, lane, k, k0, i0, k1, i1);
+    pick_keys<VPL>(c, kv, j0, lane, k, s_pick, k0, i0, k1, i1);
     y0 = key_value(k0);
     y1 = key_value(k1);
     }
@@ -685,8 +741,8 @@ __device__ __forceinline__ bool logit_ranked_row(const Params &p, int t, int lan
 // must score strictly above pick k (then every expert left out scores below pick k - 1).  The
 // other picks are checked as for 16-bit logits.
 template <int VPL>
-__device__ __forceinline__ bool logit_ranked_row_f32(const Params &p, int t, int lane, int j0, int nv, float &y,
-                                                     uint32_t &idx)
+__device__ __forceinline__ bool logit_ranked_row_f32(const Params &p, int t, int lane, int j0, int nv,
+                                                     uint2 *s_pick, float &y, uint32_t &idx)
 {
     const int k = p.k;
     float v[VPL];
@@ -702,7 +758,9 @@ __device__ __forceinline__ bool logit_ranked_row_f32(const Params &p, int t, int
                 kv[u] = 0u;
     }
     uint32_t key, k1, i1;
-    pick_keys<VPL>(kv, j0, lane, k + 1, key, idx, k1, i1);   // lane k: the first expert left out
+    LaneCands c;
+    first_scan<VPL>(c, kv, (uint32_t)j0);
+    pick_keys<VPL>(c, kv, j0, lane, k + 1, s_pick, key, idx, k1, i1);   // lane k: the first expert left out
     LogitScorer score{p.norm_type, 0.f, 0.f};
     if (p.norm_type == 0) {   // the run again (an L1 hit), rather than held across the picks
         load_run<VPL, MRR_GATE_F32>(v, p, t, j0);
@@ -750,6 +808,8 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(VPL)) gating_kernel(
     uint32_t *s_gkey = p.sm_gkey >= 0 ? reinterpret_cast<uint32_t *>(smem) + p.sm_gkey + warp * p.group_count
                                       : nullptr;
     uint32_t *s_kept = p.sm_kept >= 0 ? reinterpret_cast<uint32_t *>(smem) + p.sm_kept + warp * 32 : nullptr;
+    __shared__ uint2 s_pick_all[kWarps][64];   // each warp's picks of its current row
+    uint2 *s_pick = s_pick_all[warp];
 
     // rank by logit: the inverted expert numbers of the lane's run, two per word
     uint32_t ip[(VPL + 1) / 2];
@@ -775,7 +835,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(VPL)) gating_kernel(
         uint32_t i0 = 0u, i1 = 0u;
         bool done = false;
         if constexpr (kByLogit && DT == MRR_GATE_F32) {
-            done = logit_ranked_row_f32<VPL>(p, t, lane, j0, nv, y0, i0);
+            done = logit_ranked_row_f32<VPL>(p, t, lane, j0, nv, s_pick, y0, i0);
         } else if constexpr (kByLogit) {
             uint32_t w[W];
             if (kAhead) {
@@ -790,7 +850,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(VPL)) gating_kernel(
             done = logit_ranked_row<VPL, DT>(p, t, lane, nv, w, ip, y0, i0);
         }
         if (!done)
-            full_row<VPL, DT>(p, t, lane, j0, nv, smem, s_row, s_gkey, s_kept, flags, y0, i0, y1, i1);
+            full_row<VPL, DT>(p, t, lane, j0, nv, smem, s_row, s_gkey, s_kept, s_pick, flags, y0, i0, y1, i1);
 
         // ---- step 4: scale and write
         const bool has0 = lane < k, has1 = lane + 32 < k;

@@ -449,3 +449,34 @@ def test_rank_by_logit_misaligned_rows(dt, e):
         assert np.array_equal(fast["expert_idx"], full["expert_idx"])
         assert np.array_equal(fast["y_out"].view(np.uint32), full["y_out"].view(np.uint32))
         check_against_oracle(fast, ref, dt, kw)
+
+
+def _ordered(f32: np.ndarray) -> np.ndarray:
+    """float32 values as integers that step by one per representable float (-0 and +0 equal)."""
+    b = f32.astype(np.float32).view(np.int32).astype(np.int64)
+    return np.where(b < 0, -(b & 0x7FFFFFFF), b)
+
+
+@pytest.mark.parametrize("dt", ["float16", "bfloat16"])
+@pytest.mark.parametrize("norm_type,bound", [(1, 4), (2, 3)])
+def test_scores_of_every_16bit_logit(dt, norm_type, bound):
+    """Sigmoid and softplus scores (norm_out, no bias) for every finite 16-bit logit, against the
+    exact function rounded to float32: within `bound` float32 ulps.  Where the exact score is
+    below the smallest normal float, the kernel may flush it to zero (归一化公式)."""
+    import torch
+
+    bits = np.arange(65536, dtype=np.uint16)
+    x = torch.from_numpy(bits.view(np.int16).copy()).view(getattr(torch, dt)).float().numpy()
+    x[~np.isfinite(x)] = 0.0
+    x = x.reshape(256, 256)
+    gpu = run_gpu_gating(x, dt, 1, norm_type=norm_type)
+    assert gpu["status"] == m.MRR_OK and gpu["guards"]
+    xd = x.astype(np.float64)
+    exact = 1.0 / (1.0 + np.exp(-xd)) if norm_type == 1 else np.logaddexp(0.0, xd)
+    exact32 = exact.astype(np.float32)
+    got = gpu["norm_out"]
+    tiny = np.abs(exact) < np.finfo(np.float32).tiny
+    assert np.all(np.abs(got[tiny]) < np.finfo(np.float32).tiny)
+    ulps = np.abs(_ordered(got) - _ordered(exact32))[~tiny]
+    print(f"{dt} norm_type {norm_type}: max {ulps.max()} ulp, mean {ulps.mean():.3f}")
+    assert ulps.max() <= bound
