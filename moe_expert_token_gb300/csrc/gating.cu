@@ -131,9 +131,15 @@ extern "C" mrr_status mrr_gating_topk_run(const void *x, mrr_gate_dtype dt, int6
     const bool by_logit = !hashing &&
                           p.group_path == kNoGroups && p.sm_bias < 0 && p.sm_extra < 0 && !norm_out &&
                           k <= (dt == MRR_GATE_F32 ? 31 : 32);
-    const cudaError_t err = dt == MRR_GATE_F32    ? launch_f32(p, vpl, by_logit, smem, sms, stream)
-                            : dt == MRR_GATE_BF16 ? launch_bf16(p, vpl, by_logit, smem, sms, stream)
-                                                  : launch_f16(p, vpl, by_logit, smem, sms, stream);
+    // the grouped sigmoid instance: every condition its kernel takes as fixed (see full_row)
+    const bool grouped_sigmoid = !by_logit && !hashing && p.group_path == kLaneGroups && group_count == 8 &&
+                                 k == kFixedK && norm_type == 1 &&
+                                 p.sm_bias == 0 && p.sm_extra < 0 && !norm_out && e == 32 * (int64_t)vpl &&
+                                 p.vec_bytes == 16 && (vpl == 4 || vpl == 8 || vpl == 12 || vpl == 16);
+    const int path = by_logit ? kPathLogit : (grouped_sigmoid ? kPathGroupedSigmoid : kPathFull);
+    const cudaError_t err = dt == MRR_GATE_F32    ? launch_f32(p, vpl, path, smem, sms, stream)
+                            : dt == MRR_GATE_BF16 ? launch_bf16(p, vpl, path, smem, sms, stream)
+                                                  : launch_f16(p, vpl, path, smem, sms, stream);
     if (err != cudaSuccess) {
         (void)cudaGetLastError();
         return MRR_ERR_CUDA;

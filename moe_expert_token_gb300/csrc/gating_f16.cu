@@ -4,9 +4,9 @@
 
 namespace mrr_gate {
 
-cudaError_t launch_f16(const Params &p, int vpl, bool by_logit, size_t smem, int sms, cudaStream_t stream)
+cudaError_t launch_f16(const Params &p, int vpl, int path, size_t smem, int sms, cudaStream_t stream)
 {
-    return launch_dtype<MRR_GATE_F16>(p, vpl, by_logit, smem, sms, stream);
+    return launch_dtype<MRR_GATE_F16>(p, vpl, path, smem, sms, stream);
 }
 
 }  // namespace mrr_gate

@@ -47,6 +47,8 @@ constexpr uint32_t kNoIndex = 0xffffffffu;
 constexpr int kSmemOptIn = 100 * 1024;          // the largest call needs 78,848 bytes
 
 enum GroupPath { kNoGroups = 0, kLaneGroups = 1, kSmemGroups = 2 };
+enum KernelPath { kPathFull = 0, kPathLogit = 1, kPathGroupedSigmoid = 2 };
+constexpr int kFixedK = 8;                      // the picks of the grouped sigmoid instance
 
 struct Params {
     const void *x;
@@ -119,14 +121,16 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
-// this lane's run of row `row`, experts [j0, j0 + VPL), as floats; experts at or past e read -inf
+// this lane's run of row `row` (e experts), experts [j0, j0 + VPL), as floats; experts at or past
+// e read -inf.  vec_bytes is the widest load the rows' alignment allows.
 template <int VPL, int DT>
-__device__ __forceinline__ void load_run(float (&v)[VPL], const Params &p, long long row, int j0)
+__device__ __forceinline__ void load_run(float (&v)[VPL], const void *x, long long row, int e, int j0,
+                                         int vec_bytes)
 {
-    const int nv = p.e - j0;
+    const int nv = e - j0;
     if (DT == MRR_GATE_F32) {
-        const float *src = static_cast<const float *>(p.x) + row * p.e + j0;
-        if (VPL % 4 == 0 && nv >= VPL && p.vec_bytes >= 16) {
+        const float *src = static_cast<const float *>(x) + row * e + j0;
+        if (VPL % 4 == 0 && nv >= VPL && vec_bytes >= 16) {
 #pragma unroll
             for (int c = 0; c < VPL / 4; ++c) {
                 const float4 q = __ldg(reinterpret_cast<const float4 *>(src) + c);
@@ -135,7 +139,7 @@ __device__ __forceinline__ void load_run(float (&v)[VPL], const Params &p, long 
                 v[4 * c + 2] = q.z;
                 v[4 * c + 3] = q.w;
             }
-        } else if (VPL % 2 == 0 && nv >= VPL && p.vec_bytes >= 8) {
+        } else if (VPL % 2 == 0 && nv >= VPL && vec_bytes >= 8) {
 #pragma unroll
             for (int c = 0; c < VPL / 2; ++c) {
                 const float2 q = __ldg(reinterpret_cast<const float2 *>(src) + c);
@@ -149,8 +153,8 @@ __device__ __forceinline__ void load_run(float (&v)[VPL], const Params &p, long 
         }
         return;
     }
-    const unsigned short *src = static_cast<const unsigned short *>(p.x) + row * p.e + j0;
-    if (VPL % 8 == 0 && nv >= VPL && p.vec_bytes >= 16) {
+    const unsigned short *src = static_cast<const unsigned short *>(x) + row * e + j0;
+    if (VPL % 8 == 0 && nv >= VPL && vec_bytes >= 16) {
 #pragma unroll
         for (int c = 0; c < VPL / 8; ++c) {
             const uint4 q = __ldg(reinterpret_cast<const uint4 *>(src) + c);
@@ -159,7 +163,7 @@ __device__ __forceinline__ void load_run(float (&v)[VPL], const Params &p, long 
             for (int h = 0; h < 8; ++h)
                 v[8 * c + h] = bits16_to_float<DT>(w[h >> 1] >> (16 * (h & 1)));
         }
-    } else if (VPL % 4 == 0 && nv >= VPL && p.vec_bytes >= 8) {
+    } else if (VPL % 4 == 0 && nv >= VPL && vec_bytes >= 8) {
 #pragma unroll
         for (int c = 0; c < VPL / 4; ++c) {
             const uint2 q = __ldg(reinterpret_cast<const uint2 *>(src) + c);
@@ -168,7 +172,7 @@ __device__ __forceinline__ void load_run(float (&v)[VPL], const Params &p, long 
             for (int h = 0; h < 4; ++h)
                 v[4 * c + h] = bits16_to_float<DT>(w[h >> 1] >> (16 * (h & 1)));
         }
-    } else if (VPL % 2 == 0 && nv >= VPL && p.vec_bytes >= 4) {
+    } else if (VPL % 2 == 0 && nv >= VPL && vec_bytes >= 4) {
 #pragma unroll
         for (int c = 0; c < VPL / 2; ++c) {
             const uint32_t q = __ldg(reinterpret_cast<const unsigned int *>(src) + c);
@@ -396,19 +400,28 @@ constexpr int min_ctas_per_sm(int vpl) { return vpl <= 8 ? 6 : (vpl <= 12 ? 5 : 
 // Steps 1-3 of the page for row t with every score evaluated: normalise the lane's run, add the
 // bias, rank the groups, make the k picks (or look the experts up for hash routing).  Lane i
 // returns pick i in (y0, i0) and pick i + 32 in (y1, i1).
-template <int VPL, int DT>
-__device__ __forceinline__ void full_row(const Params &p, int t, int lane, int j0, int nv, float *smem,
+//
+// kFixed: the instance for the grouped sigmoid case (DeepSeek-V3's routing shape), launched only
+// when e = 32 * VPL, x's rows take 16-byte loads, the bias row is given, the experts form 8
+// groups (each an aligned block of 4 lanes), k = kFixedK, the normalisation is sigmoid, and there
+// is no hash table, no additional bias and no norm_out.  Those are then compile-time facts: the same arithmetic in the same order as
+// the general instance, with its checks and loops over them folded away.
+template <int VPL, int DT, bool kFixed>
+__device__ __forceinline__ void full_row(const Params &p, int t, int lane, int j0, int nv_rt, float *smem,
                                          float *s_row, uint32_t *s_gkey, uint32_t *s_kept, uint2 *s_pick,
                                          uint32_t &flags, float &y0, uint32_t &i0, float &y1, uint32_t &i1)
 {
-    const int e = p.e, k = p.k;
+    const int e = kFixed ? 32 * VPL : p.e, k = kFixed ? kFixedK : p.k;
+    const int nv = kFixed ? VPL : nv_rt;
+    const int group_path = kFixed ? (int)kLaneGroups : p.group_path;
     // ---- steps 1-2
     float v[VPL];
-    load_run<VPL, DT>(v, p, t, j0);
-    const bool extra = p.sm_extra >= 0 && p.extra_mask[t];
-    const float *bias = extra ? smem + p.sm_extra + j0 : (p.sm_bias >= 0 ? smem + p.sm_bias + j0 : nullptr);
-    normalise_and_bias<VPL>(v, p.norm_type, nv, bias);
-    if (p.norm_out) {
+    load_run<VPL, DT>(v, p.x, t, e, j0, kFixed ? 16 : p.vec_bytes);
+    const bool extra = !kFixed && p.sm_extra >= 0 && p.extra_mask[t];
+    const float *bias = kFixed ? smem + j0
+                               : (extra ? smem + p.sm_extra + j0 : (p.sm_bias >= 0 ? smem + p.sm_bias + j0 : nullptr));
+    normalise_and_bias<VPL>(v, kFixed ? 1 : p.norm_type, nv, bias);
+    if (!kFixed && p.norm_out) {
         float *dst = p.norm_out + (long long)t * e + j0;
         if (VPL % 4 == 0 && nv >= VPL && p.out_vec) {
 #pragma unroll
@@ -425,7 +438,7 @@ __device__ __forceinline__ void full_row(const Params &p, int t, int lane, int j
     // ---- step 3
     y0 = y1 = 0.f;
     i0 = i1 = 0u;
-    if (p.input_ids) {
+    if (!kFixed && p.input_ids) {
         // hash routing: the table row, scores looked up in the staged row
 #pragma unroll
         for (int u = 0; u < VPL; ++u)
@@ -462,13 +475,13 @@ __device__ __forceinline__ void full_row(const Params &p, int t, int lane, int j
     }
 
     LaneCands c;
-    if (p.group_path == kLaneGroups) {
+    if (group_path == kLaneGroups) {
         // each group is an aligned block of lanes_per_group lanes (a power of two); the group's
         // two best keys come from the lanes' caches
         first_scan<VPL>(c, kv, (uint32_t)j0);
-        const int lpg = p.lanes_per_group;
-        const int g = lane >> p.lpg_shift;
-        const bool member = g < p.group_count;
+        const int lpg = kFixed ? 4 : p.lanes_per_group;
+        const int g = lane >> (kFixed ? 2 : p.lpg_shift);
+        const bool member = kFixed || g < p.group_count;
         uint32_t g1 = c.b1, g2 = c.b2;
         for (int o = 1; o < lpg; o <<= 1) {
             const uint32_t o1 = __shfl_xor_sync(kFull, g1, o), o2 = __shfl_xor_sync(kFull, g2, o);
@@ -489,7 +502,7 @@ __device__ __forceinline__ void full_row(const Params &p, int t, int lane, int j
             c.fill = 0u;
         }
     } else {
-    if (p.group_path == kSmemGroups) {
+    if (group_path == kSmemGroups) {
         const int G = p.group_count, gs = p.group_size;
 #pragma unroll
         for (int u = 0; u < VPL; ++u)
@@ -746,7 +759,7 @@ __device__ __forceinline__ bool logit_ranked_row_f32(const Params &p, int t, int
 {
     const int k = p.k;
     float v[VPL];
-    load_run<VPL, MRR_GATE_F32>(v, p, t, j0);
+    load_run<VPL, MRR_GATE_F32>(v, p.x, t, p.e, j0, p.vec_bytes);
     uint32_t kv[VPL];
 #pragma unroll
     for (int u = 0; u < VPL; ++u)
@@ -763,7 +776,7 @@ __device__ __forceinline__ bool logit_ranked_row_f32(const Params &p, int t, int
     pick_keys<VPL>(c, kv, j0, lane, k + 1, s_pick, key, idx, k1, i1);   // lane k: the first expert left out
     LogitScorer score{p.norm_type, 0.f, 0.f};
     if (p.norm_type == 0) {   // the run again (an L1 hit), rather than held across the picks
-        load_run<VPL, MRR_GATE_F32>(v, p, t, j0);
+        load_run<VPL, MRR_GATE_F32>(v, p.x, t, p.e, j0, p.vec_bytes);
         score.mx = key_value(__shfl_sync(kFull, key, 0));
         score.r = softmax_rcp<VPL>(v, nv, score.mx);
     }
@@ -782,14 +795,16 @@ __device__ __forceinline__ bool logit_ranked_row_f32(const Params &p, int t, int
 }
 
 // VPL = experts per lane (the row's e <= 32 * VPL scores live in registers); DT = x's type;
-// kByLogit: rank by logit (no bias, no groups, no hash routing, no norm_out, k <= 32, or k <= 31
-// for float32 x), with the full evaluation as the fallback.
-template <int VPL, int DT, bool kByLogit>
+// kPath: kPathFull evaluates every score; kPathLogit ranks by logit (no bias, no groups, no hash
+// routing, no norm_out, k <= 32, or k <= 31 for float32 x), with the full evaluation as the
+// fallback; kPathGroupedSigmoid is the full evaluation specialised as full_row's kFixed says.
+template <int VPL, int DT, int kPath>
 __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(VPL)) gating_kernel(const Params p)
 {
+    constexpr bool kByLogit = kPath == kPathLogit, kFixed = kPath == kPathGroupedSigmoid;
     extern __shared__ __align__(16) float smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = p.e, k = p.k, j0 = lane * VPL, nv = e - j0;
+    const int e = kFixed ? 32 * VPL : p.e, k = kFixed ? kFixedK : p.k, j0 = lane * VPL, nv = e - j0;
 
     // no global memory touched above: wait for the previous kernel on the stream, then let the
     // next launch be scheduled (programmatic stream serialization)
@@ -800,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(VPL)) gating_kernel(
     if (p.sm_bias >= 0)
         for (int j = threadIdx.x; j < e; j += kThreads)
             smem[p.sm_bias + j] = load_as_float(p.bias, DT, j);
-    if (p.sm_extra >= 0)
+    if (!kFixed && p.sm_extra >= 0)
         for (int j = threadIdx.x; j < e; j += kThreads)
             smem[p.sm_extra + j] = load_as_float(p.extra_bias, DT, j);
     __syncthreads();
@@ -850,7 +865,8 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(VPL)) gating_kernel(
             done = logit_ranked_row<VPL, DT>(p, t, lane, nv, w, ip, y0, i0);
         }
         if (!done)
-            full_row<VPL, DT>(p, t, lane, j0, nv, smem, s_row, s_gkey, s_kept, s_pick, flags, y0, i0, y1, i1);
+            full_row<VPL, DT, kFixed>(p, t, lane, j0, nv, smem, s_row, s_gkey, s_kept, s_pick, flags, y0, i0, y1,
+                                      i1);
 
         // ---- step 4: scale and write
         const bool has0 = lane < k, has1 = lane + 32 < k;
@@ -883,10 +899,10 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(VPL)) gating_kernel(
     }
 }
 
-template <int VPL, int DT, bool kByLogit>
+template <int VPL, int DT, int kPath>
 inline cudaError_t launch_gating_dt(const Params &p, size_t smem, int sms, cudaStream_t stream)
 {
-    const auto kernel = gating_kernel<VPL, DT, kByLogit>;
+    const auto kernel = gating_kernel<VPL, DT, kPath>;
     if (smem > 48 * 1024) {
         const cudaError_t err =
             cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOptIn);
@@ -917,34 +933,42 @@ inline cudaError_t launch_gating_dt(const Params &p, size_t smem, int sms, cudaS
     return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
-// one dtype's launch: the VPL template instance for the row width, ranked by logit or not
+// one dtype's launch: the VPL template instance for the row width and the kernel path.  The
+// grouped sigmoid instance exists for 4, 8, 12 and 16 experts per lane (e = 128, 256, 384, 512).
 template <int DT>
-inline cudaError_t launch_dtype(const Params &p, int vpl, bool by_logit, size_t smem, int sms, cudaStream_t stream)
+inline cudaError_t launch_dtype(const Params &p, int vpl, int path, size_t smem, int sms, cudaStream_t stream)
 {
 #define MRR_GATE_CASE(V)                                                                       \
     case V:                                                                                    \
-        return by_logit ? launch_gating_dt<V, DT, true>(p, smem, sms, stream)                  \
-                        : launch_gating_dt<V, DT, false>(p, smem, sms, stream);
+        return path == kPathLogit ? launch_gating_dt<V, DT, kPathLogit>(p, smem, sms, stream)  \
+                                  : launch_gating_dt<V, DT, kPathFull>(p, smem, sms, stream);
+#define MRR_GATE_CASE_FIXED(V)                                                                 \
+    case V:                                                                                    \
+        if (path == kPathGroupedSigmoid)                                                       \
+            return launch_gating_dt<V, DT, kPathGroupedSigmoid>(p, smem, sms, stream);         \
+        return path == kPathLogit ? launch_gating_dt<V, DT, kPathLogit>(p, smem, sms, stream)  \
+                                  : launch_gating_dt<V, DT, kPathFull>(p, smem, sms, stream);
     switch (vpl) {
         MRR_GATE_CASE(1)
         MRR_GATE_CASE(2)
-        MRR_GATE_CASE(4)
+        MRR_GATE_CASE_FIXED(4)
         MRR_GATE_CASE(6)
-        MRR_GATE_CASE(8)
-        MRR_GATE_CASE(12)
-        MRR_GATE_CASE(16)
+        MRR_GATE_CASE_FIXED(8)
+        MRR_GATE_CASE_FIXED(12)
+        MRR_GATE_CASE_FIXED(16)
         MRR_GATE_CASE(24)
     default:
         break;
     }
-    return by_logit ? launch_gating_dt<32, DT, true>(p, smem, sms, stream)
-                    : launch_gating_dt<32, DT, false>(p, smem, sms, stream);
+    return path == kPathLogit ? launch_gating_dt<32, DT, kPathLogit>(p, smem, sms, stream)
+                              : launch_gating_dt<32, DT, kPathFull>(p, smem, sms, stream);
 #undef MRR_GATE_CASE
+#undef MRR_GATE_CASE_FIXED
 }
 
 // defined in gating_f16.cu, gating_bf16.cu and gating_f32.cu
-cudaError_t launch_f16(const Params &p, int vpl, bool by_logit, size_t smem, int sms, cudaStream_t stream);
-cudaError_t launch_bf16(const Params &p, int vpl, bool by_logit, size_t smem, int sms, cudaStream_t stream);
-cudaError_t launch_f32(const Params &p, int vpl, bool by_logit, size_t smem, int sms, cudaStream_t stream);
+cudaError_t launch_f16(const Params &p, int vpl, int path, size_t smem, int sms, cudaStream_t stream);
+cudaError_t launch_bf16(const Params &p, int vpl, int path, size_t smem, int sms, cudaStream_t stream);
+cudaError_t launch_f32(const Params &p, int vpl, int path, size_t smem, int sms, cudaStream_t stream);
 
 }  // namespace mrr_gate
