@@ -16,12 +16,15 @@
 //  * scores become order-preserving 32-bit keys, so an arg-max over the row is two redux.sync
 //    instructions (the largest key, then the lowest expert index among the lanes holding it);
 //  * each lane caches its three best remaining candidates and rescans its run only when all are
-//    used, so a pick costs a handful of instructions instead of a pass over the row;
-//  * group scores come from a shuffle butterfly when each group is an aligned block of lanes,
-//    else from the row staged in shared memory;
+//    used, so a pick costs a handful of instructions instead of a pass over the row; the lane
+//    that gave a pick records it in shared memory, and lane i reads pick i at the end;
+//  * group scores come from a shuffle butterfly over the lanes' caches when each group is an
+//    aligned block of lanes, else from the row staged in shared memory;
 //  * where the normalisation alone ranks the experts (no bias, no groups), the row is ranked by
 //    logit and only the chosen experts are scored; a 16-bit logit's order key is packed with its
 //    expert into one word, so a pick is one redux.sync;
+//  * the grouped sigmoid routing shape (8 lane-aligned groups, top-8, bias) has an instance of
+//    its own with those facts fixed at compile time;
 //  * 8 warps per CTA, shared memory sized to the call, as many CTAs as fit on the SMs.
 #pragma once
 
