@@ -101,8 +101,8 @@ struct Params {
     const uint8_t *const *src_tk;   // [N] rank i's top-k weights (any alignment), or null
     const long long *src_rows;      // [N] rows each rank's buffers hold, or null (not checked)
     int ptr_off;                    // byte offset of the pointer tables' copy in dynamic shared
-                                    // memory (tokens, then scales, then top-k), or -1: read them
-                                    // from global memory
+                                    // memory (tokens, then scales, then top-k, then the rows), or
+                                    // -1: read them from global memory
 };
 
 // The per-rank source tables the multi-source form reads: Params' global tables, or their copy in
@@ -111,6 +111,7 @@ struct Sources {
     const uint8_t *const *tok;
     const uint8_t *const *sc;
     const uint8_t *const *tk;
+    const long long *rows;  // rows each rank's buffers hold, or null (not checked)
 };
 
 // ------------------------------------------------------------------------------------------------
@@ -245,12 +246,13 @@ __device__ __forceinline__ uint32_t check_sources(const Params &p, const Sources
 
 // Multi-source form with capacities: rank i's rows, R(i+1) - R(i) from the scanned SrcOffset
 // table, must fit the rows its buffers hold.  Threads t0, t0 + ts, ...; kFlagSource or 0.
-__device__ __forceinline__ uint32_t check_capacity(const Params &p, const uint32_t *row_ex, int t0, int ts)
+__device__ __forceinline__ uint32_t check_capacity(const Params &p, const Sources &src, const uint32_t *row_ex,
+                                                   int t0, int ts)
 {
     uint32_t f = 0u;
-    if (p.src_rows)
+    if (src.rows)
         for (int i = t0; i < p.N; i += ts)
-            if ((long long)(row_ex[(i + 1) * p.E] - row_ex[i * p.E]) > p.src_rows[i])
+            if ((long long)(row_ex[(i + 1) * p.E] - row_ex[i * p.E]) > src.rows[i])
                 f = kFlagSource;
     return f;
 }
@@ -1215,25 +1217,31 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
     m.N = p.N;
     m.E = p.E;
     m.inv = p.inverse;
-    Sources src{p.src_tok, p.src_sc, p.src_tk};
+    Sources src{p.src_tok, p.src_sc, p.src_tk, p.src_rows};
     ring.src_tab = p.src_tok;
-    // Multi-source form: copy the per-rank pointer tables into shared memory (their loads overlap
-    // the count loads); the bulk driver then finds a rank's buffer without a global round trip.
-    // The block synchronises before anything reads the copy.
+    // Multi-source form: copy the per-rank pointer tables and row capacities into shared memory
+    // (their loads overlap the count loads); the capacity check before the token stream and the
+    // bulk driver's rank lookups then take no global round trip.  The block synchronises before
+    // anything reads the copy.
     auto stage_pointers = [&]() {
         if (kMulti && p.ptr_off >= 0) {
             const uint8_t **t = reinterpret_cast<const uint8_t **>(smem + p.ptr_off);
-            const uint8_t **tok = t, **sc = t + p.N, **tk = t + (p.src_sc ? 2 : 1) * p.N;
+            const int n_sc = p.src_sc ? 1 : 0, n_tk = p.src_tk ? 1 : 0;
+            const uint8_t **tok = t, **sc = t + p.N, **tk = t + (1 + n_sc) * p.N;
+            long long *rows = reinterpret_cast<long long *>(t + (1 + n_sc + n_tk) * p.N);
             for (int i = tid; i < p.N; i += nthr) {
                 tok[i] = p.src_tok[i];
                 if (p.src_sc)
                     sc[i] = p.src_sc[i];
                 if (p.src_tk)
                     tk[i] = p.src_tk[i];
+                if (p.src_rows)
+                    rows[i] = p.src_rows[i];
             }
             src.tok = tok;
             src.sc = p.src_sc ? sc : nullptr;
             src.tk = p.src_tk ? tk : nullptr;
+            src.rows = p.src_rows ? rows : nullptr;
             ring.src_tab = tok;
         }
     };
@@ -1323,7 +1331,7 @@ __global__ void __launch_bounds__(1024) reroute_kernel(const Params p)
             // while DstOffset is scanned.  Counts that fail validation return before this point.
             uint32_t src_flag = 0u;
             auto mid = [&]() {
-                const uint32_t f = check_sources(p, src, kBulk, tid, nthr) | check_capacity(p, rex, tid, nthr);
+                const uint32_t f = check_sources(p, src, kBulk, tid, nthr) | check_capacity(p, src, rex, tid, nthr);
                 if (__syncthreads_or(f != 0u))
                     src_flag = kFlagSource;
                 else
@@ -1417,7 +1425,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(const Params p)
     if (p.multi) {
         // the multi-source form's per-rank pointers, checked once here for the copy kernel, which
         // reads this status word before it touches any source
-        const Sources src{p.src_tok, p.src_sc, p.src_tk};
+        const Sources src{p.src_tok, p.src_sc, p.src_tk, p.src_rows};
         if (__syncthreads_or(check_sources(p, src, p.multi_bulk != 0, tid, nthr) != 0u)) {
             if (tid == 0)
                 p.status[0] = kFlagSource;
@@ -1433,7 +1441,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(const Params p)
         else
             issue_count_loads<int>(p, 0, cb);
         uint32_t flags = cta_scan(p, cb, rex, cnt_t, dof, s_warp, &s_flags, &s_sum);
-        if (p.multi && !flags && __syncthreads_or(check_capacity(p, rex, tid, nthr) != 0u))
+        if (p.multi && !flags &&
+            __syncthreads_or(check_capacity(p, Sources{p.src_tok, p.src_sc, p.src_tk, p.src_rows}, rex, tid, nthr) != 0u))
             flags = kFlagSource;
         if (flags) {
             if (tid == 0)
@@ -1497,7 +1506,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(const Params p)
     if (tid == 0)
         p.g_row_ex[NE] = (uint32_t)p.A;
     __syncthreads();  // the row-major starts above, read by position below (inverse move)
-    if (p.multi && __syncthreads_or(check_capacity(p, p.g_row_ex, tid, nthr) != 0u)) {
+    if (p.multi &&
+        __syncthreads_or(check_capacity(p, Sources{p.src_tok, p.src_sc, p.src_tk, p.src_rows}, p.g_row_ex, tid, nthr) != 0u)) {
         if (tid == 0)
             p.status[0] = kFlagSource;
         return;
@@ -2094,8 +2104,9 @@ mrr_status run_plan_impl(const mrr_v2_plan_t *plan, const MultiSrc *ms, const vo
     p.scan_in_smem = scan_in_smem ? 1 : 0;
     p.ptr_off = -1;
     if (ms) {
-        // the pointer tables' copy in shared memory, behind everything else, when it fits
-        const int64_t pb = 8 * N * (1 + (ms->scales ? 1 : 0) + (ms->topk ? 1 : 0));
+        // the pointer tables' and capacities' copy in shared memory, behind everything else,
+        // when it fits
+        const int64_t pb = 8 * N * (1 + (ms->scales ? 1 : 0) + (ms->topk ? 1 : 0) + (ms->rows ? 1 : 0));
         if (round_up(smem, 16) + pb <= optin - 1024) {
             p.ptr_off = (int)round_up(smem, 16);
             smem = p.ptr_off + pb;
