@@ -98,6 +98,12 @@ __device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src_smem, uint32_t 
                  : "memory");
 }
 
+// Ask L2 for the 128-byte line holding p (a hint: no data moves to the thread).
+__device__ __forceinline__ void prefetch_line_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ask L2 to fetch [src, src + bytes) ahead of use (16-byte aligned, size a multiple of 16); no
 // completion to wait for
 __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
