@@ -136,7 +136,12 @@ extern "C" mrr_status mrr_gating_topk_run(const void *x, mrr_gate_dtype dt, int6
                                  k == kFixedK && norm_type == 1 &&
                                  p.sm_bias == 0 && p.sm_extra < 0 && !norm_out && e == 32 * (int64_t)vpl &&
                                  p.vec_bytes == 16 && (vpl == 4 || vpl == 8 || vpl == 12 || vpl == 16);
-    const int path = by_logit ? kPathLogit : (grouped_sigmoid ? kPathGroupedSigmoid : kPathFull);
+    // the fixed-shape rank-by-logit instances: e = 32 * VPL, 16-byte rows, k in {2, 4, 6, 8}
+    const bool logit_fixed = by_logit && e == 32 * (int64_t)vpl && p.vec_bytes == 16 &&
+                             (vpl == 4 || vpl == 8 || vpl == 12 || vpl == 16) &&
+                             (k == 2 || k == 4 || k == 6 || k == 8);
+    const int path = by_logit ? (logit_fixed ? kPathLogitFixed : kPathLogit)
+                              : (grouped_sigmoid ? kPathGroupedSigmoid : kPathFull);
     const cudaError_t err = dt == MRR_GATE_F32    ? launch_f32(p, vpl, path, smem, sms, stream)
                             : dt == MRR_GATE_BF16 ? launch_bf16(p, vpl, path, smem, sms, stream)
                                                   : launch_f16(p, vpl, path, smem, sms, stream);

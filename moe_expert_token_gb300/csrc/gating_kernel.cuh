@@ -50,7 +50,7 @@ constexpr uint32_t kNoIndex = 0xffffffffu;
 constexpr int kSmemOptIn = 100 * 1024;          // the largest call needs 78,848 bytes
 
 enum GroupPath { kNoGroups = 0, kLaneGroups = 1, kSmemGroups = 2 };
-enum KernelPath { kPathFull = 0, kPathLogit = 1, kPathGroupedSigmoid = 2 };
+enum KernelPath { kPathFull = 0, kPathLogit = 1, kPathGroupedSigmoid = 2, kPathLogitFixed = 3 };
 constexpr int kFixedK = 8;                      // the picks of the grouped sigmoid instance
 
 struct Params {
@@ -610,11 +610,12 @@ __device__ __forceinline__ float softmax_rcp(const float (&x)[VPL], int nv, floa
 
 // this lane's run of row `row` as 16-bit words, two experts per 32-bit word (experts past e: zero)
 template <int VPL>
-__device__ __forceinline__ void load_words(uint32_t (&w)[(VPL + 1) / 2], const Params &p, int row, int j0, int nv)
+__device__ __forceinline__ void load_words(uint32_t (&w)[(VPL + 1) / 2], const void *x, int row, int e, int vec_bytes,
+                                           int j0, int nv)
 {
     constexpr int W = (VPL + 1) / 2;
-    const unsigned short *src = static_cast<const unsigned short *>(p.x) + (long long)row * p.e + j0;
-    if (VPL % 8 == 0 && nv >= VPL && p.vec_bytes >= 16) {
+    const unsigned short *src = static_cast<const unsigned short *>(x) + (long long)row * e + j0;
+    if (VPL % 8 == 0 && nv >= VPL && vec_bytes >= 16) {
 #pragma unroll
         for (int c = 0; c < VPL / 8; ++c) {
             const uint4 q = __ldg(reinterpret_cast<const uint4 *>(src) + c);
@@ -623,14 +624,14 @@ __device__ __forceinline__ void load_words(uint32_t (&w)[(VPL + 1) / 2], const P
             w[4 * c + 2] = q.z;
             w[4 * c + 3] = q.w;
         }
-    } else if (VPL % 4 == 0 && nv >= VPL && p.vec_bytes >= 8) {
+    } else if (VPL % 4 == 0 && nv >= VPL && vec_bytes >= 8) {
 #pragma unroll
         for (int c = 0; c < VPL / 4; ++c) {
             const uint2 q = __ldg(reinterpret_cast<const uint2 *>(src) + c);
             w[2 * c] = q.x;
             w[2 * c + 1] = q.y;
         }
-    } else if (VPL % 2 == 0 && nv >= VPL && p.vec_bytes >= 4) {
+    } else if (VPL % 2 == 0 && nv >= VPL && vec_bytes >= 4) {
 #pragma unroll
         for (int c = 0; c < W; ++c)
             w[c] = __ldg(reinterpret_cast<const unsigned int *>(src) + c);
@@ -679,12 +680,13 @@ __device__ __forceinline__ bool logit_rank_holds(uint32_t key, int lane, int k, 
 // logit_rank_holds under which the two rankings agree; where one fails it returns false and the
 // caller evaluates the row in full.  Otherwise lane i < k returns pick i in (y, idx), the same
 // expert, order and score as the full evaluation (for float32 functions that are monotone there).
-template <int VPL, int DT>
-__device__ __forceinline__ bool logit_ranked_row(const Params &p, int t, int lane, int nv, const uint32_t (&w)[(VPL + 1) / 2],
-                                                 const uint32_t (&ip)[(VPL + 1) / 2], float &y, uint32_t &idx)
+template <int VPL, int DT, int kK>
+__device__ __forceinline__ bool logit_ranked_row(const Params &p, int t, int lane, int nv,
+                                                 const uint32_t (&w)[(VPL + 1) / 2], const uint32_t (&ip)[(VPL + 1) / 2],
+                                                 float &y, uint32_t &idx)
 {
     constexpr int W = (VPL + 1) / 2;
-    const int k = p.k;
+    const int k = kK ? kK : p.k;   // kK: the fixed-shape instance (e = 32 * VPL, 16-byte loads)
     // 16-bit order keys, two at a time: positive h -> h ^ 0x8000, negative h -> (h ^ 0xffff) + 1,
     // so -0 and +0 both map to 0x8000 and every key is >= 1; then packed with the expert
     uint32_t pk[VPL];
@@ -734,7 +736,7 @@ __device__ __forceinline__ bool logit_ranked_row(const Params &p, int t, int lan
     LogitScorer score{p.norm_type, 0.f, 0.f};
     if (p.norm_type == 0) {   // the run again (an L1 hit), rather than held across the picks
         uint32_t w2[(VPL + 1) / 2];
-        load_words<VPL>(w2, p, t, lane * VPL, nv);
+        load_words<VPL>(w2, p.x, t, kK ? 32 * VPL : p.e, kK ? 16 : p.vec_bytes, lane * VPL, nv);
         float x[VPL];
 #pragma unroll
         for (int u = 0; u < VPL; ++u)
@@ -756,13 +758,13 @@ __device__ __forceinline__ bool logit_ranked_row(const Params &p, int t, int lan
 // the expert actually ranked next instead: the row takes k + 1 picks (k <= 31), and pick k - 1
 // must score strictly above pick k (then every expert left out scores below pick k - 1).  The
 // other picks are checked as for 16-bit logits.
-template <int VPL>
-__device__ __forceinline__ bool logit_ranked_row_f32(const Params &p, int t, int lane, int j0, int nv,
-                                                     uint2 *s_pick, float &y, uint32_t &idx)
+template <int VPL, int kK>
+__device__ __forceinline__ bool logit_ranked_row_f32(const Params &p, int t, int lane, int j0, int nv, uint2 *s_pick,
+                                                     float &y, uint32_t &idx)
 {
-    const int k = p.k;
+    const int k = kK ? kK : p.k;   // kK: the fixed-shape instance (e = 32 * VPL, 16-byte loads)
     float v[VPL];
-    load_run<VPL, MRR_GATE_F32>(v, p.x, t, p.e, j0, p.vec_bytes);
+    load_run<VPL, MRR_GATE_F32>(v, p.x, t, kK ? 32 * VPL : p.e, j0, kK ? 16 : p.vec_bytes);
     uint32_t kv[VPL];
 #pragma unroll
     for (int u = 0; u < VPL; ++u)
@@ -779,7 +781,7 @@ __device__ __forceinline__ bool logit_ranked_row_f32(const Params &p, int t, int
     pick_keys<VPL>(c, kv, j0, lane, k + 1, s_pick, key, idx, k1, i1);   // lane k: the first expert left out
     LogitScorer score{p.norm_type, 0.f, 0.f};
     if (p.norm_type == 0) {   // the run again (an L1 hit), rather than held across the picks
-        load_run<VPL, MRR_GATE_F32>(v, p.x, t, p.e, j0, p.vec_bytes);
+        load_run<VPL, MRR_GATE_F32>(v, p.x, t, kK ? 32 * VPL : p.e, j0, kK ? 16 : p.vec_bytes);
         score.mx = key_value(__shfl_sync(kFull, key, 0));
         score.r = softmax_rcp<VPL>(v, nv, score.mx);
     }
@@ -800,14 +802,25 @@ __device__ __forceinline__ bool logit_ranked_row_f32(const Params &p, int t, int
 // VPL = experts per lane (the row's e <= 32 * VPL scores live in registers); DT = x's type;
 // kPath: kPathFull evaluates every score; kPathLogit ranks by logit (no bias, no groups, no hash
 // routing, no norm_out, k <= 32, or k <= 31 for float32 x), with the full evaluation as the
-// fallback; kPathGroupedSigmoid is the full evaluation specialised as full_row's kFixed says.
-template <int VPL, int DT, int kPath>
-__global__ void __launch_bounds__(kThreads, min_ctas_per_sm(VPL)) gating_kernel(const Params p)
+// fallback; kPathGroupedSigmoid is the full evaluation specialised as full_row's kFixed says;
+// kPathLogitFixed ranks by logit with the row shape fixed: e = 32 * VPL, 16-byte loads, k = kK
+// (the host launches it only then; the same arithmetic, with the pick loop unrolled).
+//
+// Register budget: min_ctas_per_sm(VPL), except for the fixed-shape float32 rank-by-logit
+// instances, whose unrolled picks over 32-bit keys spilled at 48 registers (12 experts per lane):
+// 4 CTAs (64 registers) measured 13.37 -> 12.17 us on 16384 x 384 float32 logits, top-6.
+template <int VPL, int DT, int kPath, int kK = 0>
+__global__ void __launch_bounds__(kThreads, (DT == MRR_GATE_F32 && kPath == kPathLogitFixed) ? 4 : min_ctas_per_sm(VPL))
+    gating_kernel(const Params p)
 {
-    constexpr bool kByLogit = kPath == kPathLogit, kFixed = kPath == kPathGroupedSigmoid;
+    constexpr bool kFixedLogit = kPath == kPathLogitFixed;
+    constexpr bool kByLogit = kPath == kPathLogit || kFixedLogit, kFixed = kPath == kPathGroupedSigmoid;
     extern __shared__ __align__(16) float smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = kFixed ? 32 * VPL : p.e, k = kFixed ? kFixedK : p.k, j0 = lane * VPL, nv = e - j0;
+    const int e = (kFixed || kFixedLogit) ? 32 * VPL : p.e;
+    const int k = kFixed ? kFixedK : (kFixedLogit ? kK : p.k);
+    const int j0 = lane * VPL, nv = e - j0;
+#define MRR_GATE_ROW_SHAPE (kFixedLogit ? 32 * VPL : p.e), (kFixedLogit ? 16 : p.vec_bytes)
 
     // no global memory touched above: wait for the previous kernel on the stream, then let the
     // next launch be scheduled (programmatic stream serialization)
@@ -845,7 +858,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(VPL)) gating_kernel(
     const int stride = gridDim.x * kWarps;
     uint32_t w_next[W];
     if (kAhead && blockIdx.x * kWarps + warp < p.T)
-        load_words<VPL>(w_next, p, blockIdx.x * kWarps + warp, j0, nv);
+        load_words<VPL>(w_next, p.x, blockIdx.x * kWarps + warp, MRR_GATE_ROW_SHAPE, j0, nv);
 
     uint32_t flags = 0u;
     for (int t = blockIdx.x * kWarps + warp; t < p.T; t += stride) {
@@ -853,7 +866,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(VPL)) gating_kernel(
         uint32_t i0 = 0u, i1 = 0u;
         bool done = false;
         if constexpr (kByLogit && DT == MRR_GATE_F32) {
-            done = logit_ranked_row_f32<VPL>(p, t, lane, j0, nv, s_pick, y0, i0);
+            done = logit_ranked_row_f32<VPL, kFixedLogit ? kK : 0>(p, t, lane, j0, nv, s_pick, y0, i0);
         } else if constexpr (kByLogit) {
             uint32_t w[W];
             if (kAhead) {
@@ -861,11 +874,11 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(VPL)) gating_kernel(
                 for (int c = 0; c < W; ++c)
                     w[c] = w_next[c];
                 if (t + stride < p.T)
-                    load_words<VPL>(w_next, p, t + stride, j0, nv);
+                    load_words<VPL>(w_next, p.x, t + stride, MRR_GATE_ROW_SHAPE, j0, nv);
             } else {
-                load_words<VPL>(w, p, t, j0, nv);
+                load_words<VPL>(w, p.x, t, MRR_GATE_ROW_SHAPE, j0, nv);
             }
-            done = logit_ranked_row<VPL, DT>(p, t, lane, nv, w, ip, y0, i0);
+            done = logit_ranked_row<VPL, DT, kFixedLogit ? kK : 0>(p, t, lane, nv, w, ip, y0, i0);
         }
         if (!done)
             full_row<VPL, DT, kFixed>(p, t, lane, j0, nv, smem, s_row, s_gkey, s_kept, s_pick, flags, y0, i0, y1,
@@ -900,12 +913,13 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm(VPL)) gating_kernel(
             p.status[1] = gridDim.x;
         }
     }
+#undef MRR_GATE_ROW_SHAPE
 }
 
-template <int VPL, int DT, int kPath>
+template <int VPL, int DT, int kPath, int kK = 0>
 inline cudaError_t launch_gating_dt(const Params &p, size_t smem, int sms, cudaStream_t stream)
 {
-    const auto kernel = gating_kernel<VPL, DT, kPath>;
+    const auto kernel = gating_kernel<VPL, DT, kPath, kK>;
     if (smem > 48 * 1024) {
         const cudaError_t err =
             cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOptIn);
@@ -936,8 +950,26 @@ inline cudaError_t launch_gating_dt(const Params &p, size_t smem, int sms, cudaS
     return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
+// The fixed-shape rank-by-logit instances: e = 32 * VPL for VPL in {4, 8, 12, 16} (128 to 512
+// experts) and k in {2, 4, 6, 8}.
+template <int VPL, int DT>
+inline cudaError_t launch_logit_fixed(const Params &p, size_t smem, int sms, cudaStream_t stream)
+{
+    switch (p.k) {
+    case 2:
+        return launch_gating_dt<VPL, DT, kPathLogitFixed, 2>(p, smem, sms, stream);
+    case 4:
+        return launch_gating_dt<VPL, DT, kPathLogitFixed, 4>(p, smem, sms, stream);
+    case 6:
+        return launch_gating_dt<VPL, DT, kPathLogitFixed, 6>(p, smem, sms, stream);
+    default:
+        return launch_gating_dt<VPL, DT, kPathLogitFixed, 8>(p, smem, sms, stream);
+    }
+}
+
 // one dtype's launch: the VPL template instance for the row width and the kernel path.  The
-// grouped sigmoid instance exists for 4, 8, 12 and 16 experts per lane (e = 128, 256, 384, 512).
+// grouped sigmoid and the fixed-shape rank-by-logit instances exist for 4, 8, 12 and 16 experts
+// per lane (e = 128, 256, 384, 512).
 template <int DT>
 inline cudaError_t launch_dtype(const Params &p, int vpl, int path, size_t smem, int sms, cudaStream_t stream)
 {
@@ -949,6 +981,8 @@ inline cudaError_t launch_dtype(const Params &p, int vpl, int path, size_t smem,
     case V:                                                                                    \
         if (path == kPathGroupedSigmoid)                                                       \
             return launch_gating_dt<V, DT, kPathGroupedSigmoid>(p, smem, sms, stream);         \
+        if (path == kPathLogitFixed)                                                           \
+            return launch_logit_fixed<V, DT>(p, smem, sms, stream);                            \
         return path == kPathLogit ? launch_gating_dt<V, DT, kPathLogit>(p, smem, sms, stream)  \
                                   : launch_gating_dt<V, DT, kPathFull>(p, smem, sms, stream);
     switch (vpl) {

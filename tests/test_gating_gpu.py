@@ -437,6 +437,33 @@ def test_rank_by_logit_matches_full_evaluation(dt, norm_type, e, k):
                              max_tie_rows=near / T_each, x=x[rows])
 
 
+@pytest.mark.parametrize("dt", ["float16", "bfloat16", "float32"])
+@pytest.mark.parametrize("norm_type", [0, 1, 2])
+@pytest.mark.parametrize("e", [128, 256, 384, 512])
+@pytest.mark.parametrize("k", [2, 4, 6, 8])
+def test_fixed_shape_logit_instances(dt, norm_type, e, k):
+    """e = 32 x experts-per-lane (128 to 512) and k in {2, 4, 6, 8}, 16-byte rows, no norm_out:
+    the fixed-shape rank-by-logit instances run (the pick loop unrolled).  They must agree bit for
+    bit with the full evaluation (norm_out asked for) on the stress rows, and with the oracle."""
+    rng = np.random.default_rng(e * 10 + k + 1000 * norm_type)
+    T_each = 8
+    x, n_kinds = _logit_rows(rng, T_each, e, dt)
+    kw = dict(norm_type=norm_type, eps=1e-9, routed_scaling_factor=1.3)
+    fast = run_gpu_gating(x, dt, k, out_flag=False, **kw)
+    full = run_gpu_gating(x, dt, k, out_flag=True, **kw)
+    assert fast["status"] == m.MRR_OK and fast["guards"]
+    assert np.array_equal(fast["expert_idx"], full["expert_idx"])
+    assert np.array_equal(fast["y_out"].view(np.uint32), full["y_out"].view(np.uint32))
+    ref = gating.gating_topk(x, k, **kw)
+    for kind in range(n_kinds):
+        rows = slice(kind * T_each, (kind + 1) * T_each)
+        near = sum(_decisive_near_tie(ref["norm_out"][t], x[t], k, 1, 1, 0)
+                   for t in range(rows.start, rows.stop))
+        check_against_oracle({**fast, "expert_idx": fast["expert_idx"][rows], "y_out": fast["y_out"][rows]},
+                             {key: v[rows] for key, v in ref.items()}, dt, kw,
+                             max_tie_rows=near / T_each, x=x[rows])
+
+
 @pytest.mark.parametrize("dt,T,e,k,norm_type", [("float16", 16384, 384, 6, 1), ("bfloat16", 20000, 256, 8, 2),
                                                 ("float16", 7001, 1000, 16, 1), ("bfloat16", 9000, 768, 32, 1),
                                                 ("float32", 16384, 384, 6, 1), ("float32", 10000, 160, 9, 2),
