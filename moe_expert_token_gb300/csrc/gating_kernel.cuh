@@ -407,8 +407,9 @@ constexpr int min_ctas_per_sm(int vpl) { return vpl <= 8 ? 6 : (vpl <= 12 ? 5 : 
 // kFixed: the instance for the grouped sigmoid case (DeepSeek-V3's routing shape), launched only
 // when e = 32 * VPL, x's rows take 16-byte loads, the bias row is given, the experts form 8
 // groups (each an aligned block of 4 lanes), k = kFixedK, the normalisation is sigmoid, and there
-// is no hash table, no additional bias and no norm_out.  Those are then compile-time facts: the same arithmetic in the same order as
-// the general instance, with its checks and loops over them folded away.
+// is no hash table, no additional bias and no norm_out.  Those are then compile-time facts: the
+// same arithmetic in the same order as the general instance, with its checks and loops over them
+// folded away.
 template <int VPL, int DT, bool kFixed>
 __device__ __forceinline__ void full_row(const Params &p, int t, int lane, int j0, int nv_rt, float *smem,
                                          float *s_row, uint32_t *s_gkey, uint32_t *s_kept, uint2 *s_pick,
