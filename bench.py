@@ -96,12 +96,20 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def code_text(rel: str) -> bytes:
+    """A source file's code: its text without // comments, trailing blanks and empty lines, so
+    that a change to comments alone leaves the hash (and a profile's claim to it) unchanged.  The
+    hashed sources hold no "//" inside a string literal."""
+    with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+        lines = (re.sub(r"//.*", "", line).rstrip() for line in f)
+        return "\n".join(line for line in lines if line).encode()
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for rel in ("moe_expert_token_gb300/csrc/mrr_v2.cu", "moe_expert_token_gb300/csrc/ptx.cuh",
                 "moe_expert_token_gb300/csrc/ws_layout.h"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        h.update(code_text(rel))
     return h.hexdigest()[:16]
 
 
@@ -130,8 +138,7 @@ def gating_source_hash() -> str:
     for rel in ("moe_expert_token_gb300/csrc/gating.cu", "moe_expert_token_gb300/csrc/gating_kernel.cuh",
                 "moe_expert_token_gb300/csrc/gating_f16.cu", "moe_expert_token_gb300/csrc/gating_bf16.cu",
                 "moe_expert_token_gb300/csrc/gating_f32.cu", "moe_expert_token_gb300/csrc/ptx.cuh"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        h.update(code_text(rel))
     return h.hexdigest()[:16]
 
 
