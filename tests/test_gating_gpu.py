@@ -243,15 +243,16 @@ def test_grouped_with_bias(dt, norm_type, mode):
 @pytest.mark.parametrize("dt", ["float16", "bfloat16", "float32"])
 @pytest.mark.parametrize("e", [128, 256, 384, 512])
 @pytest.mark.parametrize("mode", [0, 1])
-def test_grouped_sigmoid_instance_matches_general(dt, e, mode):
-    """Sigmoid with a bias and lane-aligned groups (8 groups of e / 8, keep 4, top-8), no norm_out:
-    the specialised kernel instance runs.  Asking for norm_out runs the general one.  The two must
-    agree bit for bit (same arithmetic, same order), and both against the oracle."""
-    rng = np.random.default_rng(e + mode)
-    T = 2048
+@pytest.mark.parametrize("k_group", [1, 3, 4, 7])
+def test_grouped_sigmoid_instance_matches_general(dt, e, mode, k_group):
+    """Sigmoid with a bias and lane-aligned groups (8 groups of e / 8, keep k_group, top-8), no
+    norm_out: the specialised kernel instance runs.  Asking for norm_out runs the general one.  The
+    two must agree bit for bit (same arithmetic, same order), and both against the oracle."""
+    rng = np.random.default_rng(e + mode + 10 * k_group)
+    T = 1024
     x = as_dtype(rng.standard_normal((T, e)) * 2, dt)
     bias = as_dtype(rng.standard_normal(e) * 0.05, dt)
-    kw = dict(k_group=4, group_count=8, group_select_mode=mode, norm_type=1, routed_scaling_factor=2.5,
+    kw = dict(k_group=k_group, group_count=8, group_select_mode=mode, norm_type=1, routed_scaling_factor=2.5,
               eps=1e-20)
     fast = run_gpu_gating(x, dt, 8, bias=bias, out_flag=False, **kw)
     full = run_gpu_gating(x, dt, 8, bias=bias, out_flag=True, **kw)
