@@ -68,8 +68,10 @@ typedef enum mrr_status {
     MRR_ERR_COUNT_SUM = 17,    /* Sum(counts) != A (or a single count > A)                     */
     MRR_ERR_TIMEOUT = 18,      /* a bounded wait inside the copy kernel gave up                */
     MRR_ERR_INDEX = 19,        /* gating top-k: an input_ids / tid2eid value out of range     */
-    MRR_ERR_SOURCE = 20        /* multi-source form: a per-rank source pointer is NULL, or a
+    MRR_ERR_SOURCE = 20,       /* multi-source form: a per-rank source pointer is NULL, or a
                                   token source is not 16-byte aligned on the bulk path        */
+    MRR_ERR_DEST = 21          /* push form: a receiver's buffer pointer is NULL, or a row
+                                  would land past the rows its buffer holds                    */
 } mrr_status;
 
 /* Token element types (section 参数说明).  Only the width matters: rows move as bytes.
@@ -337,6 +339,51 @@ mrr_status mrr_v2_run_plan_multi(const mrr_v2_plan_t *plan, const void *const *s
  */
 mrr_status mrr_v2_offsets_host(const void *counts, int count_is_i64, int64_t N, int64_t E, int64_t A,
                                int64_t *src_offset, int64_t *dst_offset, int64_t *expert_token_num);
+
+/*
+ * mrr_v2_push -- the push form of the fused receive, one sender's side: this rank writes the rows
+ * it sends straight into every receiver's expert-major buffers, so no receiver writes them
+ * rank-major and reads them back.  Receiver r's count matrix ("CANN ops-transformer
+ * MoeReRoutingV2" article, 参数说明: expert_token_num_per_rank; the dispatch's ep_recv_counts on
+ * the "torch_npu.npu_moe_distribute_dispatch" page) has this sender's row i; the receiver
+ * computes DstOffset_r(i, j) and SrcOffset_r(i, j) from it (计算公式; mrr_v2_offsets_host) and
+ * returns row i to this sender.  Rows move as bytes, scales and top-k weights with them.
+ *   send_tokens       [S, H] dt, this sender's rows: segment (r, j) -- the rows for receiver r's
+ *                     local expert j -- at rows SendOffset(r, j), the row-major exclusive prefix of
+ *                     send_counts (receiver outer)                                    (read)
+ *   send_scales       [S] / [S, scale_cols] rows in the layout `sl`, or NULL with MRR_SCALE_NONE
+ *   send_topk_w       [S] float32, or NULL (then out_topk_w must be NULL)              (read)
+ *   send_counts       [R, E] int32 / int64 (count_is_i64) in device memory: rows this sender
+ *                     sends to receiver r for expert j, each > 0, summing to S        (read)
+ *   dst_offsets       [R, E] int64, device: DstOffset_r(i, j), the expert-major row in receiver
+ *                     r's buffers where segment (r, j) starts                          (read)
+ *   recv_src_offsets  [R, E] int64, device: SrcOffset_r(i, j), the segment's first row in receiver
+ *                     r's rank-major order (for its gather index), or NULL with idx_out NULL
+ *   out_tokens        DEVICE array of R device pointers: receiver r's [rows_r, H] expert-major
+ *                     token buffer (this GPU's memory or a peer's)                      (written)
+ *   out_scales, out_topk_w   DEVICE arrays of R pointers, or NULL when the sends have none
+ *   idx_out           DEVICE array of R pointers to receiver r's int32 gather index
+ *                     (permute_token_idx, idx_type 0: idx[d] = its rank-major row), or NULL
+ *   out_rows          DEVICE array [R] int64: the rows receiver r's buffers hold, or NULL (not
+ *                     checked); a row that would land at or past it is not written
+ *   workspace         at least 4096 bytes of device memory for the status words; the device's
+ *                     findings are read with mrr_v2_read_status: MRR_ERR_COUNT_NONPOS,
+ *                     MRR_ERR_COUNT_SUM (nothing moved), MRR_ERR_DEST (a NULL receiver pointer
+ *                     or a row past out_rows: those rows are skipped)
+ * R * E must be at most 4096 (MRR_ERR_SHAPE otherwise), and S, H, dt, sl, scale_cols follow
+ * mrr_v2_plan's rules with S in the place of A.  Each receiver's expert_token_num comes from its
+ * own count matrix.  Enqueues one launch on `stream` and allocates nothing.  The writes use plain
+ * stores of up to 16 bytes per thread, whatever memory the pointers name: no bulk copy and no
+ * multicast.  Across senders the segments are disjoint, so the senders' launches need no order
+ * among themselves.
+ */
+mrr_status mrr_v2_push(const void *send_tokens, const void *send_scales, const float *send_topk_w,
+                       mrr_token_dtype dt, int64_t S, int64_t H, const void *send_counts, int count_is_i64,
+                       int64_t R, int64_t E, mrr_scale_layout sl, int64_t scale_cols,
+                       const int64_t *dst_offsets, const int64_t *recv_src_offsets,
+                       void *const *out_tokens, void *const *out_scales, float *const *out_topk_w,
+                       int32_t *const *idx_out, const int64_t *out_rows,
+                       void *workspace, size_t workspace_bytes, mrr_stream_t stream);
 
 /* mrr_status_str -- static, human-readable name of a status code (never NULL). */
 const char *mrr_status_str(mrr_status s);

@@ -17,9 +17,9 @@ ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 CSRC = os.path.join(PKG, "csrc")
 SOURCES = [os.path.join(CSRC, f) for f in ("gating_f16.cu", "gating_bf16.cu", "gating_f32.cu", "mrr_v2.cu",
-                                            "mrr_v2_noalloc.cu", "gating.cu")]
+                                            "mrr_v2_noalloc.cu", "mrr_push.cu", "gating.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "gating_kernel.cuh"),
-                  os.path.join(CSRC, "ws_layout.h"),
+                  os.path.join(CSRC, "ws_layout.h"), os.path.join(CSRC, "mrr_shape.h"),
                   os.path.join(INCLUDE, "mrr_v2.h"), os.path.join(INCLUDE, "mrr_gating.h")]
 LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libmrr_v2.so")

@@ -37,6 +37,7 @@
 #include <chrono>
 #include <type_traits>
 
+#include "mrr_shape.h"
 #include "mrr_v2.h"
 #include "ptx.cuh"
 #include "ws_layout.h"
@@ -52,9 +53,12 @@ constexpr int kMaxGrid = kStatusWords - 2;
 constexpr int64_t kFusedMaxSegs = 4096;            // N*E scanned inside every CTA up to this
 constexpr int64_t kSmemScanMaxSegs = 16384;        // above kFusedMaxSegs: the scan kernel scans in
                                                    // shared memory up to this (about 200 KB)
-constexpr uint32_t kFlagNonPos = 1u, kFlagSum = 2u, kFlagTimeout = 4u;
-constexpr uint32_t kFlagBadIndex = 8u;  // set by the gating kernel (gating.cu)
-constexpr uint32_t kFlagSource = 16u;   // multi-source form: a per-rank pointer is null or misaligned
+using mrr_ws::kFlagBadIndex;  // set by the gating kernel (gating.cu)
+using mrr_ws::kFlagDest;      // set by the push form (mrr_push.cu)
+using mrr_ws::kFlagNonPos;
+using mrr_ws::kFlagSource;    // multi-source form: a per-rank pointer is null or misaligned
+using mrr_ws::kFlagSum;
+using mrr_ws::kFlagTimeout;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // bound on any single mbarrier wait: 2 s
 constexpr int kMaxStages = 8;
 
@@ -1779,6 +1783,18 @@ cudaError_t launch_copy(const Params &p, int grid, int block, int smem, cudaStre
 
 }  // namespace
 
+namespace mrr_host {
+
+mrr_status check_shape(int64_t A, int64_t H, int dt, int64_t N, int64_t E, int count_is_i64, int sl,
+                       int64_t scale_cols, int64_t etn_type, int64_t idx_type, int64_t *row_bytes,
+                       int64_t *scale_row_bytes)
+{
+    return ::check_shape(A, H, dt, N, E, count_is_i64, sl, scale_cols, etn_type, idx_type, row_bytes,
+                         scale_row_bytes);
+}
+
+}  // namespace mrr_host
+
 extern "C" {
 
 const char *mrr_status_str(mrr_status s)
@@ -1816,6 +1832,8 @@ const char *mrr_status_str(mrr_status s)
         return "MRR_ERR_INDEX: an input_ids or tid2eid value is out of range";
     case MRR_ERR_SOURCE:
         return "MRR_ERR_SOURCE: a per-rank source pointer is NULL, or not 16-byte aligned on the bulk path";
+    case MRR_ERR_DEST:
+        return "MRR_ERR_DEST: a receiver's buffer pointer is NULL, or a row would land past its rows";
     }
     return "unknown mrr_status";
 }
@@ -2430,6 +2448,8 @@ mrr_status mrr_v2_read_status(const void *workspace, size_t workspace_bytes, mrr
         return MRR_ERR_INDEX;
     if (flags & kFlagSource)
         return MRR_ERR_SOURCE;
+    if (flags & kFlagDest)
+        return MRR_ERR_DEST;
     return MRR_OK;
 }
 

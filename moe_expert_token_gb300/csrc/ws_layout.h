@@ -1,5 +1,5 @@
 // Layout of the caller-owned workspace of the re-routing op, shared by every translation unit
-// that sizes or addresses one (mrr_v2.cu, mrr_v2_noalloc.cu).
+// that sizes or addresses one (mrr_v2.cu, mrr_v2_noalloc.cu, mrr_push.cu).
 //
 //   bytes 0 .. 4095       status words: [0] count-error flags, [1] grid size, [2 + b] CTA b's flags
 //   bytes 4096 .. 4351    the bulk path's chunk counter (one 64-bit word, the rest padding)
@@ -18,6 +18,14 @@ constexpr int kStatusBytes = 4096;
 constexpr int kStatusWords = kStatusBytes / 4;
 constexpr int kTicketOffset = kStatusBytes;
 constexpr int kHeaderBytes = kStatusBytes + 256;
+
+// The flags kernels leave in the status words; mrr_v2_read_status maps them to status codes.
+constexpr uint32_t kFlagNonPos = 1u;    // a count <= 0
+constexpr uint32_t kFlagSum = 2u;       // the counts do not sum to the rows given
+constexpr uint32_t kFlagTimeout = 4u;   // a bounded wait gave up
+constexpr uint32_t kFlagBadIndex = 8u;  // gating: an input_ids / tid2eid value out of range
+constexpr uint32_t kFlagSource = 16u;   // multi-source form: a per-rank source is missing or too small
+constexpr uint32_t kFlagDest = 32u;     // push form: a receiver's buffer is missing or too small
 
 // Length of a table indexed with one padding word per 32 entries (plus one end entry).
 __host__ __device__ constexpr int64_t padded_len(int64_t n) { return n + (n >> 5) + 1; }

@@ -34,6 +34,7 @@ MRR_ERR_COUNT_SUM = 17
 MRR_ERR_TIMEOUT = 18
 MRR_ERR_INDEX = 19
 MRR_ERR_SOURCE = 20
+MRR_ERR_DEST = 21
 MRR_GATE_F16, MRR_GATE_BF16, MRR_GATE_F32 = 0, 1, 2
 MRR_NOALLOC_MAX_SEGMENTS = 16384
 MRR_NOALLOC_SCRATCH_BYTES = 137984
@@ -132,6 +133,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                                           P, P, P, P, P, I64, P, ctypes.c_size_t, P]
     lib.mrr_v2_offsets_host.restype = I32
     lib.mrr_v2_offsets_host.argtypes = [P, I32, I64, I64, I64, P, P, P]
+    lib.mrr_v2_push.restype = I32
+    lib.mrr_v2_push.argtypes = [P, P, P, I32, I64, I64, P, I32, I64, I64, I32, I64, P, P, P, P, P, P, P,
+                                P, ctypes.c_size_t, P]
     lib.mrr_v2_run_noalloc.restype = I32
     lib.mrr_v2_run_noalloc.argtypes = [P, I32, I64, I64, P, I32, I64, I64, P, I32, I64, P,
                                        P, P, P, P, P, I64, I64, I32, P]
@@ -239,6 +243,17 @@ def mrr_v2_offsets_host(counts, count_is_i64, N, E, A, src_offset, dst_offset, e
     """Host addresses: counts [N, E] (int32 / int64), int64 outputs [N, E], [N, E], [E] or None."""
     return load_library().mrr_v2_offsets_host(counts, int(count_is_i64), N, E, A, src_offset, dst_offset,
                                               expert_token_num)
+
+
+def mrr_v2_push(send_tokens, send_scales, send_topk_w, dt, S, H, send_counts, count_is_i64, R, E, sl,
+                scale_cols, dst_offsets, recv_src_offsets, out_tokens, out_scales, out_topk_w, idx_out,
+                out_rows, workspace, workspace_bytes, stream) -> int:
+    """The push form, one sender's side; out_tokens / out_scales / out_topk_w / idx_out / out_rows are
+    device addresses of [R] tables (pointers, or int64 rows), or None."""
+    return load_library().mrr_v2_push(
+        send_tokens, send_scales, send_topk_w, dt, S, H, send_counts, int(count_is_i64), R, E, sl,
+        scale_cols, dst_offsets, recv_src_offsets, out_tokens, out_scales, out_topk_w, idx_out, out_rows,
+        workspace, workspace_bytes, stream)
 
 
 def mrr_v2_read_status(workspace, workspace_bytes, stream) -> int:

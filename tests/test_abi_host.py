@@ -27,7 +27,7 @@ def test_exports_every_header_function(lib):
     assert set(names) == {"mrr_v2_plan", "mrr_v2_run", "mrr_v2_run_plan", "mrr_v2_read_status",
                           "mrr_status_str", "mrr_v2_run_noalloc", "mrr_v2_unroute_plan",
                           "mrr_v2_unroute", "mrr_v1_run", "mrr_gating_topk_run", "mrr_v2_run_multi",
-                          "mrr_v2_run_plan_multi", "mrr_v2_offsets_host"}
+                          "mrr_v2_run_plan_multi", "mrr_v2_offsets_host", "mrr_v2_push"}
     out = subprocess.run(["nm", "-D", "--defined-only", m.library_path()], capture_output=True,
                          text=True, check=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
@@ -265,3 +265,34 @@ def test_run_plan_multi_refuses_the_inverse_direction(lib):
     st = m.mrr_v2_run_plan_multi(plan, T, None, None, None, m.MRR_BF16, C, O1, None, I, X, None, 1, WS,
                                  1 << 20, None)
     assert st in (m.MRR_ERR_PLAN, m.MRR_ERR_CUDA)
+
+
+def test_push_host_refusals(lib):
+    """mrr_v2_push's argument checks run on the host before anything is enqueued (no GPU needed):
+    the addresses below are never dereferenced."""
+    a = 1 << 20   # a 16-byte aligned stand-in address
+    bf16 = m.DTYPE_CODES["bfloat16"]
+    none = m.MRR_SCALE_NONE
+
+    def push(**kw):
+        args = dict(send_tokens=a, send_scales=None, send_topk_w=None, dt=bf16, S=16, H=8, send_counts=a,
+                    count_is_i64=0, R=2, E=2, sl=none, scale_cols=0, dst_offsets=a, recv_src_offsets=None,
+                    out_tokens=a, out_scales=None, out_topk_w=None, idx_out=None, out_rows=None, workspace=a,
+                    workspace_bytes=4096, stream=None)
+        args.update(kw)
+        return m.mrr_v2_push(*args.values())
+
+    assert push(R=64, E=65, S=8192) == m.MRR_ERR_SHAPE            # more than 4096 segments
+    assert push(S=3) == m.MRR_ERR_SHAPE                           # fewer rows than segments
+    assert push(H=16384) == m.MRR_ERR_SHAPE
+    assert push(dt=99) == m.MRR_ERR_DTYPE
+    assert push(workspace_bytes=1024) == m.MRR_ERR_WORKSPACE
+    assert push(workspace=a + 8) == m.MRR_ERR_WORKSPACE
+    assert push(out_tokens=None) == m.MRR_ERR_NULL
+    assert push(send_counts=None) == m.MRR_ERR_NULL
+    assert push(sl=m.MRR_SCALE_F32_A, scale_cols=1) == m.MRR_ERR_NULL   # a scale layout without scales
+    assert push(idx_out=a) == m.MRR_ERR_NULL                       # an index without source offsets
+    assert push(send_topk_w=a) == m.MRR_ERR_TOPK_PAIR
+    assert push(send_counts=a + 2) == m.MRR_ERR_ALIGN
+    assert push(dst_offsets=a + 4) == m.MRR_ERR_ALIGN
+    assert m.mrr_status_str(m.MRR_ERR_DEST).startswith("MRR_ERR_DEST")
