@@ -45,9 +45,11 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", type=int, default=2, help="workload 1..5 (2 is the headline)")
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--op", choices=["route", "unroute", "multi", "gating"], default="route",
+    ap.add_argument("--op", choices=["route", "unroute", "multi", "push", "gating"], default="route",
                     help="route: rank-major -> expert-major (the op); unroute: the inverse move; "
                          "multi: the op reading each source rank's rows from a buffer of its own; "
+                         "push: one sender writing the workload's rows into N receivers' buffers "
+                         "(mrr_v2_push; the receivers are this GPU's memory); "
                          "gating: the upstream gating top-k op (--config 1, 2 or 3)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU oracle baseline budget (seconds of oracle work)")
@@ -116,7 +118,9 @@ def kernel_source_hash() -> str:
 def profiled_traffic(config: int, op: str = "route"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
     name = {"route": f"reroute_kernel_C{config}.md", "unroute": f"reroute_kernel_inverse_C{config}.md",
-            "multi": f"reroute_kernel_multi_C{config}.md"}[op]
+            "multi": f"reroute_kernel_multi_C{config}.md"}.get(op)
+    if name is None:   # no committed summary for this op
+        return None
     path = os.path.join(ROOT, "profiles", name)
     try:
         text = open(path, encoding="utf-8").read()
@@ -247,17 +251,20 @@ def row_sample(p, frac: float):
 
 def op_bytes(p, op: str) -> int:
     """Algorithmic bytes of one step.  The inverse move writes no index and no per-expert counts;
-    the multi-source form moves the same bytes as the op (plus N pointers per table, not counted)."""
+    the multi-source form moves the same bytes as the op (plus N pointers per table, not counted);
+    the push form writes the index but no per-expert counts, and reads two int64 offset tables."""
     if op in ("route", "multi"):
         return p.algorithmic_bytes()
+    if op == "push":
+        return p.algorithmic_bytes() - p.E * p.counts.dtype.itemsize + 2 * 8 * p.N * p.E
     return p.algorithmic_bytes() - 4 * p.A - p.E * p.counts.dtype.itemsize
 
 
 def oracle_step(p, op: str, lib):
     import oracle
 
-    if op in ("route", "multi"):   # multi: the oracle of the concatenation (the same rows)
-        return oracle.run_problem(p, lib=lib)
+    if op in ("route", "multi", "push"):   # multi: the oracle of the concatenation (the same rows);
+        return oracle.run_problem(p, lib=lib)  # push: the same rows placed expert-major
     # the workload's payloads stand for the expert-major rows the inverse move reads
     return oracle.unroute(p.tokens, p.counts, permute_scales=p.scales, permute_topk=p.topk, lib=lib)
 
@@ -280,7 +287,9 @@ def time_oracle(p, budget_s: float, op: str = "route", max_reps: int = 1000):
 
 def config_dict(p, k, extra=None, op="route"):
     name = {"route": p.name, "unroute": "inverse move of " + p.name,
-            "multi": p.name + ", each source rank's rows in a buffer of their own"}[op]
+            "multi": p.name + ", each source rank's rows in a buffer of their own",
+            "push": p.name + ", pushed by one sender into the N receivers' expert-major buffers "
+                             "(this GPU's memory)"}[op]
     d = {"workload": name, "op": op,
          "A": p.A, "H": p.H, "N": p.N, "E": p.E, "token_dtype": p.token_dtype,
          "count_dtype": str(p.counts.dtype), "scales": p.scale_layout, "scale_cols": p.scale_cols,
@@ -346,7 +355,13 @@ class RouteSetup:
         sl = m.SCALE_CODES[p.scale_layout]
         A, H, N, E = p.A, p.H, p.N, p.E
         i64 = int(p.counts.dtype == np.int64)
-        if op in ("route", "multi"):
+        if op == "push":   # no plan: one launch of the push kernel (plain copies, 3 CTAs per SM)
+            import types
+
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            st, plan = m.MRR_OK, types.SimpleNamespace(path=2, grid=min(3 * sms, -(-A // 8)), block=256,
+                                                       chunk_bytes=0, stages=0, fuse_scan=1, workspace_bytes=4096)
+        elif op in ("route", "multi"):
             st, plan = m.mrr_v2_plan(A, H, code, N, E, i64, sl, p.scale_cols, p.topk is not None, 1,
                                      p.idx_type, local_rank)
         else:
@@ -395,6 +410,25 @@ class RouteSetup:
                     s[key] = None
                 s["rows"] = torch.tensor(np.full(N, cap) if multi_layout == "slots" else rows, dtype=torch.int64,
                                          device=dev)
+            if op == "push":
+                # N receivers, each holding this sender's rows for it expert-major: segment (r, j)
+                # at DstOffset = the rows of r's experts before j (also the segment's rank-major row)
+                c64 = p.counts.astype(np.int64)
+                rows_r = c64.sum(axis=1)
+                offs = np.concatenate([np.zeros((N, 1), np.int64), np.cumsum(c64, axis=1)[:, :-1]], axis=1)
+                s["dst_off"] = torch.from_numpy(np.ascontiguousarray(offs)).to(dev)
+                s["out_rows"] = torch.from_numpy(rows_r.copy()).to(dev)
+                for key, rb in (("tok", p.row_bytes), ("sc", p.scale_row_bytes), ("tk", 4), ("idx", 4)):
+                    if (key == "sc" and p.scales is None) or (key == "tk" and p.topk is None):
+                        s["tab_" + key] = None
+                        continue
+                    parts = [torch.empty(int(rows_r[r]) * rb, dtype=torch.uint8, device=dev) for r in range(N)]
+                    for r, t in enumerate(parts):
+                        s[f"{key}@{r}"] = t
+                    s["tab_" + key] = torch.tensor([t.data_ptr() for t in parts], dtype=torch.int64, device=dev)
+                s["ws"] = torch.empty(4096, dtype=torch.uint8, device=dev)
+                self.sets.append(s)
+                continue
             s["out_tokens"] = torch.empty(A * p.row_bytes, dtype=torch.uint8, device=dev)
             s["out_scales"] = (None if p.scales is None
                                else torch.empty(A * p.scale_row_bytes, dtype=torch.uint8, device=dev))
@@ -410,6 +444,12 @@ class RouteSetup:
             self.args = [(P(s["tokens"]), code, A, H, P(s["counts"]), i64, N, E, P(s["scales"]), sl,
                           p.scale_cols, P(s["topk"]), P(s["out_tokens"]), P(s["out_scales"]), P(s["idx"]),
                           P(s["etn"]), P(s["out_topk"]), 1, p.idx_type, P(s["ws"]), s["ws"].numel())
+                         for s in self.sets]
+        elif op == "push":
+            self.fn = lib.mrr_v2_push
+            self.args = [(P(s["tokens"]), P(s["scales"]), P(s["topk"]), code, A, H, P(s["counts"]), i64, N, E, sl,
+                          p.scale_cols, P(s["dst_off"]), P(s["dst_off"]), P(s["tab_tok"]), P(s["tab_sc"]),
+                          P(s["tab_tk"]), P(s["tab_idx"]), P(s["out_rows"]), P(s["ws"]), s["ws"].numel())
                          for s in self.sets]
         elif op == "multi":
             self.fn = lib.mrr_v2_run_multi
@@ -547,7 +587,7 @@ def run_gpu(args):
 
     # end to end through the C ABI from pinned host buffers: H2D inputs, run, D2H outputs
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.op != "push":   # the push form's receivers are device buffers only
         e2e = run_e2e(args, p, sets, setup.launch, dev, bytes_step, world, dist)
 
     cpu = cpu_par = None
@@ -608,7 +648,8 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
                      "traffic": profiled_traffic(args.config, args.op),
-                     "kernel": "mrr::reroute_kernel", "bytes_per_launch": bytes_step,
+                     "kernel": "mrr_push::push_kernel" if args.op == "push" else "mrr::reroute_kernel",
+                     "bytes_per_launch": bytes_step,
                      "mean_launch_us": mean_launch_ms * 1e3,
                      "timing": "CUDA events around the K back-to-back launches on the launching stream; per launch = region / K"},
         "cpu_baseline": cpu,

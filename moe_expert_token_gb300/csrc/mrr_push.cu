@@ -7,11 +7,12 @@
 // its send counts; the receiver's DstOffset_r(i, j) (and SrcOffset_r(i, j), for the gather index)
 // arrive from the counts exchange.
 //
-// GB300 design: one warp moves one row at a time, 16 bytes per lane per access where the
-// pointers and the row size allow (else 8, 4 or 1), with plain loads and stores -- a receiver's
-// buffer may be a peer GPU's memory, which the bulk copy engine is not used for.  Every CTA
-// scans the send counts into shared memory (at most 4096 segments) and finds a row's segment by
-// a binary search there.
+// GB300 design: a warp takes about 16 KB of consecutive source rows at a time and moves each
+// segment's share of them as one byte range, 16 bytes per lane per access where the pointers and
+// sizes allow (else 8, 4 or 1), four accesses in flight per lane, with plain loads and stores --
+// a receiver's buffer may be a peer GPU's memory, which the bulk copy engine is not used for.
+// Every CTA scans the send counts into shared memory (at most 4096 segments) and finds a chunk's
+// first segment by a binary search there.
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -26,6 +27,7 @@ namespace mrr_push {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxSegments = 4096;  // R * E
+constexpr int64_t kChunkBytes = 16384;  // token bytes a warp takes at a time (at least one row)
 constexpr int kMaxGrid = mrr_ws::kStatusWords - 2;
 constexpr uint32_t kFull = 0xffffffffu;
 
@@ -54,9 +56,9 @@ __device__ __forceinline__ int64_t count_at(const Params &p, int k)
                           : (int64_t)__ldg(static_cast<const int *>(p.counts) + k);
 }
 
-// Lane `lane` of a warp moves its share of one row of `bytes` bytes, in the widest accesses the
+// Lane `lane` of a warp moves its share of `bytes` contiguous bytes, in the widest accesses the
 // two addresses and the size allow.
-__device__ __forceinline__ void copy_row(uint8_t *dst, const uint8_t *src, int64_t bytes, int lane)
+__device__ __forceinline__ void copy_range(uint8_t *dst, const uint8_t *src, int64_t bytes, int lane)
 {
     const uintptr_t a = reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src) | (uintptr_t)bytes;
     if ((a & 15u) == 0) {
@@ -159,11 +161,17 @@ __global__ void __launch_bounds__(kThreads, 3) push_kernel(const Params p)
     if (!flags && total != p.S)
         flags = mrr_ws::kFlagSum;
 
-    // ---- the rows: warp w of CTA b takes rows b * kWarps + w, then every gridDim.x * kWarps-th
+    // ---- the rows, in chunks of consecutive source rows (about 16 KB of tokens each): warp w of
+    // CTA b takes chunk b * kWarps + w, then every gridDim.x * kWarps-th.  Inside a chunk the rows
+    // of one segment are consecutive on both sides, so each such piece moves as one byte range.
     uint32_t dflag = 0u;
     if (!flags) {
+        const int64_t rpc = p.tok.rb < kChunkBytes ? kChunkBytes / p.tok.rb : 1;  // rows per chunk
+        const int64_t nchunks = (p.S + rpc - 1) / rpc;
         const int64_t step = (int64_t)gridDim.x * kWarps;
-        for (int64_t s = (int64_t)blockIdx.x * kWarps + warp; s < p.S; s += step) {
+        for (int64_t c = (int64_t)blockIdx.x * kWarps + warp; c < nchunks; c += step) {
+            int64_t s = c * rpc;
+            const int64_t s_end = min(p.S, s + rpc);
             // the segment holding row s: the last g with SendOffset(g) <= s (counts > 0, so the
             // offsets strictly increase)
             int lo = 0, hi = p.RE;
@@ -174,27 +182,36 @@ __global__ void __launch_bounds__(kThreads, 3) push_kernel(const Params p)
                 else
                     hi = mid;
             }
-            const int g = lo, r = g / p.E;
-            const int64_t k = s - s_off[g];
-            const int64_t d = __ldg(p.dst_off + g) + k;
-            uint8_t *const to = p.tok.out[r];
-            uint8_t *const to_sc = p.sc.src ? p.sc.out[r] : nullptr;
-            uint8_t *const to_tk = p.tk.src ? p.tk.out[r] : nullptr;
-            int32_t *const to_idx = p.idx_out ? p.idx_out[r] : nullptr;
-            const bool ok = to && (!p.sc.src || to_sc) && (!p.tk.src || to_tk) && (!p.idx_out || to_idx) && d >= 0 &&
-                            (!p.out_rows || d < __ldg(p.out_rows + r));
-            if (!ok) {
-                dflag = mrr_ws::kFlagDest;  // this row is not written
-                continue;
-            }
-            copy_row(to + d * p.tok.rb, p.tok.src + s * p.tok.rb, p.tok.rb, lane);
-            if (p.sc.src)
-                copy_row(to_sc + d * p.sc.rb, p.sc.src + s * p.sc.rb, p.sc.rb, lane);
-            if (lane == 0) {
-                if (p.tk.src)
-                    memcpy(to_tk + d * 4, p.tk.src + s * 4, 4);
-                if (to_idx)
-                    to_idx[d] = (int32_t)(__ldg(p.rsrc_off + g) + k);
+            for (int g = lo; s < s_end; ++g) {
+                const int64_t n = min(s_end, s_off[g + 1]) - s;  // rows of segment g in this chunk
+                const int r = g / p.E;
+                const int64_t k = s - s_off[g];
+                const int64_t d = __ldg(p.dst_off + g) + k;
+                uint8_t *const to = p.tok.out[r];
+                uint8_t *const to_sc = p.sc.src ? p.sc.out[r] : nullptr;
+                uint8_t *const to_tk = p.tk.src ? p.tk.out[r] : nullptr;
+                int32_t *const to_idx = p.idx_out ? p.idx_out[r] : nullptr;
+                // the rows of the piece that land inside receiver r's buffers
+                int64_t m = n;
+                if (!to || (p.sc.src && !to_sc) || (p.tk.src && !to_tk) || (p.idx_out && !to_idx) || d < 0)
+                    m = 0;
+                else if (p.out_rows)
+                    m = max((int64_t)0, min(n, __ldg(p.out_rows + r) - d));
+                if (m < n)
+                    dflag = mrr_ws::kFlagDest;  // rows past the receiver's end are not written
+                if (m > 0) {
+                    copy_range(to + d * p.tok.rb, p.tok.src + s * p.tok.rb, m * p.tok.rb, lane);
+                    if (p.sc.src)
+                        copy_range(to_sc + d * p.sc.rb, p.sc.src + s * p.sc.rb, m * p.sc.rb, lane);
+                    if (p.tk.src)
+                        copy_range(to_tk + d * 4, p.tk.src + s * 4, m * 4, lane);
+                    if (to_idx) {
+                        const int64_t first = __ldg(p.rsrc_off + g) + k;
+                        for (int64_t t = lane; t < m; t += 32)
+                            to_idx[d + t] = (int32_t)(first + t);
+                    }
+                }
+                s += n;
             }
         }
     }
