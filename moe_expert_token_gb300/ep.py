@@ -16,14 +16,17 @@ This module holds the two exchanges the push form needs before any row moves, wr
 1. ``exchange_counts``: every rank sends send_counts[r, j] (rows it sends to rank r's local
    expert j) and receives recv_counts[i, j] (rows rank i sends to its own expert j) -- the count
    matrix of its re-routing, the dispatch page's ep_recv_counts;
-2. ``sender_dst_offsets``: every rank computes DstOffset of its count matrix with the library's
-   ``mrr_v2_offsets_host`` (the same prefix the kernels scan) and returns row i to rank i, so
-   each rank learns where each of its segments lands in every receiver's output.
+2. ``sender_offsets``: every rank computes SrcOffset and DstOffset of its count matrix with the
+   library's ``mrr_v2_offsets_host`` (the same prefixes the kernels scan) and returns row i of
+   each to rank i, so each rank learns where each of its segments lands in every receiver's
+   output (DstOffset) and which rank-major rows they are there (SrcOffset, for the receiver's
+   gather index).
 
 After these, sender i moves its rows for receiver r's expert j to rows
-[DstOffset_r(i, j), DstOffset_r(i, j) + counts) of r's output: with plain stores to the peer's
-memory over NVLink, or an NCCL put.  The receiver's per-expert counts come from its own count
-matrix.  The arithmetic runs in the C library; this module only moves tensors.
+[DstOffset_r(i, j), DstOffset_r(i, j) + counts) of r's output: ``mrr_v2_push`` does it with plain
+stores into the receivers' buffers (over NVLink, a peer's memory), or an NCCL put can.  The
+receiver's per-expert counts come from its own count matrix.  The arithmetic runs in the C
+library; this module only moves tensors.
 """
 from __future__ import annotations
 
@@ -62,19 +65,26 @@ def receiver_offsets(recv_counts, A: int):
     return src, dst, etn
 
 
-def sender_dst_offsets(recv_counts, group=None):
-    """For the push form: returns [W, E] int64 on recv_counts' device, row r holding the rows of
-    rank r's expert-major output at which this rank's segments for r's experts 0..E-1 start.
-    Every rank computes DstOffset of its own count matrix and sends row i to rank i."""
+def sender_offsets(recv_counts, group=None):
+    """For the push form: returns (dst, src), each [W, E] int64 on recv_counts' device.  Row r of
+    dst holds the rows of rank r's expert-major output at which this rank's segments for r's
+    experts 0..E-1 start; row r of src the rows of r's rank-major order they are (what r's gather
+    index names).  Every rank computes both for its own count matrix and sends row i to rank i:
+    the dst_offsets and recv_src_offsets of ``mrr_v2_push``."""
     import torch
     import torch.distributed as dist
 
     A = int(recv_counts.sum().item())
-    _, dst, _ = receiver_offsets(recv_counts, A)
-    dst = dst.to(recv_counts.device)
-    back = torch.empty_like(dst)
-    dist.all_to_all_single(back.view(-1), dst.contiguous().view(-1), group=group)
-    return back
+    src, dst, _ = receiver_offsets(recv_counts, A)
+    both = torch.stack([dst, src], dim=1).to(recv_counts.device).contiguous()   # [W, 2, E]
+    back = torch.empty_like(both)
+    dist.all_to_all_single(back.view(-1), both.view(-1), group=group)
+    return back[:, 0].contiguous(), back[:, 1].contiguous()
 
 
-__all__ = ["exchange_counts", "receiver_offsets", "sender_dst_offsets"]
+def sender_dst_offsets(recv_counts, group=None):
+    """The dst half of ``sender_offsets``."""
+    return sender_offsets(recv_counts, group)[0]
+
+
+__all__ = ["exchange_counts", "receiver_offsets", "sender_offsets", "sender_dst_offsets"]

@@ -5,12 +5,13 @@ The dispatch ("torch_npu.npu_moe_distribute_dispatch" page: ep_recv_counts, expa
 rank the rows its peers send to its local experts; the re-routing ("CANN ops-transformer
 MoeReRoutingV2" article, section 计算公式) lays them out expert-major.  In the push form no
 receiver re-routes anything: sender i writes its segment for receiver r's expert j at the row
-DstOffset_r(i, j) it learned from ``moe_expert_token_gb300.ep.sender_dst_offsets``.
+DstOffset_r(i, j) it learned from ``moe_expert_token_gb300.ep.sender_offsets`` (with SrcOffset_r(i, j),
+the rank-major rows its segment is at the receiver, for the receiver's gather index).
 
 Each rank here sends seeded payload rows to every rank; the payloads travel with gloo, and the
 receiver places every sender's segments at the offsets THAT SENDER computed, never its own.
-The assembled buffer must equal, byte for byte, the oracle's re-routing of the rank-major
-concatenation the receiver would otherwise have re-routed, and the per-expert counts the
+The assembled buffer and gather index must equal, byte for byte, the oracle's re-routing of the
+rank-major concatenation the receiver would otherwise have re-routed, and the per-expert counts the
 receiver's own offsets give must equal the oracle's.  No GPU is used: the arithmetic is the
 library's host routine and the transport is gloo.
 """
@@ -62,8 +63,11 @@ def _rank_main(rank, world, port, q):
         counts, rows = _send_plan(rank, world)
         # 1. counts exchange: row i of recv = what rank i sends to this rank's experts
         recv = ep.exchange_counts(torch.from_numpy(counts))
-        # 2. every sender learns where its segments land in every receiver's output
-        where = ep.sender_dst_offsets(recv).numpy()             # [world, E]: row r -> receiver r
+        # 2. every sender learns where its segments land in every receiver's output, and which
+        #    rank-major rows they are there
+        where_t, src_t = ep.sender_offsets(recv)
+        where, src_rows = where_t.numpy(), src_t.numpy()       # [world, E]: row r -> receiver r
+        assert np.array_equal(where, ep.sender_dst_offsets(recv).numpy())
         # 3. payloads: to rank r, this rank's rows for r's experts in expert order, with the
         #    offsets it computed for them
         send_rows = [np.concatenate([rows[r, j] for j in range(E_LOCAL)]) for r in range(world)]
@@ -77,21 +81,27 @@ def _rank_main(rank, world, port, q):
         off_in = torch.empty(world * E_LOCAL, dtype=torch.int64)
         dist.all_to_all_single(off_in, torch.from_numpy(where.reshape(-1).copy()))
         off_in = off_in.numpy().reshape(world, E_LOCAL)          # row i: sender i's offsets here
+        src_in = torch.empty(world * E_LOCAL, dtype=torch.int64)
+        dist.all_to_all_single(src_in, torch.from_numpy(src_rows.reshape(-1).copy()))
+        src_in = src_in.numpy().reshape(world, E_LOCAL)          # row i: sender i's source rows here
         # 4. the receiver places each sender's segments where the SENDER said
         rc = recv.numpy()
         A = int(rc.sum())
         inbox = inbox.numpy().reshape(A, ROW_BYTES)
         out = np.full((A, ROW_BYTES), 0xEE, np.uint8)
+        idx = np.full(A, -1, np.int32)                           # the gather index the senders write
         pos = 0
         for i in range(world):
             for j in range(E_LOCAL):
                 n = int(rc[i, j])
                 out[off_in[i, j]:off_in[i, j] + n] = inbox[pos:pos + n]
+                idx[off_in[i, j]:off_in[i, j] + n] = src_in[i, j] + np.arange(n)
                 pos += n
         # 5. against the oracle's re-routing of the rank-major rows this rank received
         ref = oracle.run(inbox, rc)
         _, _, etn = ep.receiver_offsets(recv, A)
         ok = (np.array_equal(out, ref["permute_tokens"])
+              and np.array_equal(idx, ref["permute_token_idx"])
               and np.array_equal(etn.numpy(), ref["expert_token_num"].astype(np.int64))
               and np.array_equal(rc, np.stack([_send_plan(i, world)[0][rank] for i in range(world)])))
         q.put((rank, bool(ok), A))
