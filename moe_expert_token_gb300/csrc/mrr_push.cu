@@ -7,7 +7,7 @@
 // its send counts; the receiver's DstOffset_r(i, j) (and SrcOffset_r(i, j), for the gather index)
 // arrive from the counts exchange.
 //
-// GB300 design: a warp takes about 16 KB of consecutive source rows at a time and moves each
+// GB300 design: a warp takes about 8 KB of consecutive source rows at a time and moves each
 // segment's share of them as one byte range, 16 bytes per lane per access where the pointers and
 // sizes allow (else 8, 4 or 1), four accesses in flight per lane, with plain loads and stores --
 // a receiver's buffer may be a peer GPU's memory, which the bulk copy engine is not used for.
@@ -27,7 +27,7 @@ namespace mrr_push {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxSegments = 4096;  // R * E
-constexpr int64_t kChunkBytes = 16384;  // token bytes a warp takes at a time (at least one row)
+constexpr int64_t kChunkBytes = 8192;   // token bytes a warp takes at a time (at least one row)
 constexpr int kMaxGrid = mrr_ws::kStatusWords - 2;
 constexpr uint32_t kFull = 0xffffffffu;
 
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 3) push_kernel(const Params p)
     if (!flags && total != p.S)
         flags = mrr_ws::kFlagSum;
 
-    // ---- the rows, in chunks of consecutive source rows (about 16 KB of tokens each): warp w of
+    // ---- the rows, in chunks of consecutive source rows (about 8 KB of tokens each): warp w of
     // CTA b takes chunk b * kWarps + w, then every gridDim.x * kWarps-th.  Inside a chunk the rows
     // of one segment are consecutive on both sides, so each such piece moves as one byte range.
     uint32_t dflag = 0u;
