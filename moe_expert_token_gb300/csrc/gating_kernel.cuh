@@ -495,11 +495,23 @@ __device__ __forceinline__ void full_row(const Params &p, int t, int lane, int j
         const uint32_t gkey = p.select_mode == 0 ? g1 : order_key(key_value(g1) + key_value(g2));
         const bool leader = member && (lane & (lpg - 1)) == 0;
         bool kept = false;
-        for (int r = 0; r < p.k_group; ++r) {
-            const bool cand = leader && !kept;
-            const uint32_t top = __reduce_max_sync(kFull, cand ? gkey : 0u);
-            const uint32_t win = __reduce_min_sync(kFull, cand && gkey == top ? (uint32_t)g : kNoIndex);
-            kept = kept || (member && (uint32_t)g == win);
+        if constexpr (kFixed) {
+            // 8 groups: each lane counts the groups ranked above its own (a higher score, or an
+            // equal one at a lower group) from the 8 group keys, which lanes 0, 4, ..., 28 hold
+            int above = 0;
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                const uint32_t kh = __shfl_sync(kFull, gkey, 4 * h);
+                above += (kh > gkey || (kh == gkey && h < g)) ? 1 : 0;
+            }
+            kept = above < p.k_group;
+        } else {
+            for (int r = 0; r < p.k_group; ++r) {
+                const bool cand = leader && !kept;
+                const uint32_t top = __reduce_max_sync(kFull, cand ? gkey : 0u);
+                const uint32_t win = __reduce_min_sync(kFull, cand && gkey == top ? (uint32_t)g : kNoIndex);
+                kept = kept || (member && (uint32_t)g == win);
+            }
         }
         if (!kept) {   // a dropped group's experts leave the candidates
             c.b1 = c.b2 = c.b3 = 0u;
