@@ -364,7 +364,9 @@ __device__ __forceinline__ void pick_keys(LaneCands &c, const uint32_t (&kv)[VPL
 {
     for (int i = 0; i < k; ++i) {
         uint32_t top = __reduce_max_sync(kFull, c.b1);
-        if (top == kRefill) {   // some lane has used up its cache (or the row holds a NaN score)
+        // a lane uses up its three cached keys after giving three picks at the earliest; before
+        // that a top of kRefill is a NaN score's key, which is picked like any other
+        if (i >= 3 && top == kRefill) {   // some lane has used up its cache (or a NaN score)
             __syncwarp();
             if (c.b1 == kRefill) {
                 KeyRun<VPL> run;
