@@ -124,6 +124,19 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
+// warp_sum when only lanes below kLanes (a power of two) hold nonzero values: the same additions
+// in the same order, less the rounds that only add zeros; lanes below kLanes get the sum
+template <int kLanes>
+__device__ __forceinline__ float warp_sum_low(float v)
+{
+#pragma unroll
+    for (int o = kLanes / 2; o > 0; o >>= 1)
+        v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+__host__ __device__ constexpr int pow2_at_least(int k) { return k <= 1 ? 1 : 2 * pow2_at_least((k + 1) / 2); }
+
 // this lane's run of row `row` (e experts), experts [j0, j0 + VPL), as floats; experts at or past
 // e read -inf.  vec_bytes is the widest load the rows' alignment allows.
 template <int VPL, int DT>
@@ -195,15 +208,19 @@ __device__ __forceinline__ void load_run(float (&v)[VPL], const void *x, long lo
 // Sigmoid: 1 / (1 + e^-x) with e^-x = 2^(-x log2 e).  The product -x log2 e is carried in two
 // floats, hi + lo (Cody and Waite's split of the constant, "Software Manual for the Elementary
 // Functions", 1980: log2 e = kHi + kLo with kHi a float, and an fma recovers the rounding error of
-// -x kHi exactly).  The hardware base-2 exponential (ex2.approx) takes hi, the first-order factor
-// 2^lo = 1 + lo ln 2 corrects for lo, and rcp.approx gives the reciprocal.  Rounding -x log2 e to
-// one float instead would cost up to |x| 2^-24 ln 2 of relative error, about 17 ulp at |x| = 25.
-// lo is tiny wherever 2^hi is a normal float; where 2^hi is 0 or inf (|x| above about 88, or
-// x = +-inf, where lo is huge, infinite or NaN) the clamp to [-1, 1] keeps the factor finite and
-// positive, so 0 and inf pass through (sigmoid 1 or 0), and a NaN logit stays NaN.
-// Subnormals flush: 2^hi below 2^-126 leaves 1 + 2^hi = 1, and a sigmoid below 2^-126
-// (x < -87.3) comes out 0.  Over every float16 and bfloat16 logit the result is within a few
-// float32 ulps of the exact sigmoid (tests/test_gating_gpu.py measures it).
+// -x kHi exactly).  The hardware base-2 exponential (ex2.approx) takes hi and the first-order
+// factor 2^lo = 1 + lo ln 2 corrects for lo.  The sum is formed at half scale, d = (1 + e^-x) / 2
+// = 2^hi (1/2 + lo ln 2 / 2) + 1/2, in one fma (one rounding where 1 + 2^hi 2^lo took two), and
+// sigmoid = rcp.approx(d) / 2, the halving exact.  Rounding -x log2 e to one float instead would
+// cost up to |x| 2^-24 ln 2 of relative error, about 17 ulp at |x| = 25.
+// lo is tiny wherever 2^hi is a normal float.  The extremes: hi is capped at 200 (2^hi is inf from
+// 128 on), so for x below about -139 or x = -inf lo is large or +inf, the factor saturates to 1
+// and d = inf: sigmoid 0.  For large x or x = +inf, 2^hi = 0 and the factor (a NaN at +inf, which
+// the saturating fma turns into 0) stays in [0, 1], so d = 1/2: sigmoid 1.  A NaN logit gives
+// hi = 200, factor 0 and d = inf * 0: the score stays NaN.  Subnormals flush: 2^hi below 2^-126
+// gives d = 1/2, and a sigmoid below the smallest normal float comes out 0 or subnormal.  Over
+// every float16 and bfloat16 logit the result is within a few float32 ulps of the exact sigmoid
+// (tests/test_gating_gpu.py measures it).
 __device__ __forceinline__ float ex2_approx_ftz(float t)
 {
     float r;
@@ -218,15 +235,22 @@ __device__ __forceinline__ float rcp_approx_ftz(float t)
     return r;
 }
 
+__device__ __forceinline__ float fma_sat(float a, float b, float c)
+{
+    float r;
+    asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ float sigmoid_score(float x)
 {
     constexpr float kHi = 1.44269502162933349609375f;   // log2 e rounded to float
     constexpr float kLo = 1.9259629911266175e-8f;        // log2 e - kHi
-    constexpr float kLn2 = 0.693147180559945309f;
-    const float hi = -x * kHi;
-    const float lo = fminf(fmaxf(fmaf(-x, kLo, fmaf(-x, kHi, -hi)), -1.f), 1.f);
-    const float e = ex2_approx_ftz(hi) * fmaf(lo, kLn2, 1.f);
-    return rcp_approx_ftz(1.f + e);
+    constexpr float kHalfLn2 = 0.3465735902799726547f;
+    const float hi = fminf(-x * kHi, 200.f);
+    const float lo = fmaf(-x, kLo, fmaf(-x, kHi, -hi));
+    const float d = fmaf(ex2_approx_ftz(hi), fma_sat(lo, kHalfLn2, 0.5f), 0.5f);
+    return 0.5f * rcp_approx_ftz(d);
 }
 
 __device__ __forceinline__ float softplus_score(float x)
@@ -354,15 +378,18 @@ __device__ __noinline__ LaneCands refill(const KeyRun<VPL> run, uint32_t j0, con
     return c;
 }
 
-// The k picks: each is the largest remaining key over the warp, ties to the lower expert (two
-// redux.sync).  Expert numbers are distinct across lanes, so the lane whose b1 is the winning
-// expert is the one that gave the pick; it records the pick in s_pick[i] (64 entries per warp).
-// Lane i returns pick i's key and expert in (k0, i0), pick i + 32's in (k1, i1).
-template <int VPL>
+// The k picks: each is the largest remaining key over the warp (a redux.sync), ties to the lower
+// expert.  A lane's experts all come before the next lane's and its cache keeps equal keys in
+// expert order, so the pick goes to the lowest lane whose b1 is the top key: one ballot when k is
+// a compile-time kK (the picks then unrolled), else a second redux.sync for the lowest expert.
+// The giving lane records the pick in s_pick[i] (64 entries per warp).  Lane i returns pick i's
+// key and expert in (k0, i0), pick i + 32's in (k1, i1).
+template <int VPL, int kK = 0>
 __device__ __forceinline__ void pick_keys(LaneCands &c, const uint32_t (&kv)[VPL], int j0, int lane, int k,
                                           uint2 *s_pick, uint32_t &k0, uint32_t &i0, uint32_t &k1, uint32_t &i1)
 {
-    for (int i = 0; i < k; ++i) {
+    const uint32_t below = (1u << lane) - 1u;   // the lanes below this one
+    auto pick = [&](int i) {
         uint32_t top = __reduce_max_sync(kFull, c.b1);
         // a lane uses up its three cached keys after giving three picks at the earliest; before
         // that a top of kRefill is a NaN score's key, which is picked like any other
@@ -377,15 +404,30 @@ __device__ __forceinline__ void pick_keys(LaneCands &c, const uint32_t (&kv)[VPL
             }
             top = __reduce_max_sync(kFull, c.b1);
         }
-        const uint32_t win = __reduce_min_sync(kFull, c.b1 == top ? c.u1 : kNoIndex);
-        if (c.u1 == win) {
-            s_pick[i] = make_uint2(top, win);
+        bool give;
+        if constexpr (kK > 0) {   // the lowest lane at the top key
+            const bool at_top = c.b1 == top;
+            const uint32_t tied = __ballot_sync(kFull, at_top);
+            give = at_top && (tied & below) == 0u;
+        } else {
+            give = c.u1 == __reduce_min_sync(kFull, c.b1 == top ? c.u1 : kNoIndex);
+        }
+        if (give) {
+            s_pick[i] = make_uint2(top, c.u1);
             c.b1 = c.b2;
             c.u1 = c.u2;
             c.b2 = c.b3;
             c.u2 = c.u3;
             c.b3 = c.fill;
         }
+    };
+    if constexpr (kK > 0) {
+#pragma unroll
+        for (int i = 0; i < kK; ++i)
+            pick(i);
+    } else {
+        for (int i = 0; i < k; ++i)
+            pick(i);
     }
     __syncwarp();
     const uint2 p0 = lane < k ? s_pick[lane] : make_uint2(0u, 0u);
@@ -498,14 +540,15 @@ __device__ __forceinline__ void full_row(const Params &p, int t, int lane, int j
         const bool leader = member && (lane & (lpg - 1)) == 0;
         bool kept = false;
         if constexpr (kFixed) {
-            // 8 groups: each lane counts the groups ranked above its own (a higher score, or an
-            // equal one at a lower group) from the 8 group keys, which lanes 0, 4, ..., 28 hold
-            int above = 0;
-#pragma unroll
-            for (int h = 0; h < 8; ++h) {
-                const uint32_t kh = __shfl_sync(kFull, gkey, 4 * h);
-                above += (kh > gkey || (kh == gkey && h < g)) ? 1 : 0;
-            }
+            // 8 groups: a group's rank is the number of groups ranked above it (a higher score,
+            // or an equal one at a lower group).  The group keys sit in lanes 0, 4, ..., 28; lane
+            // s of a group's four compares its key with groups 2s and 2s + 1, and the four add up.
+            const int s = lane & 3, ha = 2 * s, hb = 2 * s + 1;
+            const uint32_t ka = __shfl_sync(kFull, gkey, 4 * ha), kb = __shfl_sync(kFull, gkey, 4 * hb);
+            int above = (ka > gkey || (ka == gkey && ha < g)) ? 1 : 0;
+            above += (kb > gkey || (kb == gkey && hb < g)) ? 1 : 0;
+            above += __shfl_xor_sync(kFull, above, 1);
+            above += __shfl_xor_sync(kFull, above, 2);
             kept = above < p.k_group;
         } else {
             for (int r = 0; r < p.k_group; ++r) {
@@ -570,7 +613,7 @@ __device__ __forceinline__ void full_row(const Params &p, int t, int lane, int j
     }
 
     uint32_t k0, k1;
-    pick_keys<VPL>(c, kv, j0, lane, k, s_pick, k0, i0, k1, i1);
+    pick_keys<VPL, kFixed ? kFixedK : 0>(c, kv, j0, lane, k, s_pick, k0, i0, k1, i1);
     y0 = key_value(k0);
     y1 = key_value(k1);
     }
@@ -793,7 +836,8 @@ __device__ __forceinline__ bool logit_ranked_row_f32(const Params &p, int t, int
     uint32_t key, k1, i1;
     LaneCands c;
     first_scan<VPL>(c, kv, (uint32_t)j0);
-    pick_keys<VPL>(c, kv, j0, lane, k + 1, s_pick, key, idx, k1, i1);   // lane k: the first expert left out
+    // lane k: the first expert left out
+    pick_keys<VPL, kK ? kK + 1 : 0>(c, kv, j0, lane, k + 1, s_pick, key, idx, k1, i1);
     LogitScorer score{p.norm_type, 0.f, 0.f};
     if (p.norm_type == 0) {   // the run again (an L1 hit), rather than held across the picks
         load_run<VPL, MRR_GATE_F32>(v, p.x, t, kK ? 32 * VPL : p.e, j0, kK ? 16 : p.vec_bytes);
@@ -901,7 +945,9 @@ __global__ void __launch_bounds__(kThreads, (DT == MRR_GATE_F32 && kPath == kPat
 
         // ---- step 4: scale and write
         const bool has0 = lane < k, has1 = lane + 32 < k;
-        const float ysum = warp_sum((has0 ? y0 : 0.f) + (has1 ? y1 : 0.f));
+        const float y_lane = (has0 ? y0 : 0.f) + (has1 ? y1 : 0.f);
+        const float ysum = (kFixed || kFixedLogit) ? warp_sum_low<pow2_at_least(kFixed ? kFixedK : kK)>(y_lane)
+                                                   : warp_sum(y_lane);
         const float scale = p.rsf * __frcp_rn(ysum + p.eps);
         if (has0) {
             store_from_float(p.y_out, DT, (long long)t * k + lane, y0 * scale);

@@ -263,6 +263,33 @@ def test_grouped_sigmoid_instance_matches_general(dt, e, mode, k_group):
     check_against_oracle(fast, ref, dt, kw)
 
 
+@pytest.mark.parametrize("dt", ["float16", "bfloat16", "float32"])
+@pytest.mark.parametrize("e", [256, 512])
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("k_group", [1, 4, 7])
+def test_grouped_sigmoid_instance_ties(dt, e, mode, k_group):
+    """The specialised grouped instance on rows full of exact ties: logits 0 or 2 (every 5th row
+    all 1) and, for group maxima, a bias of 0 or 1/2 leave at most four distinct scores per row.
+    Equal scores and equal group scores go to the lower expert and group, exactly as the oracle's
+    stable order has them, and the instance agrees with the general one bit for bit.  (For group
+    sums the bias is 0: with more distinct scores two different pairs can have the same exact sum,
+    which float32 rounding may order either way.)"""
+    rng = np.random.default_rng(e + 3 * mode + k_group)
+    T = 320
+    x = rng.choice(np.array([0.0, 2.0], np.float32), size=(T, e))
+    x[::5] = 1.0
+    bias = (rng.integers(0, 2, size=e) * 0.5 if mode == 0 else np.zeros(e)).astype(np.float32)
+    kw = dict(k_group=k_group, group_count=8, group_select_mode=mode, norm_type=1, routed_scaling_factor=2.5,
+              eps=1e-20)
+    fast = run_gpu_gating(x, dt, 8, bias=bias, out_flag=False, **kw)
+    full = run_gpu_gating(x, dt, 8, bias=bias, out_flag=True, **kw)
+    assert np.array_equal(fast["expert_idx"], full["expert_idx"])
+    assert np.array_equal(fast["y_out"].view(np.uint32), full["y_out"].view(np.uint32))
+    ref = gating.gating_topk(x, 8, bias=bias, **kw)
+    assert np.array_equal(fast["expert_idx"], ref["expert_idx"])
+    check_against_oracle(fast, ref, dt, kw, max_tie_rows=0)
+
+
 @pytest.mark.parametrize("norm_type", [0, 1, 2])
 def test_additional_bias_rows(norm_type):
     """The page's additional_bias case: every other token uses additional_bias instead of bias."""
