@@ -13,8 +13,9 @@
 // instructions per row:
 //  * one warp owns one row; lane l holds the contiguous run of experts [l*VPL, (l+1)*VPL) in
 //    registers, read with 16-, 8- or 4-byte loads where the row alignment allows;
-//  * scores become order-preserving 32-bit keys, so an arg-max over the row is two redux.sync
-//    instructions (the largest key, then the lowest expert index among the lanes holding it);
+//  * scores become order-preserving 32-bit keys, so an arg-max over the row is a redux.sync for
+//    the largest key and then the lowest lane holding it (a ballot where k is a compile-time
+//    constant, else a second redux.sync over the experts);
 //  * each lane caches its three best remaining candidates and rescans its run only when all are
 //    used, so a pick costs a handful of instructions instead of a pass over the row; the lane
 //    that gave a pick records it in shared memory, and lane i reads pick i at the end;
@@ -810,7 +811,7 @@ __device__ __forceinline__ bool logit_ranked_row(const Params &p, int t, int lan
     return true;
 }
 
-// Rank by logit for float32 x: the logits' 32-bit order keys go through the same two-redux picks
+// Rank by logit for float32 x: the logits' 32-bit order keys go through the same cached-key picks
 // as the full evaluation's scores, and only the chosen experts are scored.  The next lower float32
 // logit is one ulp down and almost always scores the same, so the boundary is checked against
 // the expert actually ranked next instead: the row takes k + 1 picks (k <= 31), and pick k - 1
