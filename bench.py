@@ -493,11 +493,27 @@ class RouteSetup:
                 raise RuntimeError(m.mrr_status_str(st))
 
 
+HOLD_CYCLES = 600_000   # about 0.3 ms at the 2070 MHz maximum SM clock
+
+
+def hold_stream(stream):
+    """Queue a bounded device-side sleep (HOLD_CYCLES SM cycles) on `stream`.  Placed after the
+    synchronize that opens a timed region and before its start event, it keeps the stream busy
+    while the host makes its first calls after the synchronize, so that the region begins with
+    the first launch already queued rather than waiting on the host (the blocking-kernel method
+    of GPU benchmark harnesses).  The sleep itself lies before the start event."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(HOLD_CYCLES)
+
+
 def timed_steps(setup, K, W, stream, dev, dist=None, clocks=None):
     """W warm-up steps, then exactly K steps between two CUDA events on the launching stream,
     bracketed by a barrier and a device synchronize on both sides.  The warm-up runs directly
-    before the timed region (nothing idles the GPU or the host in between).  An extra event after
-    the first timed step shows how long that step took from the start of the region.
+    before the timed region (nothing idles the GPU or the host in between), and hold_stream
+    queues a short device sleep ahead of the start event.  An extra event after the first timed
+    step shows how long that step took from the start of the region.
     Returns (region ms, first step us)."""
     import torch
 
@@ -511,6 +527,7 @@ def timed_steps(setup, K, W, stream, dev, dist=None, clocks=None):
     torch.cuda.synchronize(dev)
     if clocks is not None:
         clocks.t_start = time.time()
+    hold_stream(stream)
     # only our launches run on this stream between the two events, back to back
     t_begin.record(stream)
     for k in range(K):
@@ -651,7 +668,9 @@ def run_gpu(args):
                      "kernel": "mrr_push::push_kernel" if args.op == "push" else "mrr::reroute_kernel",
                      "bytes_per_launch": bytes_step,
                      "mean_launch_us": mean_launch_ms * 1e3,
-                     "timing": "CUDA events around the K back-to-back launches on the launching stream; per launch = region / K"},
+                     "timing": "CUDA events around the K back-to-back launches on the launching stream, a bounded "
+                               "device sleep queued ahead of the start event so that the first launch is "
+                               "already queued; per launch = region / K"},
         "cpu_baseline": cpu,
         "cpu_parallel": cpu_par,
         "timing_detail": detail,
@@ -949,6 +968,7 @@ def run_gating(args):
         dist.barrier()
     torch.cuda.synchronize(dev)
     clocks.t_start = time.time()
+    hold_stream(stream)
     a.record(stream)
     for i in range(K):
         launch(sets[i % R], stream)
