@@ -146,17 +146,42 @@ def gating_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_gating_traffic(config: int):
-    """DRAM bytes per launch of the gating kernel from its committed ncu summary, if current."""
+def profiled_gating_field(config: int, field: str):
+    """An integer field (e.g. DRAM bytes per launch) of the gating kernel's committed ncu summary
+    for workload `config`, if that summary was taken on the current kernel source."""
     try:
         text = open(os.path.join(ROOT, "profiles", GATING_PROFILES[config]), encoding="utf-8").read()
     except (OSError, KeyError):
         return None
     src = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
-    tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
-    if not src or not tr or src.group(1) != gating_source_hash():
+    val = re.search(field + r":\s*([0-9]+)", text)
+    if not src or not val or src.group(1) != gating_source_hash():
         return None
-    return int(tr.group(1))
+    return int(val.group(1))
+
+
+def profiled_gating_traffic(config: int):
+    """DRAM bytes per launch of the gating kernel from its committed ncu summary, if current."""
+    return profiled_gating_field(config, "traffic_bytes_per_launch")
+
+
+SM_COUNT = 152          # GB300: 2 dies x 76 SMs
+ISSUE_PER_SM = 4        # one warp instruction per cycle from each of an SM's 4 schedulers
+
+
+def gating_issue_roofline(config: int, mean_launch_us: float, clocks: dict):
+    """The gating kernel is bound by instruction issue, not HBM: its warp instructions per launch
+    (from the committed ncu summary, if current) over the launch time, against the GPU's issue
+    peak (SMs x 4 schedulers x the SM clock sampled during the run, else the 2070 MHz maximum)."""
+    inst = profiled_gating_field(config, "warp_instructions_per_launch")
+    if inst is None or mean_launch_us <= 0:
+        return None
+    mhz = clocks.get("sm_mhz") or 2070.0
+    peak = SM_COUNT * ISSUE_PER_SM * mhz * 1e6
+    achieved = inst / (mean_launch_us * 1e-6)
+    return {"bound": "issue", "achieved": achieved, "peak": peak, "unit": "warp instructions/s",
+            "frac": achieved / peak, "warp_instructions_per_launch": inst, "sm_mhz": mhz,
+            "source": "profiles/" + GATING_PROFILES[config]}
 
 
 class ClockSampler:
@@ -994,6 +1019,7 @@ def run_gating(args):
         cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": f"the first 256 token rows, {reps} runs in {el:.1f} s, single thread",
                "tokens_per_s": tok_s}
+    clock_summary = clocks.summary()
     if rank == 0:
         print(json.dumps({
             "metric": GATING_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
@@ -1007,7 +1033,8 @@ def run_gating(args):
                          "traffic": profiled_gating_traffic(args.config),
                          "kernel": "mrr_gate::gating_kernel", "bytes_per_launch": B,
                          "mean_launch_us": local_ms / K * 1e3},
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K, "clocks": clocks.summary()}), flush=True)
+            "issue_roofline": gating_issue_roofline(args.config, local_ms / K * 1e3, clock_summary),
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K, "clocks": clock_summary}), flush=True)
     if dist is not None:
         dist.destroy_process_group()
     return 0

@@ -1,5 +1,6 @@
 """CPU checks of bench.py's host logic: the multi-rank aggregation (max time over ranks, whole-job
-throughput) on two gloo ranks, the reference arm's JSON line, and the row sampler."""
+throughput) on two gloo ranks, the reference arm's JSON line, the row sampler, and the gating
+line's issue roofline."""
 import json
 import os
 import socket
@@ -79,3 +80,27 @@ def test_reference_arm_other_ranks_do_nothing(capsys, monkeypatch):
     monkeypatch.setenv("WORLD_SIZE", "2")
     assert bench.main(["--impl", "reference", "--steps", "5", "--warmup", "3"]) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_gating_issue_roofline_reads_a_current_summary_only(tmp_path, monkeypatch):
+    """The gating line's issue roofline takes the warp instructions per launch from the
+    workload's ncu summary only when the summary's source hash is the current one, and divides
+    them by the launch time against SMs x 4 schedulers x the sampled SM clock."""
+    (tmp_path / "profiles").mkdir()
+    name = bench.GATING_PROFILES[2]
+    (tmp_path / "profiles" / name).write_text(
+        "kernel_source_sha256: 0123abcd\ntraffic_bytes_per_launch: 1000\n"
+        "warp_instructions_per_launch: 7000000\n", encoding="utf-8")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "gating_source_hash", lambda: "0123abcd")
+    assert bench.profiled_gating_traffic(2) == 1000
+    r = bench.gating_issue_roofline(2, 10.0, {"sm_mhz": 2000.0})
+    assert r["bound"] == "issue" and r["warp_instructions_per_launch"] == 7000000
+    assert r["peak"] == pytest.approx(152 * 4 * 2000e6)
+    assert r["achieved"] == pytest.approx(7e6 / 10e-6)
+    assert r["frac"] == pytest.approx(7e11 / (152 * 4 * 2e9))
+    assert bench.gating_issue_roofline(2, 10.0, {"sm_mhz": None})["sm_mhz"] == 2070.0
+    assert bench.gating_issue_roofline(1, 10.0, {}) is None          # no summary for workload 1 here
+    monkeypatch.setattr(bench, "gating_source_hash", lambda: "ffff0000")
+    assert bench.gating_issue_roofline(2, 10.0, {"sm_mhz": 2000.0}) is None
+    assert bench.profiled_gating_traffic(2) is None
