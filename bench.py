@@ -88,6 +88,27 @@ def throughput_gbs(world: int, bytes_per_step: int, steps: int, elapsed_ms: floa
     return world * bytes_per_step * steps / (elapsed_ms * 1e-3) / 1e9
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    import platform
+    import subprocess
+
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo", encoding="utf-8"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -356,7 +377,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic", "config": config_dict(p, args.config, {"sample_rows": q.A}, args.op),
         "tokens_per_s": q.A * args.steps / el,
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "cpu": cpu_model(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -635,7 +656,7 @@ def run_gpu(args):
     cpu = cpu_par = None
     if rank == 0 and not args.no_cpu_baseline:
         gbs, reps, el = time_oracle(p, args.cpu_seconds, args.op)
-        cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "cpu": cpu_model(), "kind": "oracle",
                "sample": f"the full workload, {reps} runs in {el:.1f} s, single thread"}
         if args.op == "route":
             cpu_par = time_cpu_parallel(p, min(args.cpu_seconds, 10.0))
@@ -725,7 +746,7 @@ def time_cpu_parallel(p, budget_s: float):
         gbs, reps, el, threads, _ = pb.time_problem(p, budget_s)
     except Exception as e:  # a host without OpenMP: report, do not fail the bench line
         return {"value": None, "error": str(e)[:200]}
-    return {"value": gbs, "unit": "GB/s", "cores": threads,
+    return {"value": gbs, "unit": "GB/s", "cores": threads, "cpu": cpu_model(),
             "kind": "openmp blocks of per-segment memcpy (a plain parallel program, not the oracle)",
             "sample": f"the full workload, {reps} runs in {el:.1f} s"}
 
@@ -927,7 +948,8 @@ def run_gating_reference(args, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": gating_config_dict(w, args.config, {"sample_rows": rows}),
         "tokens_per_s": rows * args.steps / el,
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "cpu": cpu_model(), "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
     return 0
 
@@ -1016,7 +1038,7 @@ def run_gating(args):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         gbs, tok_s, reps, el = time_gating_oracle(w, min(args.cpu_seconds, 10.0))
-        cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "cpu": cpu_model(), "kind": "oracle",
                "sample": f"the first 256 token rows, {reps} runs in {el:.1f} s, single thread",
                "tokens_per_s": tok_s}
     clock_summary = clocks.summary()
