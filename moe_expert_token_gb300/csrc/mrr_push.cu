@@ -294,7 +294,7 @@ extern "C" mrr_status mrr_v2_push(const void *send_tokens, const void *send_scal
     p.idx_out = idx_out;
     p.out_rows = out_rows;
     p.status = static_cast<uint32_t *>(workspace);
-    // one warp per row in flight: enough CTAs to fill the SMs, never more than the rows need
+    // a warp per chunk of rows: enough CTAs to fill the SMs, never more than the rows need
     const int64_t want = (S + kWarps - 1) / kWarps;
     int64_t cap = (int64_t)sms * 3;  // three CTAs of 8 warps fit on an SM (80 registers)
     if (cap > kMaxGrid)
