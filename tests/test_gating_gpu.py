@@ -534,6 +534,38 @@ def _ordered(f32: np.ndarray) -> np.ndarray:
     return np.where(b < 0, -(b & 0x7FFFFFFF), b)
 
 
+@pytest.mark.parametrize("dt", ["float16", "bfloat16", "float32"])
+@pytest.mark.parametrize("grouped", [False, True])
+def test_infinite_logits_with_sigmoid(dt, grouped):
+    """Logits of +inf and -inf among finite ones, sigmoid scores: +inf scores 1 and -inf scores 0
+    (归一化公式), so the experts and weights are those of the oracle; equal scores (several +inf
+    logits, or a finite logit whose sigmoid rounds to 1) go to the lower expert.  Grouped: the
+    8-group top-8 shape with a bias (the specialised instance) and, with norm_out, the general
+    one, which must agree bit for bit.  Ungrouped: no bias, so rows are ranked by logit."""
+    rng = np.random.default_rng(7 + grouped)
+    T, e = 512, 256
+    x = as_dtype(rng.standard_normal((T, e)) * 3, dt)
+    x[rng.random((T, e)) < 0.05] = np.inf
+    x[rng.random((T, e)) < 0.05] = -np.inf
+    x[::9] = -np.inf                                # rows with every score 0 (plus the bias)
+    x[1::9, :40] = np.inf                           # rows whose best scores all tie at 1
+    if grouped:
+        bias = as_dtype(rng.random(e) * 0.1, dt)
+        kw = dict(k_group=4, group_count=8, group_select_mode=1, norm_type=1, routed_scaling_factor=2.5,
+                  eps=1e-20)
+        fast = run_gpu_gating(x, dt, 8, bias=bias, out_flag=False, **kw)
+        full = run_gpu_gating(x, dt, 8, bias=bias, out_flag=True, **kw)
+        assert np.array_equal(fast["expert_idx"], full["expert_idx"])
+        assert np.array_equal(fast["y_out"].view(np.uint32), full["y_out"].view(np.uint32))
+        ref = gating.gating_topk(x, 8, bias=bias, **kw)
+    else:
+        kw = dict(norm_type=1, eps=1e-6)
+        fast = run_gpu_gating(x, dt, 6, out_flag=False, **kw)
+        ref = gating.gating_topk(x, 6, **kw)
+    assert np.all(np.isfinite(fast["y_out"]))
+    check_against_oracle(fast, ref, dt, kw, x=x)
+
+
 @pytest.mark.parametrize("dt", ["float16", "bfloat16"])
 @pytest.mark.parametrize("norm_type,bound", [(1, 4), (2, 3)])
 def test_scores_of_every_16bit_logit(dt, norm_type, bound):
