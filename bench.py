@@ -136,10 +136,18 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def push_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in ("moe_expert_token_gb300/csrc/mrr_push.cu", "moe_expert_token_gb300/csrc/mrr_shape.h",
+                "moe_expert_token_gb300/csrc/ptx.cuh", "moe_expert_token_gb300/csrc/ws_layout.h"):
+        h.update(code_text(rel))
+    return h.hexdigest()[:16]
+
+
 def profiled_traffic(config: int, op: str = "route"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
     name = {"route": f"reroute_kernel_C{config}.md", "unroute": f"reroute_kernel_inverse_C{config}.md",
-            "multi": f"reroute_kernel_multi_C{config}.md"}.get(op)
+            "multi": f"reroute_kernel_multi_C{config}.md", "push": f"push_kernel_C{config}.md"}.get(op)
     if name is None:   # no committed summary for this op
         return None
     path = os.path.join(ROOT, "profiles", name)
@@ -149,7 +157,7 @@ def profiled_traffic(config: int, op: str = "route"):
         return None
     src = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
     tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
-    if not src or not tr or src.group(1) != kernel_source_hash():
+    if not src or not tr or src.group(1) != (push_source_hash() if op == "push" else kernel_source_hash()):
         return None
     return int(tr.group(1))
 
